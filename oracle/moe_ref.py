@@ -1,0 +1,357 @@
+"""Plain, slow CPU oracle of the single-GPU fused-MoE layer (test infrastructure).
+
+Only the tests, ``__graft_entry__.smoke()`` and the CPU-baseline leg of ``bench.py``
+may import or run anything in ``oracle/``.  The CUDA library never calls it and
+shares no code with it: no kernels, headers, constants or helpers.
+
+Arithmetic is float64 (torch CPU and numpy) unless the step fixes a narrower
+precision; every narrowing is written out where the step stores its result.
+
+The pages define the layer as a modular pipeline, prepare -> experts ->
+finalize, run on one device without dispatch or combine:
+
+* "[vLLM] MoE Oracle & Prepare/Finalize" blog, section "No DP/EP: the simplest
+  case" (the ``MoEPrepareAndFinalizeNoDPEPModular`` class): prepare multiplies a1
+  by the top-k weight when ``apply_router_weight_on_input`` (top-k must be 1),
+  then quantises the input; finalize hands the expert rows and top-k weights to
+  a weight-and-reduce step.
+* "Fused MoE Kernel Features" (vLLM design doc), section "Fused MoE Modular
+  All2All backends": prepare returns the quantised type, finalize takes and
+  returns the original activation type in the standard (token-major) format;
+  with no quantisation type the kernels run in bf16.  Section "Fused Experts
+  Kernels": the experts apply an activation between two GEMMs (SiLU-and-mul is
+  the default SwiGLU); quantisation format "G(128)" means one scale per token
+  per 128-channel block.
+* "[flashinfer] MoE Finalize + AllReduce fusion" page, introduction: finalize
+  multiplies the top-k expert rows by their routing scales and sums them,
+  optionally adds the shared-expert row, then (after the all-reduce, absent on
+  one GPU) adds the residual, applies RMSNorm and optionally packs NVFP4.
+
+Where the pages leave a step open (router, alignment, scale formats, finalize
+order) each function below states the plain reading it takes.
+
+Parity status: every function here is pinned by ``tests/test_oracle_*.py``
+against invariants, closed forms, brute force or library routines.  The whole
+layer composed of them has no printed worked example on the pages, so parity of
+the composition rests on the per-step pins.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass
+from typing import Optional
+
+import numpy as np
+import torch
+
+from . import codecs
+
+F64 = torch.float64
+AMAX_FLOOR = float(np.float32(1e-10))  # the amax clamp, as an fp32 number
+
+
+def _np(t) -> np.ndarray:
+    if isinstance(t, torch.Tensor):
+        return t.detach().cpu().to(torch.float64).numpy() if t.is_floating_point() else t.detach().cpu().numpy()
+    return np.asarray(t)
+
+
+def to_bf16_tensor(x64: np.ndarray) -> torch.Tensor:
+    """fp64 array -> bf16 torch tensor with a single round-to-nearest-even step."""
+    r = codecs.round_bf16(x64)
+    return torch.from_numpy(np.ascontiguousarray(r)).to(torch.float32).to(torch.bfloat16)  # exact
+
+
+# =========================================================================== route
+def route_softmax_renorm(logits: torch.Tensor, top_k: int):
+    """Top-k routing with softmax weights renormalised over the selected experts.
+
+    The pages take ``topk_ids``/``topk_weights`` as given (prepare and finalize
+    arguments in the "No DP/EP" listing); the router is read as: rank experts
+    by the fp32 logit, larger first, equal logits to the lower expert index; weight_j = exp(l_j - l_max) / sum over the selected
+    experts of exp(l_i - l_max), which equals the full softmax renormalised over
+    the top-k.  Weights are computed in fp64 and stored as fp32.
+    """
+    L = _np(logits)  # fp32 values held exactly in fp64
+    T, E = L.shape
+    assert 1 <= top_k <= E
+    ids = np.empty((T, top_k), dtype=np.int32)
+    w = np.empty((T, top_k), dtype=np.float32)
+    for t in range(T):
+        order = sorted(range(E), key=lambda i: (-L[t, i], i))[:top_k]
+        ids[t] = order
+        sel = L[t, order]
+        e = np.exp(sel - sel[0])  # sel[0] is the largest selected logit
+        w[t] = (e / e.sum()).astype(np.float32)
+    return torch.from_numpy(ids), torch.from_numpy(w)
+
+
+def route_sigmoid_top1(logits: torch.Tensor):
+    """Top-1 routing with weight sigmoid(logit) (Llama-4-like router).
+
+    The "Fused MoE Kernel Features" page notes that Llama-type models with
+    top-k == 1 apply the top-k weight to the input activation; the weight
+    itself is read as sigmoid of the selected logit, not renormalised.
+    Argmax ties go to the lower expert index.
+    """
+    L = _np(logits)
+    T, E = L.shape
+    ids = np.empty((T, 1), dtype=np.int32)
+    w = np.empty((T, 1), dtype=np.float32)
+    for t in range(T):
+        best = 0
+        for i in range(1, E):
+            if L[t, i] > L[t, best]:
+                best = i
+        ids[t, 0] = best
+        w[t, 0] = np.float32(1.0 / (1.0 + math.exp(-L[t, best])))
+    return torch.from_numpy(ids), torch.from_numpy(w)
+
+
+# =========================================================================== align
+@dataclass
+class Alignment:
+    expert_offsets: torch.Tensor  # [E+1] int32, offsets[E] = S = T*k
+    sorted_slot: torch.Tensor     # [S] int32, value f = t*k + j
+    inv_slot: torch.Tensor        # [S] int32, inv_slot[sorted_slot[p]] = p
+    tile_map: torch.Tensor        # [num_tiles, 2] int32: (expert, first row)
+    num_tiles: int
+
+
+def align(topk_ids: torch.Tensor, num_experts: int, block_m: int) -> Alignment:
+    """Per-expert grouping of the token slots (the "alignment and permutation").
+
+    Reading: slot f = t*k + j is the j-th choice of token t; the
+    slots are sorted by the key (expert id, f), so each expert's rows are
+    contiguous and in ascending slot order; expert_offsets is the exclusive
+    prefix sum of the per-expert counts (unpadded, so offsets[E] = T*k); the
+    tile map lists, expert by expert, the first row of each block_m-row tile.
+    """
+    flat = [int(v) for v in _np(topk_ids).reshape(-1)]
+    S = len(flat)
+    order = sorted(range(S), key=lambda f: (flat[f], f))
+    counts = [0] * num_experts
+    for e in flat:
+        counts[e] += 1
+    offsets = [0]
+    for c in counts:
+        offsets.append(offsets[-1] + c)
+    inv = [0] * S
+    for p, f in enumerate(order):
+        inv[f] = p
+    tiles = []
+    for e in range(num_experts):
+        r = offsets[e]
+        while r < offsets[e + 1]:
+            tiles.append((e, r))
+            r += block_m
+    tm = torch.tensor(tiles, dtype=torch.int32).reshape(-1, 2)
+    return Alignment(torch.tensor(offsets, dtype=torch.int32), torch.tensor(order, dtype=torch.int32),
+                     torch.tensor(inv, dtype=torch.int32), tm, len(tiles))
+
+
+# =========================================================================== prepare
+def quantize_fp8_g128(x64: np.ndarray, group: int = 128):
+    """Per-row, per-128-column fp8 E4M3 quantisation ("G(128)" format).
+
+    Reading: for each row and each 128-column group,
+    s = fp32(max(amax, fp32(1e-10)) / 448) and q = e4m3_rn_satfinite(fp32(x / s)).
+    The scale is stored as the fp32 value used for dequantisation, x ~ q * s.
+    x must hold values exactly representable in fp32 (bf16 inputs are).
+    Returns (codes uint8 [R, C], scales fp32 [R, C/128]).
+    """
+    R, C = x64.shape
+    assert C % group == 0
+    g = x64.reshape(R, C // group, group)
+    amax = np.abs(g).max(axis=2)
+    s = codecs.round_fp32(np.maximum(amax, AMAX_FLOOR) / 448.0)  # IEEE fp32 division
+    ratio = codecs.round_fp32(g / s[:, :, None])               # IEEE fp32 division
+    q = codecs.e4m3_encode(ratio).reshape(R, C)
+    return q, s.astype(np.float32)
+
+
+def dequant_fp8_g128(q: np.ndarray, s: np.ndarray, group: int = 128) -> np.ndarray:
+    R, C = q.shape
+    return (codecs.e4m3_decode(q).reshape(R, C // group, group) * s.astype(np.float64)[:, :, None]).reshape(R, C)
+
+
+def prepare(a1: torch.Tensor, topk_weights: torch.Tensor, apply_router_weight_on_input: bool, quant: str):
+    """Prepare step of the no-DP/EP prepare/finalize ("[vLLM] MoE Oracle &
+    Prepare/Finalize" blog, "No DP/EP" section).
+
+    With ``apply_router_weight_on_input`` (allowed only for top-k == 1) the
+    input is first multiplied by the top-k weight cast to the activation type:
+    a1 = bf16(a1 * bf16(w)).  Then the input is quantised: ``quant == 'bf16'``
+    is "no quantisation type", a passthrough; ``quant == 'fp8'`` is the
+    per-token G(128) E4M3 format.  Returns (a1q, a1q_scale or None) with a1q a
+    bf16 tensor or a uint8 tensor of E4M3 codes.
+    """
+    x = _np(a1)
+    if apply_router_weight_on_input:
+        w = _np(topk_weights)
+        assert w.shape[1] == 1, "apply_router_weight_on_input needs top_k == 1"
+        wb = codecs.round_bf16(w[:, 0])
+        x = codecs.round_bf16(x * wb[:, None])
+    if quant == "bf16":
+        return to_bf16_tensor(x), None
+    if quant == "fp8":
+        q, s = quantize_fp8_g128(x)
+        return torch.from_numpy(q), torch.from_numpy(s)
+    raise ValueError(quant)
+
+
+# =========================================================================== experts
+def dequant_weight_block(w_codes: np.ndarray, w_scale: np.ndarray, block: int = 128) -> np.ndarray:
+    """[N, K] E4M3 codes with [N/128, K/128] fp32 block scales -> fp64 [N, K]."""
+    N, K = w_codes.shape
+    v = codecs.e4m3_decode(w_codes)
+    return v * np.repeat(np.repeat(w_scale.astype(np.float64), block, axis=0), block, axis=1)[:N, :K]
+
+
+def silu_and_mul(gu: torch.Tensor) -> torch.Tensor:
+    """act(x) = silu(x[:, :I]) * x[:, I:], silu(g) = g / (1 + exp(-g)).
+
+    The "Fused Experts Kernels" table names SiLU (the SwiGLU gate) as the
+    activation between the two expert GEMMs; the gate half comes first."""
+    I = gu.shape[1] // 2
+    g, u = gu[:, :I], gu[:, I:]
+    return g / (1.0 + torch.exp(-g)) * u
+
+
+def expert_rows(A64: torch.Tensor, W13: torch.Tensor, W2: torch.Tensor, quant: str) -> torch.Tensor:
+    """One expert on a block of (already dequantised) input rows.
+
+    g, u = A W13[:I]^T, A W13[I:]^T (fp64); h = silu(g) * u, stored the way the
+    intermediate is stored (bf16, or re-quantised to fp8 G(128) when the
+    activations are fp8); y = h W2^T in fp64, stored bf16.  Returns fp64 values
+    of the stored bf16 y."""
+    h = silu_and_mul(A64 @ W13.T)
+    hn = h.numpy()
+    if quant == "bf16":
+        h_st = codecs.round_bf16(hn)
+    else:
+        q, s = quantize_fp8_g128(codecs.round_fp32(hn))
+        h_st = dequant_fp8_g128(q, s)
+    y = torch.from_numpy(h_st) @ W2.T
+    return torch.from_numpy(codecs.round_bf16(y.numpy()))
+
+
+def _weights64(w, w_scale, e, quant):
+    if quant == "bf16":
+        return torch.from_numpy(_np(w[e]))
+    return torch.from_numpy(dequant_weight_block(_np(w[e]).astype(np.uint8), _np(w_scale[e])))
+
+
+def _act64(a1q, a1q_scale, rows, quant):
+    if quant == "bf16":
+        return torch.from_numpy(_np(a1q)[rows])
+    return torch.from_numpy(dequant_fp8_g128(_np(a1q)[rows].astype(np.uint8), _np(a1q_scale)[rows]))
+
+
+def experts(a1q, a1q_scale, w13, w13_scale, w2, w2_scale, al: Alignment, top_k: int, quant: str) -> torch.Tensor:
+    """Grouped expert computation: for every expert e and every sorted row
+    p in [offsets[e], offsets[e+1]), slot f = sorted_slot[p] of token t = f // k
+    gets y[f] = expert_e(a1q[t]).  Output: the unweighted expert rows in
+    token-major order [T*k, H] (fp64 holding bf16 values), the layout finalize
+    takes ("fused_expert_output" in the "No DP/EP" listing)."""
+    offs = _np(al.expert_offsets)
+    order = _np(al.sorted_slot)
+    S = int(offs[-1])
+    H = a1q.shape[1]
+    y = torch.zeros((S, H), dtype=F64)
+    for e in range(len(offs) - 1):
+        p0, p1 = int(offs[e]), int(offs[e + 1])
+        if p0 == p1:
+            continue
+        slots = order[p0:p1]
+        A = _act64(a1q, a1q_scale, slots // top_k, quant)
+        y[torch.from_numpy(slots.astype(np.int64))] = expert_rows(
+            A, _weights64(w13, w13_scale, e, quant), _weights64(w2, w2_scale, e, quant), quant)
+    return y
+
+
+def token_expert_rows(a1q, a1q_scale, w13, w13_scale, w2, w2_scale, topk_ids, t: int, quant: str) -> torch.Tensor:
+    """The k expert rows of one token, y[t*k + j] for j < k (used to check
+    sampled tokens of full-size layers one by one)."""
+    ids = _np(topk_ids)[t]
+    A = _act64(a1q, a1q_scale, np.array([t]), quant)
+    return torch.cat([expert_rows(A, _weights64(w13, w13_scale, int(e), quant),
+                                  _weights64(w2, w2_scale, int(e), quant), quant) for e in ids], 0)
+
+
+def dense_mlp(x: torch.Tensor, w13: torch.Tensor, w2: torch.Tensor) -> torch.Tensor:
+    """Shared expert: one SwiGLU MLP over all tokens on the unweighted bf16 a1
+    (the optional shared-expert row of the flashinfer finalize page).  Output
+    fp64 holding bf16 values."""
+    return expert_rows(torch.from_numpy(_np(x)), torch.from_numpy(_np(w13)), torch.from_numpy(_np(w2)), "bf16")
+
+
+# =========================================================================== finalize
+def nvfp4_quantize(x64: np.ndarray, global_scale: float):
+    """NVFP4 packing of rows of x: 16-element groups, each with one E4M3 scale.
+
+    Reading: sf = e4m3_rn_satfinite(amax / (6 g)); codes
+    q_i = e2m1_rn_satfinite(x_i / (sf g)) (q = 0 when sf = 0); element 2i in
+    the low nibble.  Returns (packed uint8 [R, C/2], scale codes uint8 [R, C/16])."""
+    R, C = x64.shape
+    g = x64.reshape(R, C // 16, 16)
+    amax = np.abs(g).max(axis=2)
+    sf_code = codecs.e4m3_encode(amax / (6.0 * global_scale))
+    sf = codecs.e4m3_decode(sf_code)
+    denom = (sf * global_scale)[:, :, None]
+    with np.errstate(divide="ignore", invalid="ignore"):
+        ratio = np.where(denom > 0, g / np.where(denom > 0, denom, 1.0), 0.0)
+    codes = codecs.e2m1_encode(ratio).reshape(R, C)
+    packed = (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)
+    return packed, sf_code
+
+
+def nvfp4_dequantize(packed: np.ndarray, sf_code: np.ndarray, global_scale: float) -> np.ndarray:
+    R, Ch = packed.shape
+    codes = np.empty((R, Ch * 2), dtype=np.uint8)
+    codes[:, 0::2] = packed & 0xF
+    codes[:, 1::2] = packed >> 4
+    v = codecs.e2m1_decode(codes).reshape(R, -1, 16)
+    return (v * (codecs.e4m3_decode(sf_code) * global_scale)[:, :, None]).reshape(R, Ch * 2)
+
+
+@dataclass
+class FinalizeOut:
+    out: np.ndarray                      # fp64 unrounded output (after RMSNorm when given)
+    out_bf16: torch.Tensor               # bf16 rounding of `out`
+    residual_out: torch.Tensor           # bf16(sum before the norm)
+    nvfp4: Optional[tuple] = None        # (packed, scale codes) when requested
+
+
+def finalize(fused_expert_output, topk_weights, top_k: int, apply_router_weight_on_input: bool,
+             shared=None, residual=None, rms_weight=None, eps: float = 1e-6,
+             nvfp4_global_scale: Optional[float] = None) -> FinalizeOut:
+    """Finalize: top-k weight-and-reduce, + shared row, + residual, RMSNorm, NVFP4.
+
+    o_t = sum_j w_tj * y[t*k + j] (the weights are skipped when they were
+    applied on the input) + shared_t + residual_t, in fp64.  Then, when an
+    RMSNorm weight is given, o_t <- o_t / sqrt(mean_h(o_t^2) + eps) * gamma.
+    The order follows the flashinfer finalize page's introduction with its
+    all-reduce step removed (one GPU).  residual_out is bf16 of the sum before
+    the norm.  NVFP4 packs the unrounded normalised values."""
+    y = _np(fused_expert_output)
+    S, H = y.shape
+    T = S // top_k
+    y = y.reshape(T, top_k, H)
+    if apply_router_weight_on_input:
+        o = y.sum(axis=1)
+    else:
+        w = _np(topk_weights).reshape(T, top_k)
+        o = (w[:, :, None] * y).sum(axis=1)
+    if shared is not None:
+        o = o + _np(shared)
+    if residual is not None:
+        o = o + _np(residual)
+    res_out = to_bf16_tensor(o)
+    if rms_weight is not None:
+        gmm = _np(rms_weight)
+        o = o / np.sqrt((o * o).mean(axis=1, keepdims=True) + eps) * gmm[None, :]
+    fo = FinalizeOut(out=o, out_bf16=to_bf16_tensor(o), residual_out=res_out)
+    if nvfp4_global_scale is not None:
+        fo.nvfp4 = nvfp4_quantize(o, nvfp4_global_scale)
+    return fo
