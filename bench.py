@@ -1,0 +1,411 @@
+#!/usr/bin/env python3
+"""Throughput of one fused-MoE layer step on GB300 (tokens/s), with roofline.
+
+A step is the whole hot path on one batch of synthetic input already resident
+in HBM: moe_route -> moe_align -> moe_prepare -> moe_experts (+ the shared
+expert when the layer has one) -> moe_finalize, all through the C ABI on one
+stream.  Default workload: the Mixtral-8x7B-like layer (T=512, H=4096,
+I=14336, E=8, top-2, bf16), whose 2.8 GB of expert weights stream from HBM
+every step (far more than the 129 MB L2, so no flush is needed).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+With N > 1 (launched by torch.distributed.run) every rank runs an independent
+replica of the layer on its own GPU -- the layer has no exchange step on one
+node -- and rank 0 prints the line: value = tokens of all ranks / max time.
+
+`--impl reference` times the CPU oracle on the host cores instead (bounded
+token samples per step); it is the slow, plain restatement of the method that
+the GPU path is checked against, not a tuned baseline.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from mixture_experts_layer_tokens_gb300.inputs import CONFIGS, make_inputs  # noqa: E402
+
+METRIC = "MoE-layer tokens/s (fraction of GB300 HBM/tensor roofline in `roofline`), 1 GPU"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default="mixtral", choices=sorted(CONFIGS))
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+# ------------------------------------------------------------------ roofline accounting
+def experts_algorithmic(cfg, counts):
+    """Bytes and FLOPs one expert pass must move/do: the weights of the experts
+    that received tokens (+ fp8 block scales), the activations read once, the
+    intermediate h written and read once, the output rows written once; FLOPs
+    6 H I per token slot (no padded rows)."""
+    esz = 1 if cfg.quant == "fp8" else 2
+    touched = int((counts > 0).sum())
+    w = touched * 3 * cfg.H * cfg.I * esz
+    if cfg.quant == "fp8":
+        w += touched * 3 * (cfg.H // 128) * (cfg.I // 128) * 4
+    S = cfg.T * cfg.top_k
+    act = cfg.T * cfg.H * esz + 2 * S * cfg.I * esz + S * cfg.H * 2
+    if cfg.quant == "fp8":
+        act += cfg.T * (cfg.H // 128) * 4 + 2 * S * (cfg.I // 128) * 4
+    flops = 6.0 * S * cfg.H * cfg.I
+    return w + act, flops
+
+
+def finalize_algorithmic(cfg, nvfp4):
+    T, H, k = cfg.T, cfg.H, cfg.top_k
+    rd = T * k * H * 2 + 2 * T * H * 2 + H * 2 + T * k * 4
+    wr = T * H // 2 + T * H // 16 if nvfp4 else T * H * 2
+    return rd + wr
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """Polls the SM clock and the clock-event reasons of one GPU through NVML
+    (read-only queries) every ~2 ms from a thread, for the duration of a timed
+    region."""
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, device_index):
+        import ctypes
+        import threading
+        self.samples, self.max_mhz, self.err = [], None, None
+        self._stop = threading.Event()
+        try:
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                raise RuntimeError("nvmlInit failed")
+            h = ctypes.c_void_p()
+            props = torch.cuda.get_device_properties(device_index)
+            bus = f"{props.pci_domain_id:08x}:{props.pci_bus_id:02x}:{props.pci_device_id:02x}.0".encode()
+            if nv.nvmlDeviceGetHandleByPciBusId_v2(bus, ctypes.byref(h)) != 0:
+                if nv.nvmlDeviceGetHandleByIndex_v2(0, ctypes.byref(h)) != 0:
+                    raise RuntimeError("no NVML handle")
+            mx = ctypes.c_uint()
+            if nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:  # 1 = SM clock
+                self.max_mhz = mx.value
+            reasons_fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                nv.nvmlDeviceGetCurrentClocksThrottleReasons
+            self.nv, self.h, self.reasons_fn = nv, h, reasons_fn
+            self.thread = threading.Thread(target=self._run, daemon=True)
+            self.thread.start()
+        except Exception as e:  # no NVML on this machine
+            self.err, self.thread = str(e), None
+
+    def _run(self):
+        import ctypes
+        c, r = ctypes.c_uint(), ctypes.c_ulonglong()
+        while not self._stop.is_set():
+            ok = self.nv.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(c)) == 0
+            okr = self.reasons_fn(self.h, ctypes.byref(r)) == 0
+            if ok:
+                self.samples.append((c.value, r.value if okr else 0))
+            time.sleep(0.002)
+
+    def stop(self):
+        if self.thread is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "note": self.err}
+        self._stop.set()
+        self.thread.join()
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [], "samples": 0}
+        mask = 0
+        for _, r in self.samples:
+            mask |= r
+        return {"sm_mhz": statistics.median(c for c, _ in self.samples), "sm_max_mhz": self.max_mhz,
+                "reasons": sorted(n for b, n in self.REASONS.items() if mask & b), "samples": len(self.samples)}
+
+
+# ------------------------------------------------------------------ oracle baseline
+def oracle_tokens_seconds(inp, tokens):
+    """Time the plain CPU oracle on the given tokens of the workload (fp64)."""
+    from oracle import moe_ref
+    cfg = inp.cfg
+    t0 = time.perf_counter()
+    logits = inp.logits[tokens].cpu()
+    if cfg.scoring == "sigmoid":
+        ids, w = moe_ref.route_sigmoid_top1(logits)
+    else:
+        ids, w = moe_ref.route_softmax_renorm(logits, cfg.top_k)
+    a1 = inp.a1[tokens].cpu()
+    a1q, sc = moe_ref.prepare(a1, w, cfg.weight_on_input, cfg.quant)
+    y = torch.cat([moe_ref.token_expert_rows(a1q, sc, inp.w13, inp.w13_scale, inp.w2, inp.w2_scale, ids, i,
+                                             cfg.quant) for i in range(len(tokens))], 0)
+    shared = moe_ref.dense_mlp(a1, inp.shared_w13[0], inp.shared_w2[0]) if cfg.shared_I else None
+    res = inp.residual[tokens].cpu() if inp.residual is not None else None
+    moe_ref.finalize(y, w, cfg.top_k, cfg.weight_on_input, shared=shared, residual=res,
+                     rms_weight=None if inp.rms_weight is None else inp.rms_weight.cpu())
+    return time.perf_counter() - t0
+
+
+def set_cpu_threads():
+    try:
+        n = len(os.sched_getaffinity(0))
+    except Exception:
+        n = os.cpu_count() or 1
+    torch.set_num_threads(n)
+    return n
+
+
+def cpu_model():
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return "unknown"
+
+
+# ------------------------------------------------------------------ distributed plumbing
+def dist_setup(args):
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() and args.impl == "gb300" else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return ws, rank, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, ws, device):
+    if ws == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ reference arm
+def run_reference(args, ws, rank):
+    if rank != 0:
+        return
+    cfg = CONFIGS[args.workload]
+    cores = set_cpu_threads()
+    inp = make_inputs(cfg, device="cpu")
+    per_step = 1
+    times = []
+    for i in range(args.warmup + args.steps):
+        tok = [(i * 7) % cfg.T]
+        dt = oracle_tokens_seconds(inp, tok)
+        if i >= args.warmup:
+            times.append(dt)
+    total = sum(times)
+    value = per_step * len(times) / total
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / len(times),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": cfg.description, "T": cfg.T, "H": cfg.H, "I": cfg.I, "E": cfg.E,
+                       "top_k": cfg.top_k},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                             "sample": f"{per_step} token of the {cfg.name} workload per step (fp64 oracle), "
+                                       f"CPU {cpu_model()}"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ GPU arm
+def run_gpu(args, ws, rank, local):
+    from mixture_experts_layer_tokens_gb300 import build as _b
+    from mixture_experts_layer_tokens_gb300 import moe
+    from mixture_experts_layer_tokens_gb300.layer import FinalizeStep, MoELayer
+
+    if rank == 0:
+        _b.build()
+    barrier(ws)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    cfg = CONFIGS[args.workload]
+    inp = make_inputs(cfg, seed=rank, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    hbm_peak, bf16_peak, peak_kind = peaks()
+
+    with torch.cuda.stream(stream):
+        if cfg.finalize_only:
+            step_obj = FinalizeStep(inp)
+            step_obj.weights()
+
+            def step():
+                step_obj.weights()
+                step_obj.finalize(True)
+            launches_per_step = 2
+        else:
+            layer = MoELayer(inp, stream=stream)
+
+            def step():
+                layer.forward(inp.logits, inp.a1)
+            # route 1, align 3, prepare 0/1, experts 3 (gather, GEMM1, GEMM2), finalize 1,
+            # shared expert 2 (identity permutation: no gather)
+            launches_per_step = 1 + 3 + (0 if layer.passthrough else 1) + 3 + 1 + (2 if cfg.shared_I else 0)
+        for _ in range(args.warmup):
+            step()
+        torch.cuda.synchronize(dev)
+        assert moe.moe_device_status() == moe.MOE_OK
+
+        # ---- timed region: K steps, events on the launching stream
+        clocks = ClockSampler(local) if rank == 0 else None
+        barrier(ws)
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(ws)
+        clk = clocks.stop() if clocks else None
+        ms = e0.elapsed_time(e1) / args.steps
+        ms_max = max_over_ranks(ms, ws, dev)
+        value = ws * cfg.T / (ms_max * 1e-3)
+
+        # ---- dominant unit: time it inside steps with events around its call
+        if cfg.finalize_only:
+            dom_name = "moe_finalize (NVFP4 out)"
+            nbytes = finalize_algorithmic(cfg, True)
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(args.steps)]
+            for a, b in ev:
+                step_obj.weights()
+                a.record(stream)
+                step_obj.finalize(True)
+                b.record(stream)
+            torch.cuda.synchronize(dev)
+            flops = 0.0
+        else:
+            dom_name = "moe_experts (gather + GEMM1 SiLU + GEMM2 scatter)"
+            counts = torch.diff(layer.al.expert_offsets).cpu().numpy()
+            nbytes, flops = experts_algorithmic(cfg, counts)
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(args.steps)]
+            for a, b in ev:
+                moe.moe_route(inp.logits, cfg.top_k, layer.scoring, layer.topk_ids, layer.topk_weights)
+                moe.moe_align(layer.topk_ids, cfg.E, out=layer.al)
+                a1q = inp.a1 if layer.passthrough else layer.a1q
+                if not layer.passthrough:
+                    moe.moe_prepare(inp.a1, layer.topk_weights, cfg.top_k, cfg.weight_on_input, cfg.quant,
+                                    layer.a1q, layer.a1q_scale)
+                a.record(stream)
+                moe.moe_experts(a1q, layer.a1q_scale, inp.w13, inp.w13_scale, inp.w2, inp.w2_scale, layer.al,
+                                cfg.quant, out=layer.y, ws=layer.ws)
+                b.record(stream)
+            torch.cuda.synchronize(dev)
+        dom_ms = statistics.median([a.elapsed_time(b) for a, b in ev])
+        achieved = nbytes / (dom_ms * 1e-3) / 1e9
+        roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
+                    "frac": round(achieved / hbm_peak, 4), "traffic": None, "kernel": dom_name,
+                    "algorithmic_bytes": int(nbytes), "ms": round(dom_ms, 4), "peak_kind": peak_kind}
+        if flops:
+            roofline["tflops"] = round(flops / (dom_ms * 1e-3) / 1e12, 1)
+            roofline["tensor_frac_of_bf16_peak"] = round(flops / (dom_ms * 1e-3) / 1e12 / bf16_peak, 4)
+
+        # ---- end to end through the public API with host buffers
+        if cfg.finalize_only:
+            e2e = None
+        else:
+            h_logits = inp.logits.cpu().pin_memory()
+            h_a1 = inp.a1.cpu().pin_memory()
+            h_out = torch.empty((cfg.T, cfg.H), dtype=torch.bfloat16).pin_memory()
+            d_logits = torch.empty_like(inp.logits)
+            d_a1 = torch.empty_like(inp.a1)
+
+            def e2e_step():
+                d_logits.copy_(h_logits, non_blocking=True)
+                d_a1.copy_(h_a1, non_blocking=True)
+                out = layer.forward(d_logits, d_a1)
+                h_out.copy_(out, non_blocking=True)
+            for _ in range(args.warmup):
+                e2e_step()
+            torch.cuda.synchronize(dev)
+            barrier(ws)
+            t0 = time.perf_counter()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for _ in range(args.steps):
+                e2e_step()
+            b.record(stream)
+            torch.cuda.synchronize(dev)
+            wall = (time.perf_counter() - t0) / args.steps
+            ems = max(a.elapsed_time(b) / args.steps, wall * 1e3)
+            ems = max_over_ranks(ems, ws, dev)
+            e2e = {"value": ws * cfg.T / (ems * 1e-3), "unit": "tokens/s",
+                   "h2d_bytes_per_step": h_logits.numel() * 4 + h_a1.numel() * 2,
+                   "d2h_bytes_per_step": h_out.numel() * 2}
+
+    if rank != 0:
+        return
+    cpu = None
+    if not args.no_cpu_baseline and ws == 1 and not cfg.finalize_only:
+        cores = set_cpu_threads()
+        # tokens one at a time until about 10 s of oracle work (at least 2 tokens)
+        dt, n = 0.0, 0
+        while (dt < 10.0 or n < 2) and n < cfg.T:
+            dt += oracle_tokens_seconds(inp, [(n * 37) % cfg.T])
+            n += 1
+        cpu = {"value": n / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+               "sample": f"{n} tokens of the {cfg.name} workload, one at a time, through the fp64 oracle "
+                         f"({dt:.1f} s), CPU {cpu_model()}"}
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "fp8" if cfg.quant == "fp8" else "bf16", "data": "synthetic",
+            "config": {"workload": cfg.description, "T": cfg.T, "H": cfg.H, "I": cfg.I, "E": cfg.E,
+                       "top_k": cfg.top_k, "parallelism": f"replicas{ws}",
+                       "l2": "no flush: each step streams the expert weights (larger than the 129 MB L2)"
+                       if not cfg.finalize_only else "inputs smaller than L2 (finalize-only workload)"},
+            "roofline": roofline, "cpu_baseline": cpu, "clocks": clk, "e2e": e2e,
+            "gpu_launches": launches_per_step * args.steps}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    ws, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        run_reference(args, ws, rank)
+    else:
+        run_gpu(args, ws, rank, local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

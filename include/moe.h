@@ -1,0 +1,203 @@
+/*
+ * moe.h -- C ABI of the single-GPU fused mixture-of-experts layer (GB300, sm_103a).
+ *
+ * The layer is the modular no-DP/EP pipeline described by the pages:
+ *
+ *   moe_route    -> topk_ids, topk_weights
+ *   moe_align    -> per-expert grouping of the (token, choice) slots
+ *   moe_prepare  -> a1q (+ a1q_scale)                         ("prepare")
+ *   moe_experts  -> fused_expert_output, unweighted rows      ("experts")
+ *   moe_finalize -> output (+ residual_out)                   ("finalize")
+ *
+ * Sources: "[vLLM] MoE Oracle & Prepare/Finalize" blog, section "No DP/EP: the
+ * simplest case" (prepare and finalize of MoEPrepareAndFinalizeNoDPEPModular);
+ * "Fused MoE Kernel Features" (vLLM design doc), sections "Fused MoE Modular
+ * All2All backends" and "Fused Experts Kernels"; "[flashinfer] MoE Finalize +
+ * AllReduce fusion" page, introduction (finalize + shared row + residual +
+ * RMSNorm + optional NVFP4 output).
+ *
+ * Conventions shared by every call
+ *  - Every pointer argument is a DEVICE pointer on the current CUDA device,
+ *    16-byte aligned, unless its comment says otherwise.  The caller owns and
+ *    allocates every buffer, workspaces included; the library allocates no
+ *    device memory.
+ *  - Every call is asynchronous on `stream` (a cudaStream_t; NULL is the legacy
+ *    default stream) and never synchronises.
+ *  - Arguments are checked on the host before any launch; a bad argument
+ *    returns an error status and launches nothing.  A launch failure returns
+ *    MOE_ERR_CUDA.  No call aborts or throws.
+ *  - Slot f = t * top_k + j names the j-th expert choice of token t.
+ *  - Sizes are element counts; T (tokens) may be 0, in which case the call
+ *    does nothing and returns MOE_OK.
+ */
+#ifndef MOE_H_
+#define MOE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *moe_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,  /* null pointer, bad size or misaligned pointer   */
+  MOE_ERR_UNSUPPORTED = 2,  /* valid request this library does not implement   */
+  MOE_ERR_WORKSPACE = 3,    /* workspace missing or smaller than required      */
+  MOE_ERR_CUDA = 4,         /* a CUDA runtime/driver call or launch failed      */
+  MOE_ERR_TIMEOUT = 5       /* a device-side wait gave up (see moe_device_status) */
+} moe_status_t;
+
+typedef enum {
+  MOE_DT_BF16 = 0,
+  MOE_DT_FP8_E4M3 = 1, /* OCP E4M3 ("e4m3fn"), saturating                    */
+  MOE_DT_NVFP4 = 2,    /* E2M1 pairs + one E4M3 scale per 16 elements        */
+  MOE_DT_FP32 = 3
+} moe_dtype_t;
+
+typedef enum {
+  MOE_SCORING_SOFTMAX_RENORM = 0, /* softmax over the chosen top-k logits     */
+  MOE_SCORING_SIGMOID = 1         /* top-1, weight = sigmoid(logit)           */
+} moe_scoring_t;
+
+/* Quantisation of the expert inputs and weights.
+ *   bf16:  {MOE_DT_BF16, 0, MOE_DT_BF16, 0, 0}   -- "no quantisation type"
+ *   fp8:   {MOE_DT_FP8_E4M3, 128, MOE_DT_FP8_E4M3, 128, 128}
+ *          activations: one fp32 scale per token per 128 channels ("G(128)");
+ *          weights: one fp32 scale per 128x128 block.
+ * Other combinations return MOE_ERR_UNSUPPORTED. */
+typedef struct {
+  moe_dtype_t act;
+  int act_group;
+  moe_dtype_t weight;
+  int w_block_n;
+  int w_block_k;
+} moe_quant_config;
+
+/* Rows per expert tile in the tile map that moe_experts consumes. */
+#define MOE_BLOCK_M 128
+
+/* ------------------------------------------------------------------ route
+ * Router: top-k experts per token and their weights.  The pages take
+ * topk_ids/topk_weights as inputs of prepare and finalize ("No DP/EP"
+ * listing); the router is the plainest reading of them:
+ *   MOE_SCORING_SOFTMAX_RENORM: the top_k largest fp32 logits, ordered larger
+ *     first, equal logits to the lower expert index; weight_j =
+ *     exp(l_j - l_max) / sum over the chosen i of exp(l_i - l_max).
+ *   MOE_SCORING_SIGMOID (top_k must be 1): argmax (lower index on ties),
+ *     weight = 1 / (1 + exp(-l)) -- the Llama-type router whose weight is
+ *     applied on the input ("Fused MoE Kernel Features", All2All section).
+ * logits [T, E] fp32 row-major; topk_ids [T, top_k] int32; topk_weights
+ * [T, top_k] fp32.  1 <= E <= 1024, 1 <= top_k <= min(E, 32).  NaN logits rank
+ * below every number. */
+moe_status_t moe_route(const float *logits, int T, int E, int top_k, int scoring,
+                       int32_t *topk_ids, float *topk_weights, moe_stream_t stream);
+
+/* ------------------------------------------------------------------ align
+ * Per-expert token alignment and permutation: the slots are sorted by the key
+ * (expert id, slot f), which groups each expert's rows contiguously in
+ * ascending slot order (deterministic).
+ *   expert_offsets [E + 1] int32: exclusive prefix sum of the per-expert
+ *                  counts; expert_offsets[E] = T * top_k.
+ *   sorted_slot    [T * top_k] int32: sorted_slot[p] = f.
+ *   inv_slot       [T * top_k] int32: inv_slot[sorted_slot[p]] = p (may be NULL).
+ *   tile_map       [moe_tile_map_capacity(T * top_k, E, block_m)] pairs of
+ *                  int32 (expert, first row p) for each block_m-row tile of
+ *                  each expert, expert by expert; entries past num_tiles are
+ *                  left untouched.
+ *   num_tiles      [1] int32: number of valid tile_map entries.
+ *   ws             scratch of moe_align_workspace_size(T, top_k, E) bytes.
+ * topk_ids values must lie in [0, E); 1 <= E <= 1024; block_m >= 1
+ * (moe_experts needs MOE_BLOCK_M). */
+moe_status_t moe_align(const int32_t *topk_ids, int T, int top_k, int E, int block_m,
+                       int32_t *expert_offsets, int32_t *sorted_slot, int32_t *inv_slot,
+                       int32_t *tile_map, int32_t *num_tiles, void *ws, size_t ws_bytes,
+                       moe_stream_t stream);
+size_t moe_align_workspace_size(int T, int top_k, int E);
+int moe_tile_map_capacity(int num_slots, int E, int block_m);
+
+/* ------------------------------------------------------------------ prepare
+ * Prepare ("No DP/EP" listing): when apply_router_weight_on_input is set
+ * (top_k must be 1) the input is first multiplied by the token's weight cast to
+ * bf16, a1 <- bf16(a1 * bf16(w)); then it is quantised per qc->act:
+ *   MOE_DT_BF16:     a1q [T, H] bf16 (a copy; when a1q == a1 and no weight is
+ *                    applied nothing is launched -- the passthrough);
+ *   MOE_DT_FP8_E4M3: a1q [T, H] E4M3 codes (uint8), a1q_scale [T, H/128] fp32:
+ *                    s = fp32(max(amax, 1e-10f) / 448) per 128 channels,
+ *                    q = e4m3_rn_satfinite(x / s) (IEEE fp32 division).
+ * a1 [T, H] bf16.  topk_weights [T, top_k] fp32 (read only with the weight
+ * flag).  topk_ids is accepted for parity with the pages' signature and unused
+ * (may be NULL).  H % 128 == 0 for fp8, H % 8 == 0 for bf16. */
+moe_status_t moe_prepare(const void *a1, const float *topk_weights, const int32_t *topk_ids,
+                         int T, int H, int top_k, int apply_router_weight_on_input,
+                         const moe_quant_config *qc, void *a1q, float *a1q_scale,
+                         moe_stream_t stream);
+
+/* ------------------------------------------------------------------ experts
+ * Grouped expert MLPs ("Fused Experts Kernels": two GEMMs with SiLU-and-mul
+ * between them).  For every expert e and sorted row p in
+ * [expert_offsets[e], expert_offsets[e+1]), with slot f = sorted_slot[p] and
+ * token t = f / top_k:
+ *   [g | u] = a1q[t] . w13[e]^T          (w13 [E, 2I, H]: rows 0..I-1 gate,
+ *                                          rows I..2I-1 up; K-contiguous)
+ *   h       = silu(g) * u                 (bf16, or E4M3 G(128) with fp8)
+ *   fused_expert_output[f] = h . w2[e]^T  (w2 [E, H, I]; bf16 [T*top_k, H],
+ *                                          token-major, unweighted)
+ * Accumulation is fp32.  fp8: a1q E4M3 + a1q_scale [T, H/128]; w13/w2 E4M3
+ * with w13_scale [E, 2I/128, H/128] and w2_scale [E, H/128, I/128] fp32; each
+ * 128-deep K block is scaled by a1q_scale * w_scale before it is added.
+ * expert_offsets / sorted_slot / tile_map / num_tiles come from moe_align with
+ * block_m = MOE_BLOCK_M.  sorted_slot may be NULL when E == 1 and top_k == 1
+ * (identity permutation; tile_map and expert_offsets are still required).
+ * ws: moe_workspace_size(...) bytes.  H % 128 == 0, I % 128 == 0. */
+moe_status_t moe_experts(const void *a1q, const float *a1q_scale, const void *w13,
+                         const float *w13_scale, const void *w2, const float *w2_scale,
+                         const int32_t *expert_offsets, const int32_t *sorted_slot,
+                         const int32_t *tile_map, const int32_t *num_tiles, int T, int H,
+                         int I, int E, int top_k, const moe_quant_config *qc,
+                         void *fused_expert_output, void *ws, size_t ws_bytes,
+                         moe_stream_t stream);
+size_t moe_workspace_size(int T, int H, int I, int E, int top_k, const moe_quant_config *qc);
+
+/* ------------------------------------------------------------------ finalize
+ * Finalize: the top-k weight-and-reduce of the "No DP/EP" listing followed by
+ * the single-GPU part of the flashinfer finalize fusion (introduction of its
+ * page, all-reduce removed):
+ *   o_t = sum_j w_tj * y[t*top_k + j]   (w_tj = 1 when the weights were
+ *                                         applied on the input)
+ *         + shared_t + residual_t        (each optional: NULL = absent)
+ *   residual_out_t = bf16(o_t)           (optional, NULL = not written)
+ *   o_t <- o_t * rsqrt(mean_h(o_t^2) + eps) * rms_weight  (when rms_weight)
+ * Sums in fp32.  Output per out_dtype:
+ *   MOE_DT_BF16:  output [T, H] bf16;
+ *   MOE_DT_FP32:  output [T, H] fp32;
+ *   MOE_DT_NVFP4: output [T, H/2] uint8, element 2i in the low nibble, and
+ *                 out_scale [T, H/16] E4M3 codes: per 16 elements
+ *                 sf = e4m3(amax / (6 g)), q = e2m1(x / (sf g)), g =
+ *                 out_global_scale > 0.
+ * fused_expert_output [T*top_k, H] bf16; topk_weights [T, top_k] fp32;
+ * shared, residual, residual_out [T, H] bf16; rms_weight [H] bf16.  topk_ids
+ * is accepted for parity with the pages' signature and unused (may be NULL).
+ * H % 8 == 0 (H % 16 == 0 for NVFP4), 1 <= top_k <= 32. */
+moe_status_t moe_finalize(void *output, const void *fused_expert_output, const float *topk_weights,
+                          const int32_t *topk_ids, const void *shared, const void *residual,
+                          const void *rms_weight, float eps, int T, int H, int top_k,
+                          int apply_router_weight_on_input, moe_dtype_t out_dtype,
+                          uint8_t *out_scale, float out_global_scale, void *residual_out,
+                          moe_stream_t stream);
+
+/* ------------------------------------------------------------------ status
+ * Every device-side wait in the library's kernels gives up after about two
+ * seconds, records MOE_ERR_TIMEOUT in a device status word and lets the
+ * kernel return.  moe_device_status synchronises the current device, returns
+ * the recorded status (MOE_OK when none) and clears it when `clear` != 0. */
+moe_status_t moe_device_status(int clear);
+const char *moe_status_string(moe_status_t status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_H_ */

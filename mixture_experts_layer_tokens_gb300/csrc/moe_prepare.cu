@@ -1,0 +1,127 @@
+// moe_prepare: the prepare step of the no-DP/EP pipeline ("[vLLM] MoE Oracle &
+// Prepare/Finalize" blog, "No DP/EP" listing): optional top-k weight on the
+// input (top_k == 1), then input quantisation -- bf16 passthrough, or fp8 E4M3
+// with one fp32 scale per token per 128 channels (the "G(128)" format of the
+// "Fused MoE Kernel Features" tables).
+//
+// HBM-bound: each thread moves one 16-byte vector of 8 bf16 values; the 16
+// threads of a 128-channel group reduce their amax with shuffles.  The scale
+// and the codes use IEEE division (never a reciprocal multiply) so the codes
+// are exactly those of the definition.
+#include "moe_common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kThreads = 256;
+
+__device__ __forceinline__ void load_bf16x8(const void* p, float (&x)[8]) {
+  const uint4 v = __ldg(reinterpret_cast<const uint4*>(p));
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    x[2 * i] = bf16lo(w[i]);
+    x[2 * i + 1] = bf16hi(w[i]);
+  }
+}
+
+__device__ __forceinline__ void apply_weight(float (&x)[8], const float* topk_weights, int t) {
+  // a1 * topk_weights.to(a1.dtype): the weight is rounded to bf16 first; the
+  // product of two bf16 numbers is exact in fp32 and is rounded once to bf16.
+  const float wb = __bfloat162float(__float2bfloat16_rn(__ldg(topk_weights + t)));
+#pragma unroll
+  for (int i = 0; i < 8; ++i) x[i] = __bfloat162float(__float2bfloat16_rn(x[i] * wb));
+}
+
+template <bool kWeight>
+__global__ void __launch_bounds__(kThreads)
+    prepare_bf16_kernel(const __nv_bfloat16* __restrict__ a1, const float* __restrict__ topk_weights, int H,
+                        long long nvec, __nv_bfloat16* __restrict__ a1q) {
+  const long long v = (long long)blockIdx.x * kThreads + threadIdx.x;
+  if (v >= nvec) return;
+  const int vec_per_row = H / 8;
+  const int t = (int)(v / vec_per_row);
+  float x[8];
+  load_bf16x8(a1 + v * 8, x);
+  if (kWeight) apply_weight(x, topk_weights, t);
+  uint4 o;
+  o.x = pack_bf16x2(x[0], x[1]);
+  o.y = pack_bf16x2(x[2], x[3]);
+  o.z = pack_bf16x2(x[4], x[5]);
+  o.w = pack_bf16x2(x[6], x[7]);
+  reinterpret_cast<uint4*>(a1q)[v] = o;
+}
+
+// One 128-channel group = 16 consecutive threads (half a warp).
+template <bool kWeight>
+__global__ void __launch_bounds__(kThreads)
+    prepare_fp8_kernel(const __nv_bfloat16* __restrict__ a1, const float* __restrict__ topk_weights, int H,
+                       long long nvec, uint8_t* __restrict__ a1q, float* __restrict__ a1q_scale) {
+  const long long v = (long long)blockIdx.x * kThreads + threadIdx.x;
+  // nvec is a multiple of 16, so a half warp is either fully in range or fully out
+  if (v >= nvec) return;
+  const int vec_per_row = H / 8;
+  const int t = (int)(v / vec_per_row);
+  float x[8];
+  load_bf16x8(a1 + v * 8, x);
+  if (kWeight) apply_weight(x, topk_weights, t);
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(x[i]));
+  const unsigned half_mask = (threadIdx.x & 16) ? 0xffff0000u : 0x0000ffffu;
+#pragma unroll
+  for (int off = 8; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(half_mask, amax, off));
+  const float s = __fdiv_rn(fmaxf(amax, 1e-10f), 448.0f);
+  uint32_t packed[2];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 r = make_float2(__fdiv_rn(x[2 * i], s), __fdiv_rn(x[2 * i + 1], s));
+    const uint32_t two = (uint32_t)__nv_cvt_float2_to_fp8x2(r, __NV_SATFINITE, __NV_E4M3);
+    if (i & 1)
+      packed[i >> 1] |= two << 16;
+    else
+      packed[i >> 1] = two;
+  }
+  reinterpret_cast<uint2*>(a1q)[v] = make_uint2(packed[0], packed[1]);
+  if ((threadIdx.x & 15) == 0) a1q_scale[v / 16] = s;  // [T, H/128] row-major == group index
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" moe_status_t moe_prepare(const void* a1, const float* topk_weights, const int32_t* topk_ids, int T, int H,
+                                    int top_k, int apply_router_weight_on_input, const moe_quant_config* qc,
+                                    void* a1q, float* a1q_scale, moe_stream_t stream) {
+  (void)topk_ids;
+  MOE_CHECK_ARG(qc && T >= 0 && H > 0 && top_k >= 1);
+  MOE_CHECK_ARG(!apply_router_weight_on_input || top_k == 1);  // the pages' `assert topk == 1`
+  const bool fp8 = qc->act == MOE_DT_FP8_E4M3;
+  if (!fp8 && qc->act != MOE_DT_BF16) return MOE_ERR_UNSUPPORTED;
+  if (fp8 && qc->act_group != 128) return MOE_ERR_UNSUPPORTED;
+  MOE_CHECK_ARG(fp8 ? H % 128 == 0 : H % 8 == 0);
+  MOE_CHECK_ARG(fits_int32((long long)T * H / 8 + kThreads));
+  if (T == 0) return MOE_OK;
+  MOE_CHECK_ARG(a1 && a1q && aligned16(a1) && aligned16(a1q));
+  MOE_CHECK_ARG(!apply_router_weight_on_input || topk_weights);
+  MOE_CHECK_ARG(!fp8 || a1q_scale);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const long long nvec = (long long)T * H / 8;
+  const unsigned grid = (unsigned)((nvec + kThreads - 1) / kThreads);
+  const auto* x = static_cast<const __nv_bfloat16*>(a1);
+  if (!fp8) {
+    if (!apply_router_weight_on_input) {
+      if (a1q == a1) return MOE_OK;  // no quantisation type: the input passes through
+      if (cudaMemcpyAsync(a1q, a1, (size_t)T * H * 2, cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+        return MOE_ERR_CUDA;
+      return MOE_OK;
+    }
+    prepare_bf16_kernel<true><<<grid, kThreads, 0, s>>>(x, topk_weights, H, nvec, static_cast<__nv_bfloat16*>(a1q));
+  } else if (apply_router_weight_on_input) {
+    prepare_fp8_kernel<true><<<grid, kThreads, 0, s>>>(x, topk_weights, H, nvec, static_cast<uint8_t*>(a1q), a1q_scale);
+  } else {
+    prepare_fp8_kernel<false><<<grid, kThreads, 0, s>>>(x, topk_weights, H, nvec, static_cast<uint8_t*>(a1q), a1q_scale);
+  }
+  return launch_status();
+}

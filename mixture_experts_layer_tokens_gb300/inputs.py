@@ -99,7 +99,9 @@ class LayerInputs:
     extra: dict = field(default_factory=dict)
 
     def to(self, device) -> "LayerInputs":
-        d = {k: (v.to(device) if isinstance(v, torch.Tensor) else v) for k, v in self.__dict__.items()}
+        mv = lambda v: v.to(device) if isinstance(v, torch.Tensor) else v
+        d = {k: mv(v) for k, v in self.__dict__.items()}
+        d["extra"] = {k: mv(v) for k, v in self.extra.items()}
         return LayerInputs(**d)
 
 
@@ -119,6 +121,14 @@ def _fp8_weights(gen, E, N, K, device):
     u = torch.rand((E, N // 128, K // 128), generator=gen, device=device) * 0.5 + 0.75
     scale = (u / (64.0 * math.sqrt(K))).to(torch.float32)
     return codes, scale
+
+
+def make_logits(cfg: LayerConfig, seed: int = 0, device="cpu") -> torch.Tensor:
+    """The router logits of `make_inputs(cfg, seed, device)` (its first draw) alone."""
+    gen = torch.Generator(device=torch.device(device))
+    gen.manual_seed(seed)
+    ncol = cfg.top_k if cfg.finalize_only else cfg.E
+    return torch.randn((cfg.T, ncol), generator=gen, device=torch.device(device), dtype=torch.float32)
 
 
 def make_inputs(cfg: LayerConfig, seed: int = 0, device="cpu") -> LayerInputs:

@@ -1,0 +1,99 @@
+"""One fused-MoE layer step composed from the C-ABI calls, with every buffer
+allocated once up front (PyTorch allocates, the library computes).
+
+Step (all on one stream):
+  moe_route -> moe_align -> moe_prepare -> moe_experts [-> shared expert via
+  moe_experts with one expert and the identity permutation] -> moe_finalize.
+
+The shared expert sees the unweighted bf16 input, as the shared-expert row of
+the flashinfer finalize fusion is added unscaled.
+"""
+from __future__ import annotations
+
+from typing import Optional
+
+import torch
+
+from . import moe
+from .inputs import LayerConfig, LayerInputs
+
+
+class MoELayer:
+    def __init__(self, inp: LayerInputs, stream: Optional[torch.cuda.Stream] = None):
+        cfg = self.cfg = inp.cfg
+        assert not cfg.finalize_only
+        self.inp = inp
+        dev = inp.logits.device
+        T, H, I, E, k = cfg.T, cfg.H, cfg.I, cfg.E, cfg.top_k
+        self.scoring = moe.MOE_SCORING_SIGMOID if cfg.scoring == "sigmoid" else moe.MOE_SCORING_SOFTMAX_RENORM
+        self.topk_ids = torch.empty((T, k), dtype=torch.int32, device=dev)
+        self.topk_weights = torch.empty((T, k), dtype=torch.float32, device=dev)
+        self.al = moe.Alignment(T, k, E, dev)
+        fp8 = cfg.quant == "fp8"
+        # bf16 without weight-on-input: prepare is the passthrough (a1q is a1)
+        self.passthrough = not fp8 and not cfg.weight_on_input
+        self.a1q = None if self.passthrough else torch.empty((T, H), dtype=torch.uint8 if fp8 else torch.bfloat16,
+                                                             device=dev)
+        self.a1q_scale = torch.empty((T, H // 128), dtype=torch.float32, device=dev) if fp8 else None
+        self.y = torch.empty((T * k, H), dtype=torch.bfloat16, device=dev)
+        self.ws = torch.empty(max(moe.workspace_size(T, H, I, E, k, cfg.quant), 16), dtype=torch.uint8, device=dev)
+        self.out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+        self.shared = None
+        if cfg.shared_I:
+            self.shared = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+            ids0 = torch.zeros((T, 1), dtype=torch.int32, device=dev)
+            self.al_shared = moe.moe_align(ids0, 1, stream=stream)
+            self.ws_shared = torch.empty(max(moe.workspace_size(T, H, cfg.shared_I, 1, 1, "bf16"), 16),
+                                         dtype=torch.uint8, device=dev)
+
+    def forward(self, logits: torch.Tensor, a1: torch.Tensor, stream=None) -> torch.Tensor:
+        cfg, inp = self.cfg, self.inp
+        moe.moe_route(logits, cfg.top_k, self.scoring, self.topk_ids, self.topk_weights, stream=stream)
+        moe.moe_align(self.topk_ids, cfg.E, out=self.al, stream=stream)
+        if self.passthrough:
+            a1q, a1q_scale = a1, None
+        else:
+            a1q, a1q_scale = moe.moe_prepare(a1, self.topk_weights, cfg.top_k, cfg.weight_on_input, cfg.quant,
+                                             self.a1q, self.a1q_scale, stream=stream)
+        moe.moe_experts(a1q, a1q_scale, inp.w13, inp.w13_scale, inp.w2, inp.w2_scale, self.al, cfg.quant,
+                        out=self.y, ws=self.ws, stream=stream)
+        shared = None
+        if self.shared is not None:
+            shared = moe.moe_experts(a1, None, inp.shared_w13, None, inp.shared_w2, None, self.al_shared, "bf16",
+                                     out=self.shared, ws=self.ws_shared, identity=True, stream=stream)
+        moe.moe_finalize(self.y, self.topk_weights, cfg.top_k, cfg.weight_on_input, shared=shared,
+                         residual=inp.residual, rms_weight=inp.rms_weight, output=self.out, stream=stream)
+        return self.out
+
+
+class FinalizeStep:
+    """The finalize-only workload: route over k logits, then finalize to bf16
+    and to NVFP4."""
+
+    def __init__(self, inp: LayerInputs):
+        cfg = self.cfg = inp.cfg
+        assert cfg.finalize_only
+        self.inp = inp
+        dev = inp.logits.device
+        T, H, k = cfg.T, cfg.H, cfg.top_k
+        self.topk_ids = torch.empty((T, k), dtype=torch.int32, device=dev)
+        self.topk_weights = torch.empty((T, k), dtype=torch.float32, device=dev)
+        self.out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+        self.out_fp4 = torch.empty((T, H // 2), dtype=torch.uint8, device=dev)
+        self.out_sf = torch.empty((T, H // 16), dtype=torch.uint8, device=dev)
+
+    def weights(self, stream=None):
+        moe.moe_route(self.inp.logits, self.cfg.top_k, moe.MOE_SCORING_SOFTMAX_RENORM, self.topk_ids,
+                      self.topk_weights, stream=stream)
+        return self.topk_weights
+
+    def finalize(self, nvfp4: bool, stream=None):
+        inp = self.inp
+        if nvfp4:
+            return moe.moe_finalize(inp.y, self.topk_weights, self.cfg.top_k, False, shared=inp.extra["shared"],
+                                    residual=inp.residual, rms_weight=inp.rms_weight, eps=1e-6,
+                                    out_dtype=moe.MOE_DT_NVFP4, out_global_scale=1.0, output=self.out_fp4,
+                                    out_scale=self.out_sf, topk_ids=inp.topk_ids, stream=stream)
+        return moe.moe_finalize(inp.y, self.topk_weights, self.cfg.top_k, False, shared=inp.extra["shared"],
+                                residual=inp.residual, rms_weight=inp.rms_weight, eps=1e-6,
+                                out_dtype=moe.MOE_DT_BF16, output=self.out, topk_ids=inp.topk_ids, stream=stream)

@@ -1,0 +1,243 @@
+"""Thin ctypes binding of the fused-MoE C ABI (``include/moe.h``).
+
+Every function here checks tensor dtypes/devices, passes ``data_ptr()`` values
+and the current torch CUDA stream to the C entry point of the same name, and
+turns a non-OK status into :class:`MoeError`.  All arithmetic happens in the
+CUDA library; there is no fallback path.  PyTorch only provides device memory
+and streams.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Tuple
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libmoe.so")
+
+MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE, MOE_ERR_CUDA, MOE_ERR_TIMEOUT = range(6)
+MOE_DT_BF16, MOE_DT_FP8_E4M3, MOE_DT_NVFP4, MOE_DT_FP32 = range(4)
+MOE_SCORING_SOFTMAX_RENORM, MOE_SCORING_SIGMOID = 0, 1
+MOE_BLOCK_M = 128
+
+# (name, argtypes, restype) of every exported entry point
+_P, _I, _F, _Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+
+
+class QuantConfig(ctypes.Structure):
+    _fields_ = [("act", ctypes.c_int), ("act_group", ctypes.c_int), ("weight", ctypes.c_int),
+                ("w_block_n", ctypes.c_int), ("w_block_k", ctypes.c_int)]
+
+
+QC_BF16 = QuantConfig(MOE_DT_BF16, 0, MOE_DT_BF16, 0, 0)
+QC_FP8 = QuantConfig(MOE_DT_FP8_E4M3, 128, MOE_DT_FP8_E4M3, 128, 128)
+_QCP = ctypes.POINTER(QuantConfig)
+
+SIGNATURES = {
+    "moe_route": ([_P, _I, _I, _I, _I, _P, _P, _P], _I),
+    "moe_align": ([_P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _Z, _P], _I),
+    "moe_align_workspace_size": ([_I, _I, _I], _Z),
+    "moe_tile_map_capacity": ([_I, _I, _I], _I),
+    "moe_prepare": ([_P, _P, _P, _I, _I, _I, _I, _QCP, _P, _P, _P], _I),
+    "moe_experts": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _QCP, _P, _P, _Z, _P], _I),
+    "moe_workspace_size": ([_I, _I, _I, _I, _I, _QCP], _Z),
+    "moe_finalize": ([_P, _P, _P, _P, _P, _P, _P, _F, _I, _I, _I, _I, _I, _P, _F, _P, _P], _I),
+    "moe_device_status": ([_I], _I),
+    "moe_status_string": ([_I], ctypes.c_char_p),
+}
+
+_lib_handle = None
+
+
+class MoeError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn} failed: {status_string(status)} (status {status})")
+
+
+def lib():
+    """Load libmoe.so (built by ``mixture_experts_layer_tokens_gb300.build``).
+
+    Raises if the library is missing: there is no CPU or PyTorch fallback."""
+    global _lib_handle
+    if _lib_handle is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "`python -m mixture_experts_layer_tokens_gb300.build` (nvcc, sm_103a)")
+        h = ctypes.CDLL(LIB_PATH)
+        for name, (args, res) in SIGNATURES.items():
+            f = getattr(h, name)
+            f.argtypes = args
+            f.restype = res
+        _lib_handle = h
+    return _lib_handle
+
+
+def status_string(status: int) -> str:
+    return lib().moe_status_string(status).decode()
+
+
+def _check(fn: str, status: int):
+    if status != MOE_OK:
+        raise MoeError(fn, status)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream: Optional[torch.cuda.Stream]):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _need(t: Optional[torch.Tensor], dtype, name: str, cuda: bool = True):
+    if t is None:
+        return
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    if cuda and not t.is_cuda:
+        raise TypeError(f"{name}: expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: expected a contiguous tensor")
+
+
+# ------------------------------------------------------------------ entry points
+def moe_route(logits: torch.Tensor, top_k: int, scoring: int = MOE_SCORING_SOFTMAX_RENORM,
+              topk_ids: Optional[torch.Tensor] = None, topk_weights: Optional[torch.Tensor] = None,
+              stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    _need(logits, torch.float32, "logits")
+    T, E = logits.shape
+    if topk_ids is None:
+        topk_ids = torch.empty((T, top_k), dtype=torch.int32, device=logits.device)
+    if topk_weights is None:
+        topk_weights = torch.empty((T, top_k), dtype=torch.float32, device=logits.device)
+    _need(topk_ids, torch.int32, "topk_ids")
+    _need(topk_weights, torch.float32, "topk_weights")
+    _check("moe_route", lib().moe_route(_ptr(logits), T, E, top_k, scoring, _ptr(topk_ids), _ptr(topk_weights),
+                                        _stream(stream)))
+    return topk_ids, topk_weights
+
+
+def align_workspace_size(T: int, top_k: int, E: int) -> int:
+    return int(lib().moe_align_workspace_size(T, top_k, E))
+
+
+def tile_map_capacity(num_slots: int, E: int, block_m: int = MOE_BLOCK_M) -> int:
+    return int(lib().moe_tile_map_capacity(num_slots, E, block_m))
+
+
+class Alignment:
+    """Device buffers written by moe_align."""
+
+    def __init__(self, T: int, top_k: int, E: int, device, block_m: int = MOE_BLOCK_M):
+        S = T * top_k
+        self.T, self.top_k, self.E, self.block_m = T, top_k, E, block_m
+        self.expert_offsets = torch.empty(E + 1, dtype=torch.int32, device=device)
+        self.sorted_slot = torch.empty(max(S, 1), dtype=torch.int32, device=device)
+        self.inv_slot = torch.empty(max(S, 1), dtype=torch.int32, device=device)
+        self.tile_map = torch.empty((max(tile_map_capacity(S, E, block_m), 1), 2), dtype=torch.int32, device=device)
+        self.num_tiles = torch.zeros(1, dtype=torch.int32, device=device)
+        self.ws = torch.empty(max(align_workspace_size(T, top_k, E), 16), dtype=torch.uint8, device=device)
+
+
+def moe_align(topk_ids: torch.Tensor, E: int, block_m: int = MOE_BLOCK_M, out: Optional[Alignment] = None,
+              stream=None) -> Alignment:
+    _need(topk_ids, torch.int32, "topk_ids")
+    T, k = topk_ids.shape
+    al = out if out is not None else Alignment(T, k, E, topk_ids.device, block_m)
+    _check("moe_align", lib().moe_align(_ptr(topk_ids), T, k, E, block_m, _ptr(al.expert_offsets),
+                                        _ptr(al.sorted_slot), _ptr(al.inv_slot), _ptr(al.tile_map),
+                                        _ptr(al.num_tiles), _ptr(al.ws), al.ws.numel(), _stream(stream)))
+    return al
+
+
+def moe_prepare(a1: torch.Tensor, topk_weights: Optional[torch.Tensor], top_k: int,
+                apply_router_weight_on_input: bool, quant: str, a1q: Optional[torch.Tensor] = None,
+                a1q_scale: Optional[torch.Tensor] = None, topk_ids: Optional[torch.Tensor] = None,
+                stream=None):
+    """quant: "bf16" (no quantisation) or "fp8" (E4M3, per-token 128-group scales).
+    Passing ``a1q=a1`` with bf16 and no weight is the passthrough (nothing runs)."""
+    _need(a1, torch.bfloat16, "a1")
+    _need(topk_weights, torch.float32, "topk_weights")
+    T, H = a1.shape
+    qc = QC_FP8 if quant == "fp8" else QC_BF16
+    if a1q is None:
+        a1q = torch.empty((T, H), dtype=torch.uint8 if quant == "fp8" else torch.bfloat16, device=a1.device)
+    if quant == "fp8" and a1q_scale is None:
+        a1q_scale = torch.empty((T, H // 128), dtype=torch.float32, device=a1.device)
+    _need(a1q, torch.uint8 if quant == "fp8" else torch.bfloat16, "a1q")
+    _need(a1q_scale, torch.float32, "a1q_scale")
+    _check("moe_prepare", lib().moe_prepare(_ptr(a1), _ptr(topk_weights), _ptr(topk_ids), T, H, top_k,
+                                            int(bool(apply_router_weight_on_input)), ctypes.byref(qc), _ptr(a1q),
+                                            _ptr(a1q_scale), _stream(stream)))
+    return a1q, a1q_scale
+
+
+def workspace_size(T: int, H: int, I: int, E: int, top_k: int, quant: str) -> int:
+    return int(lib().moe_workspace_size(T, H, I, E, top_k, ctypes.byref(QC_FP8 if quant == "fp8" else QC_BF16)))
+
+
+def moe_experts(a1q: torch.Tensor, a1q_scale: Optional[torch.Tensor], w13: torch.Tensor,
+                w13_scale: Optional[torch.Tensor], w2: torch.Tensor, w2_scale: Optional[torch.Tensor],
+                al: Alignment, quant: str, out: Optional[torch.Tensor] = None, ws: Optional[torch.Tensor] = None,
+                identity: bool = False, stream=None) -> torch.Tensor:
+    """Grouped SwiGLU experts.  ``identity=True`` (E == 1, top_k == 1) passes a
+    NULL sorted_slot: rows are the tokens in order."""
+    fp8 = quant == "fp8"
+    _need(a1q, torch.uint8 if fp8 else torch.bfloat16, "a1q")
+    _need(w13, torch.uint8 if fp8 else torch.bfloat16, "w13")
+    _need(w2, torch.uint8 if fp8 else torch.bfloat16, "w2")
+    for t, n in ((a1q_scale, "a1q_scale"), (w13_scale, "w13_scale"), (w2_scale, "w2_scale")):
+        _need(t, torch.float32, n)
+    T, H = a1q.shape
+    E, twoI, _ = w13.shape
+    I = twoI // 2
+    k = al.top_k
+    if out is None:
+        out = torch.empty((T * k, H), dtype=torch.bfloat16, device=a1q.device)
+    _need(out, torch.bfloat16, "fused_expert_output")
+    if ws is None:
+        ws = torch.empty(max(workspace_size(T, H, I, E, k, quant), 16), dtype=torch.uint8, device=a1q.device)
+    qc = QC_FP8 if fp8 else QC_BF16
+    _check("moe_experts", lib().moe_experts(
+        _ptr(a1q), _ptr(a1q_scale), _ptr(w13), _ptr(w13_scale), _ptr(w2), _ptr(w2_scale), _ptr(al.expert_offsets),
+        None if identity else _ptr(al.sorted_slot), _ptr(al.tile_map), _ptr(al.num_tiles), T, H, I, E, k,
+        ctypes.byref(qc), _ptr(out), _ptr(ws), ws.numel(), _stream(stream)))
+    return out
+
+
+def moe_finalize(fused_expert_output: torch.Tensor, topk_weights: Optional[torch.Tensor], top_k: int,
+                 apply_router_weight_on_input: bool = False, shared: Optional[torch.Tensor] = None,
+                 residual: Optional[torch.Tensor] = None, rms_weight: Optional[torch.Tensor] = None,
+                 eps: float = 1e-6, out_dtype: int = MOE_DT_BF16, out_global_scale: float = 1.0,
+                 output: Optional[torch.Tensor] = None, out_scale: Optional[torch.Tensor] = None,
+                 residual_out: Optional[torch.Tensor] = None, topk_ids: Optional[torch.Tensor] = None,
+                 stream=None):
+    _need(fused_expert_output, torch.bfloat16, "fused_expert_output")
+    _need(topk_weights, torch.float32, "topk_weights")
+    for t, n in ((shared, "shared"), (residual, "residual"), (rms_weight, "rms_weight"),
+                 (residual_out, "residual_out")):
+        _need(t, torch.bfloat16, n)
+    S, H = fused_expert_output.shape
+    T = S // top_k
+    dev = fused_expert_output.device
+    if output is None:
+        if out_dtype == MOE_DT_NVFP4:
+            output = torch.empty((T, H // 2), dtype=torch.uint8, device=dev)
+        else:
+            output = torch.empty((T, H), dtype=torch.float32 if out_dtype == MOE_DT_FP32 else torch.bfloat16,
+                                 device=dev)
+    if out_dtype == MOE_DT_NVFP4 and out_scale is None:
+        out_scale = torch.empty((T, H // 16), dtype=torch.uint8, device=dev)
+    _check("moe_finalize", lib().moe_finalize(
+        _ptr(output), _ptr(fused_expert_output), _ptr(topk_weights), _ptr(topk_ids), _ptr(shared), _ptr(residual),
+        _ptr(rms_weight), float(eps), T, H, top_k, int(bool(apply_router_weight_on_input)), out_dtype,
+        _ptr(out_scale), float(out_global_scale), _ptr(residual_out), _stream(stream)))
+    return output, out_scale
+
+
+def moe_device_status(clear: bool = True) -> int:
+    return int(lib().moe_device_status(int(clear)))

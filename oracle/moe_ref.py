@@ -201,11 +201,14 @@ def prepare(a1: torch.Tensor, topk_weights: torch.Tensor, apply_router_weight_on
 
 
 # =========================================================================== experts
+_E4M3_TABLE = codecs.e4m3_decode(np.arange(256))  # value of every code
+
+
 def dequant_weight_block(w_codes: np.ndarray, w_scale: np.ndarray, block: int = 128) -> np.ndarray:
     """[N, K] E4M3 codes with [N/128, K/128] fp32 block scales -> fp64 [N, K]."""
     N, K = w_codes.shape
-    v = codecs.e4m3_decode(w_codes)
-    return v * np.repeat(np.repeat(w_scale.astype(np.float64), block, axis=0), block, axis=1)[:N, :K]
+    v = _E4M3_TABLE[w_codes].reshape(N // block, block, K // block, block)
+    return (v * w_scale.astype(np.float64)[:, None, :, None]).reshape(N, K)
 
 
 def silu_and_mul(gu: torch.Tensor) -> torch.Tensor:

@@ -1,0 +1,84 @@
+"""GPU grouped expert GEMMs vs the oracle, fed identical prepared inputs.
+
+Sizes span several M, N and K tiles with ragged tails: experts of 0, 1, <128,
+>128 and many-tile row counts, N tiles that run past H, deep K loops."""
+import numpy as np
+import pytest
+import torch
+
+from mixture_experts_layer_tokens_gb300 import moe
+from mixture_experts_layer_tokens_gb300.inputs import CONFIGS, make_inputs, scaled
+from oracle import moe_ref
+from parity_util import check_bf16, check_fp8
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(inp, ids, dev, quant, identity=False):
+    cfg = inp.cfg
+    E, k = cfg.E, ids.shape[1]
+    w = torch.full(ids.shape, 1.0 / k)
+    al = moe.moe_align(ids.to(dev), E)
+    a1q, sc = moe.moe_prepare(inp.a1.to(dev), None, k, False, quant)
+    d = lambda t: None if t is None else t.to(dev)
+    y = moe.moe_experts(a1q, sc, d(inp.w13), d(inp.w13_scale), d(inp.w2), d(inp.w2_scale), al, quant,
+                        identity=identity)
+    torch.cuda.synchronize()
+    assert moe.moe_device_status() == moe.MOE_OK
+    ral = moe_ref.align(ids, E, 128)
+    rq, rs = moe_ref.prepare(inp.a1, None, False, quant)
+    assert torch.equal(a1q.cpu(), rq)
+    yref = moe_ref.experts(rq, rs, inp.w13, inp.w13_scale, inp.w2, inp.w2_scale, ral, k, quant)
+    return y, yref
+
+
+def _ids(T, k, E, seed, skew=False):
+    g = torch.Generator().manual_seed(seed)
+    if skew:
+        p = torch.tensor([0.5 ** i for i in range(E)])
+        p[E // 2] = 0  # one empty expert
+        ids = torch.stack([torch.multinomial(p, k, replacement=False, generator=g) for _ in range(T)])
+    else:
+        ids = torch.argsort(torch.rand((T, E), generator=g), dim=1)[:, :k]
+    return ids.to(torch.int32).contiguous()
+
+
+@pytest.mark.parametrize("T,H,I,E,k,skew", [
+    (16, 256, 512, 8, 2, False),      # the tiny layer
+    (300, 512, 384, 4, 2, False),     # 2 M tiles per expert, ragged tails
+    (700, 384, 256, 6, 2, True),      # skewed: a 5-tile expert, an empty one; GEMM2 N tile past H
+    (130, 2048, 256, 3, 1, False),    # deep K (32 stages)
+    (1, 256, 128, 8, 2, False),       # single token
+])
+def test_experts_bf16(cuda_dev, T, H, I, E, k, skew):
+    inp = make_inputs(scaled(CONFIGS["tiny"], T=T, H=H, I=I, E=E, top_k=k))
+    y, yref = _run(inp, _ids(T, k, E, T + H, skew), cuda_dev, "bf16")
+    check_bf16(y, yref, "experts bf16")
+
+
+@pytest.mark.parametrize("T,H,I,E,k,skew", [
+    (16, 256, 256, 8, 2, False),
+    (300, 512, 384, 4, 2, False),
+    (500, 384, 256, 6, 2, True),
+    (100, 1024, 512, 16, 4, False),
+])
+def test_experts_fp8(cuda_dev, T, H, I, E, k, skew):
+    inp = make_inputs(scaled(CONFIGS["deepseek"], T=T, H=H, I=I, E=E, top_k=k, shared_I=0))
+    y, yref = _run(inp, _ids(T, k, E, T + I, skew), cuda_dev, "fp8")
+    check_fp8(y, yref, "experts fp8")
+
+
+def test_experts_identity_permutation(cuda_dev):
+    # one expert, top-1, NULL sorted_slot: the shared-expert call
+    inp = make_inputs(scaled(CONFIGS["tiny"], T=200, H=512, I=256, E=1, top_k=1))
+    ids = torch.zeros((200, 1), dtype=torch.int32)
+    y, yref = _run(inp, ids, cuda_dev, "bf16", identity=True)
+    check_bf16(y, yref, "identity")
+
+
+def test_experts_twice_same_bits(cuda_dev):
+    inp = make_inputs(scaled(CONFIGS["tiny"], T=300, H=512, I=384, E=4))
+    ids = _ids(300, 2, 4, 3)
+    y1, _ = _run(inp, ids, cuda_dev, "bf16")
+    y2, _ = _run(inp, ids, cuda_dev, "bf16")
+    assert torch.equal(y1, y2)

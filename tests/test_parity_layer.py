@@ -1,0 +1,109 @@
+"""Whole-layer parity: route -> align -> prepare -> experts (+ shared) -> finalize
+through the C ABI against the oracle.
+
+Small shapes of every configuration are checked on every token; the full-size
+configurations are run exactly as the bench runs them and checked on sampled
+tokens, which the oracle computes one expert at a time."""
+import numpy as np
+import pytest
+import torch
+
+from mixture_experts_layer_tokens_gb300 import moe
+from mixture_experts_layer_tokens_gb300.inputs import CONFIGS, make_inputs, scaled
+from mixture_experts_layer_tokens_gb300.layer import MoELayer
+from oracle import moe_ref
+from parity_util import check_bf16, check_fp8, ulp_bf16
+
+pytestmark = pytest.mark.gpu
+
+
+def oracle_tokens(inp, tokens, gpu_ids, gpu_w):
+    """Oracle output rows (fp64) of the given tokens and the rounding slack of
+    the bf16 intermediates (see parity_util).  The router is checked bit-exact
+    against the oracle's; the weights fed on are the GPU's (same inputs for
+    every stage)."""
+    cfg = inp.cfg
+    k = cfg.top_k
+    logits = inp.logits[tokens].cpu()
+    if cfg.scoring == "sigmoid":
+        ids, _ = moe_ref.route_sigmoid_top1(logits)
+    else:
+        ids, _ = moe_ref.route_softmax_renorm(logits, k)
+    assert torch.equal(ids, gpu_ids[tokens].cpu())
+    w = gpu_w[tokens].cpu()
+    a1 = inp.a1[tokens].cpu()
+    a1q, sc = moe_ref.prepare(a1, w, cfg.weight_on_input, cfg.quant)
+    n, H = len(tokens), cfg.H
+    y = torch.zeros((n * k, H), dtype=torch.float64)
+    for e in sorted(set(ids.reshape(-1).tolist())):
+        slots = [(i, j) for i in range(n) for j in range(k) if int(ids[i, j]) == e]
+        rows = np.array([i for i, _ in slots])
+        A = moe_ref._act64(a1q, sc, rows, cfg.quant)
+        W13 = moe_ref._weights64(inp.w13, inp.w13_scale, e, cfg.quant)
+        W2 = moe_ref._weights64(inp.w2, inp.w2_scale, e, cfg.quant)
+        ye = moe_ref.expert_rows(A, W13, W2, cfg.quant)
+        for r, (i, j) in enumerate(slots):
+            y[i * k + j] = ye[r]
+    shared = moe_ref.dense_mlp(a1, inp.shared_w13[0], inp.shared_w2[0]) if cfg.shared_I else None
+    res = inp.residual[tokens].cpu() if inp.residual is not None else None
+    gm = None if inp.rms_weight is None else inp.rms_weight.cpu()
+    fo = moe_ref.finalize(y, w, k, cfg.weight_on_input, shared=shared, residual=res, rms_weight=gm)
+    yw = y.numpy().reshape(n, k, H)
+    ww = np.ones((n, k)) if cfg.weight_on_input else w.double().numpy()
+    slack = (np.abs(ww)[:, :, None] * ulp_bf16(yw)).sum(axis=1)
+    if shared is not None:
+        slack = slack + ulp_bf16(shared.numpy())
+    if gm is not None:
+        pre = moe_ref.finalize(y, w, k, cfg.weight_on_input, shared=shared, residual=res).out
+        slack = slack / np.sqrt((pre ** 2).mean(axis=1, keepdims=True) + 1e-6) * np.abs(gm.double().numpy())[None]
+    return fo.out, slack
+
+
+def _check(cfg, out, ref, what):
+    ref, slack = ref
+    if cfg.quant == "fp8":
+        return check_fp8(out, ref, what)
+    return check_bf16(out, ref, what, slack=slack)
+
+
+SMALL = {
+    "tiny": CONFIGS["tiny"],
+    "mixtral_small": scaled(CONFIGS["mixtral"], T=200, H=512, I=768),
+    "deepseek_small": scaled(CONFIGS["deepseek"], T=256, H=512, I=256, E=32, shared_I=256),
+    "llama_small": scaled(CONFIGS["llama8"], T=100, H=384, I=512, shared_I=256),
+    "llama_small_T1": scaled(CONFIGS["llama1"], H=384, I=512, shared_I=256),
+    "residual_rms": scaled(CONFIGS["mixtral"], T=64, H=256, I=256, residual=True, rms=True),
+}
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_layer_small_all_tokens(cuda_dev, name):
+    cfg = SMALL[name]
+    inp = make_inputs(cfg)
+    layer = MoELayer(inp.to(cuda_dev))
+    out = layer.forward(layer.inp.logits, layer.inp.a1)
+    torch.cuda.synchronize()
+    assert moe.moe_device_status() == moe.MOE_OK
+    ref = oracle_tokens(inp, list(range(cfg.T)), layer.topk_ids, layer.topk_weights)
+    _check(cfg, out, ref, name)
+
+
+@pytest.mark.parametrize("name,sample", [("mixtral", 12), ("deepseek", 3), ("llama1", 1), ("llama8", 8),
+                                         ("llama64", 6), ("llama512", 6)])
+def test_layer_full_size_sampled_tokens(cuda_dev, name, sample):
+    cfg = CONFIGS[name]
+    inp = make_inputs(cfg, device=cuda_dev)   # full-size weights drawn on the device
+    layer = MoELayer(inp)
+    for _ in range(2):                        # the second run checks reuse of every buffer
+        out = layer.forward(inp.logits, inp.a1)
+    torch.cuda.synchronize()
+    assert moe.moe_device_status() == moe.MOE_OK
+    g = torch.Generator().manual_seed(1)
+    tokens = sorted(torch.randperm(cfg.T, generator=g)[:sample].tolist())
+    if cfg.T - 1 not in tokens:
+        tokens[-1] = cfg.T - 1                # always include the last token (ragged tail)
+    ref = oracle_tokens(inp, tokens, layer.topk_ids, layer.topk_weights)
+    _check(cfg, out[tokens], ref, name)
+    # properties that hold at any size: finite everywhere, every routed expert row written
+    assert torch.isfinite(out.float()).all()
+    assert int(layer.al.expert_offsets[-1]) == cfg.T * cfg.top_k
