@@ -119,6 +119,31 @@ moe_status_t moe_align(const int32_t *topk_ids, int T, int top_k, int E, int blo
 size_t moe_align_workspace_size(int T, int top_k, int E);
 int moe_tile_map_capacity(int num_slots, int E, int block_m);
 
+/* ------------------------------------------------------------------ align, no allocation
+ * Not part of the method: the pages have no counterpart of this call.  It is
+ * moe_align for callers that cannot allocate device memory at call time --
+ * runtimes that plan every device buffer ahead and forbid allocation while
+ * serving, or plugin-style hosts whose per-call hook may not allocate -- and so
+ * cannot supply the `ws` scratch that moe_align needs.
+ *
+ * Same arguments, layouts and results as moe_align, minus ws/ws_bytes.  The
+ * scratch is a fixed array of MOE_ALIGN_NOALLOC_SCRATCH_BYTES inside the
+ * library (every GPU that loads the library holds it until the process exits);
+ * a problem needing more (moe_align_workspace_size(T, top_k, E) larger than
+ * that) is rejected with MOE_ERR_WORKSPACE before anything is launched.  The
+ * call allocates nothing.
+ *  - The first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress) with that device current; make that first call
+ *    before any stream capture on the device.
+ *  - All calls share the one array and it keeps the last call's contents (each
+ *    call writes every entry it later reads, so nothing needs clearing).  Calls
+ *    whose work overlaps on the GPU -- on different streams, or from different
+ *    host threads without ordering -- race on it: order them on one stream. */
+#define MOE_ALIGN_NOALLOC_SCRATCH_BYTES (256 * 1024)
+moe_status_t moe_align_noalloc(const int32_t *topk_ids, int T, int top_k, int E, int block_m,
+                               int32_t *expert_offsets, int32_t *sorted_slot, int32_t *inv_slot,
+                               int32_t *tile_map, int32_t *num_tiles, moe_stream_t stream);
+
 /* ------------------------------------------------------------------ prepare
  * Prepare ("No DP/EP" listing): when apply_router_weight_on_input is set
  * (top_k must be 1) the input is first multiplied by the token's weight cast to

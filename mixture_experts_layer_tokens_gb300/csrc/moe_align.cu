@@ -16,6 +16,8 @@
 //               later warps add the counts of earlier ones without clearing
 //               any table.
 // No result depends on the order in which atomics land.
+#include <atomic>
+
 #include "moe_common.cuh"
 
 namespace moe {
@@ -203,6 +205,57 @@ extern "C" moe_status_t moe_align(const int32_t* topk_ids, int T, int top_k, int
   align_scan_kernel<<<1, kScanThreads, 0, s>>>(hist, nchunks, E, block_m, expert_offsets, tile_map, num_tiles);
   if (nchunks > 0) {
     const size_t smem = (size_t)(1 + kWarps) * E * sizeof(int32_t);  // <= 36 KB at E = 1024
+    align_scatter_kernel<<<nchunks, kThreads, smem, s>>>(topk_ids, S, E, hist, sorted_slot, inv_slot);
+  }
+  return launch_status();
+}
+
+// ------------------------------------------------------------------ align without allocation
+// Scratch of moe_align_noalloc: a file-scope device array shared by every call.
+// On the host this name is only a stand-in for the symbol, not a device
+// address: host code passes kernels the address looked up below, once per
+// device.
+static __device__ __align__(256) int32_t g_align_scratch[MOE_ALIGN_NOALLOC_SCRATCH_BYTES / sizeof(int32_t)];
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::atomic<int32_t*> g_scratch_ptr[kMaxDevices];
+
+// Device address of g_align_scratch on the current device, looked up (with
+// that device current) on the first call for the device.
+moe_status_t scratch_on_current_device(int32_t** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return MOE_ERR_UNSUPPORTED;
+  int32_t* p = g_scratch_ptr[dev].load(std::memory_order_acquire);
+  if (!p) {
+    if (cudaGetSymbolAddress(reinterpret_cast<void**>(&p), g_align_scratch) != cudaSuccess || !p)
+      return MOE_ERR_CUDA;
+    g_scratch_ptr[dev].store(p, std::memory_order_release);
+  }
+  *out = p;
+  return MOE_OK;
+}
+}  // namespace
+
+extern "C" moe_status_t moe_align_noalloc(const int32_t* topk_ids, int T, int top_k, int E, int block_m,
+                                          int32_t* expert_offsets, int32_t* sorted_slot, int32_t* inv_slot,
+                                          int32_t* tile_map, int32_t* num_tiles, moe_stream_t stream) {
+  MOE_CHECK_ARG(T >= 0 && top_k >= 1 && E >= 1 && E <= kScanThreads && block_m >= 1);
+  MOE_CHECK_ARG(fits_int32((long long)T * top_k));
+  MOE_CHECK_ARG(expert_offsets && tile_map && num_tiles);
+  const int S = T * top_k;
+  if (S > 0) MOE_CHECK_ARG(topk_ids && sorted_slot);
+  if (moe_align_workspace_size(T, top_k, E) > (size_t)MOE_ALIGN_NOALLOC_SCRATCH_BYTES) return MOE_ERR_WORKSPACE;
+  int32_t* hist = nullptr;
+  const moe_status_t st = scratch_on_current_device(&hist);
+  if (st != MOE_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const int nchunks = (S + kChunk - 1) / kChunk;
+  if (nchunks > 0) align_count_kernel<<<nchunks, kThreads, E * sizeof(int32_t), s>>>(topk_ids, S, E, hist);
+  align_scan_kernel<<<1, kScanThreads, 0, s>>>(hist, nchunks, E, block_m, expert_offsets, tile_map, num_tiles);
+  if (nchunks > 0) {
+    const size_t smem = (size_t)(1 + kWarps) * E * sizeof(int32_t);
     align_scatter_kernel<<<nchunks, kThreads, smem, s>>>(topk_ids, S, E, hist, sorted_slot, inv_slot);
   }
   return launch_status();

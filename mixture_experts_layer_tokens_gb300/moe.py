@@ -39,6 +39,7 @@ SIGNATURES = {
     "moe_route": ([_P, _I, _I, _I, _I, _P, _P, _P], _I),
     "moe_align": ([_P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _Z, _P], _I),
     "moe_align_workspace_size": ([_I, _I, _I], _Z),
+    "moe_align_noalloc": ([_P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P], _I),
     "moe_tile_map_capacity": ([_I, _I, _I], _I),
     "moe_prepare": ([_P, _P, _P, _I, _I, _I, _I, _QCP, _P, _P, _P], _I),
     "moe_experts": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _QCP, _P, _P, _Z, _P], _I),
@@ -152,6 +153,22 @@ def moe_align(topk_ids: torch.Tensor, E: int, block_m: int = MOE_BLOCK_M, out: O
                                         _ptr(al.sorted_slot), _ptr(al.inv_slot), _ptr(al.tile_map),
                                         _ptr(al.num_tiles), _ptr(al.ws), al.ws.numel(), _stream(stream)))
     return al
+
+
+ALIGN_NOALLOC_SCRATCH_BYTES = 256 * 1024
+
+
+def moe_align_noalloc(topk_ids: torch.Tensor, E: int, out: Alignment, block_m: int = MOE_BLOCK_M,
+                      stream=None) -> Alignment:
+    """moe_align for callers that cannot allocate device memory at call time:
+    the library's own fixed scratch array stands in for the workspace (out.ws
+    is not used).  Calls that overlap on the GPU race on that array."""
+    _need(topk_ids, torch.int32, "topk_ids")
+    T, k = topk_ids.shape
+    _check("moe_align_noalloc", lib().moe_align_noalloc(
+        _ptr(topk_ids), T, k, E, block_m, _ptr(out.expert_offsets), _ptr(out.sorted_slot), _ptr(out.inv_slot),
+        _ptr(out.tile_map), _ptr(out.num_tiles), _stream(stream)))
+    return out
 
 
 def moe_prepare(a1: torch.Tensor, topk_weights: Optional[torch.Tensor], top_k: int,
