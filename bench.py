@@ -48,6 +48,8 @@ def parse():
     ap.add_argument("--workload", default="mixtral", choices=sorted(CONFIGS))
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graph", action="store_true", help="launch the step's calls one by one instead of "
+                    "replaying them as one captured CUDA graph")
     return ap.parse_args()
 
 
@@ -280,6 +282,17 @@ def run_gpu(args, ws, rank, local):
             step()
         torch.cuda.synchronize(dev)
         assert moe.moe_device_status() == moe.MOE_OK
+        graph = None
+        if not args.no_graph:
+            # the step's library calls captured once and replayed: same kernels, no per-call host work
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=stream):
+                step()
+            for _ in range(3):
+                graph.replay()
+            torch.cuda.synchronize(dev)
+            assert moe.moe_device_status() == moe.MOE_OK
+        run_step = graph.replay if graph is not None else step
 
         # ---- timed region: K steps, events on the launching stream
         clocks = ClockSampler(local) if rank == 0 else None
@@ -288,7 +301,7 @@ def run_gpu(args, ws, rank, local):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         for _ in range(args.steps):
-            step()
+            run_step()
         e1.record(stream)
         torch.cuda.synchronize(dev)
         barrier(ws)
@@ -297,38 +310,51 @@ def run_gpu(args, ws, rank, local):
         ms_max = max_over_ranks(ms, ws, dev)
         value = ws * cfg.T / (ms_max * 1e-3)
 
-        # ---- dominant unit: time it inside steps with events around its call
+        # ---- dominant unit: R back-to-back calls captured in one graph, replayed;
+        # CUDA events on the launching stream give the device time per call
+        R = 10
         if cfg.finalize_only:
             dom_name = "moe_finalize (NVFP4 out)"
             nbytes = finalize_algorithmic(cfg, True)
-            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                  for _ in range(args.steps)]
-            for a, b in ev:
-                step_obj.weights()
-                a.record(stream)
-                step_obj.finalize(True)
-                b.record(stream)
-            torch.cuda.synchronize(dev)
             flops = 0.0
+            step_obj.weights()
+
+            def dom_call():
+                step_obj.finalize(True)
         else:
-            dom_name = "moe_experts (gather + GEMM1 SiLU + GEMM2 scatter)"
+            dom_name = "moe_experts (plan + gather + GEMM1 SiLU + GEMM2 scatter)"
+            layer.forward(inp.logits, inp.a1)  # route/align/prepare state for the experts call
             counts = torch.diff(layer.al.expert_offsets).cpu().numpy()
             nbytes, flops = experts_algorithmic(cfg, counts)
-            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                  for _ in range(args.steps)]
-            for a, b in ev:
-                moe.moe_route(inp.logits, cfg.top_k, layer.scoring, layer.topk_ids, layer.topk_weights)
-                moe.moe_align(layer.topk_ids, cfg.E, out=layer.al)
-                a1q = inp.a1 if layer.passthrough else layer.a1q
-                if not layer.passthrough:
-                    moe.moe_prepare(inp.a1, layer.topk_weights, cfg.top_k, cfg.weight_on_input, cfg.quant,
-                                    layer.a1q, layer.a1q_scale)
-                a.record(stream)
-                moe.moe_experts(a1q, layer.a1q_scale, inp.w13, inp.w13_scale, inp.w2, inp.w2_scale, layer.al,
+            a1q_dom = inp.a1 if layer.passthrough else layer.a1q
+
+            def dom_call():
+                moe.moe_experts(a1q_dom, layer.a1q_scale, inp.w13, inp.w13_scale, inp.w2, inp.w2_scale, layer.al,
                                 cfg.quant, out=layer.y, ws=layer.ws)
-                b.record(stream)
+        for _ in range(3):
+            dom_call()
+        torch.cuda.synchronize(dev)
+        reps = max(1, args.steps // R)
+        if args.no_graph:
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for _ in range(reps * R):
+                dom_call()
+            b.record(stream)
+        else:
+            dom_graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(dom_graph, stream=stream):
+                for _ in range(R):
+                    dom_call()
+            dom_graph.replay()
             torch.cuda.synchronize(dev)
-        dom_ms = statistics.median([a.elapsed_time(b) for a, b in ev])
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for _ in range(reps):
+                dom_graph.replay()
+            b.record(stream)
+        torch.cuda.synchronize(dev)
+        dom_ms = a.elapsed_time(b) / (reps * R)
         achieved = nbytes / (dom_ms * 1e-3) / 1e9
         roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
                     "frac": round(achieved / hbm_peak, 4), "traffic": None, "kernel": dom_name,
@@ -347,11 +373,20 @@ def run_gpu(args, ws, rank, local):
             d_logits = torch.empty_like(inp.logits)
             d_a1 = torch.empty_like(inp.a1)
 
+            e2e_graph = None
+            if not args.no_graph:
+                e2e_graph = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(e2e_graph, stream=stream):
+                    layer.forward(d_logits, d_a1)
+
             def e2e_step():
                 d_logits.copy_(h_logits, non_blocking=True)
                 d_a1.copy_(h_a1, non_blocking=True)
-                out = layer.forward(d_logits, d_a1)
-                h_out.copy_(out, non_blocking=True)
+                if e2e_graph is not None:
+                    e2e_graph.replay()
+                else:
+                    layer.forward(d_logits, d_a1)
+                h_out.copy_(layer.out, non_blocking=True)
             for _ in range(args.warmup):
                 e2e_step()
             torch.cuda.synchronize(dev)
@@ -388,6 +423,7 @@ def run_gpu(args, ws, rank, local):
             "vs_baseline": None, "dtype": "fp8" if cfg.quant == "fp8" else "bf16", "data": "synthetic",
             "config": {"workload": cfg.description, "T": cfg.T, "H": cfg.H, "I": cfg.I, "E": cfg.E,
                        "top_k": cfg.top_k, "parallelism": f"replicas{ws}",
+                       "launch": "cuda_graph" if not args.no_graph else "eager",
                        "l2": "no flush: each step streams the expert weights (larger than the 129 MB L2)"
                        if not cfg.finalize_only else "inputs smaller than L2 (finalize-only workload)"},
             "roofline": roofline, "cpu_baseline": cpu, "clocks": clk, "e2e": e2e,

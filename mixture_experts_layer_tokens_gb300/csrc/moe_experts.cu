@@ -7,33 +7,47 @@
 // For the fp8 G(128) format each token carries one scale per 128 channels and
 // each weight one scale per 128x128 block.
 //
-// Three launches on the caller's stream:
+// Launches on the caller's stream:
+//   plan   : one block turns the 128-row tile map into the unit groups below and
+//            clears the split-unit flags of both GEMMs
 //   gather : a1q rows -> A rows in expert order (sorted_slot), fp8 scales
 //            transposed to [K/128][rows]; skipped for the bf16 identity case
 //   gemm1  : h = silu(A w13_g^T) * (A w13_u^T), bf16 or fp8 G(128) requantised
 //   gemm2  : y[sorted_slot[p]] = h_p w2^T, bf16 rows scattered token-major
 //
-// GEMM design (one persistent CTA per SM, 128 x 256 output tile per work item):
-//   warp 0      TMA producer: A tile 128 x 128 B and two B tiles 128 x 128 B per
-//               stage (4 stages of 48 KB), 128-byte swizzle;
-//   warp 1      allocates the 512 TMEM columns and issues tcgen05.mma from one
-//               lane (M=128, N=256, fp32 accumulate), commits to mbarriers;
-//   warps 2..   epilogue: tcgen05.ld of the accumulator rows (one TMEM lane per
-//               thread), activation / requantisation / scatter, global stores.
-// bf16: two 256-column accumulators ping-pong between work items, so the
-// epilogue of one item overlaps the main loop of the next.
-// fp8: the block scales change every 128-deep K block, so the MMA writes each K
-// block into one of two 256-column partial accumulators and eight epilogue
-// warps add partial * (a_scale * w_scale) into fp32 registers while the MMA
-// fills the other partial -- software promotion, since the scales are fp32.
+// GEMM design (one persistent CTA per SM):
+//   unit   one weight tile (256 rows of w13 -- 128 gate + 128 up -- or of w2)
+//          times a group of MG 128-row M tiles of one expert.  MG = 2 (bf16
+//          only, when units are few and the iterations are split, see
+//          schedule) loads the weight tile once per K step for up to 256 rows;
+//          MG = 1 otherwise (the fp8 register promotion holds one 128 x 256
+//          tile).  Units run expert by expert, then N tile, then group.
+//   warp 0 TMA producer: MG A tiles + two 128-row B tiles per stage, 128-byte
+//          swizzle (MG = 2: 3 stages x 64 KB; MG = 1: 4 stages x 48 KB).
+//   warp 1 allocates the 512 TMEM columns and issues tcgen05.mma from one lane
+//          (M=128, N=256 per M tile, fp32 accumulate).
+//   warps 2-9  epilogue: tcgen05.ld of accumulator rows (one TMEM lane per
+//          thread); MG = 2: warp = (lane quarter, M tile); MG = 1: warp = (lane
+//          quarter, column half); bf16 MG = 1 ping-pongs two accumulators so
+//          one unit's epilogue overlaps the next unit's main loop; because the
+//          fp8 block scales change
+//          every 128-deep K block the MMA writes each K block into one of two
+//          partial accumulators that the epilogue scales and adds into fp32
+//          registers (software promotion; the scales are fp32).
+//   schedule  with at least 4 units per CTA, units are dealt round-robin and
+//          units that share a weight tile run side by side on neighbouring
+//          SMs; with fewer (decode, deep-K GEMM2 tails) the (unit, K block)
+//          iterations are split into equal contiguous ranges, one per CTA
+//          ("stream-K").  A unit cut by a range boundary is finished by the CTA
+//          holding its first K blocks: it waits (bounded) for the later
+//          segments' fp32 partials and adds them in segment order, so results
+//          do not depend on timing.  Those later segments are always the first
+//          work of their CTAs and never wait, so the waits cannot form a cycle
+//          while all CTAs are resident.
 //
-// Work items are ordered expert by expert, then by N tile, then by M tile, so
-// the M tiles of one expert that share a weight tile run side by side (the
-// weight tile is read from HBM once) and an expert's activations stay in L2
-// while its N tiles stream past.
-//
-// Every wait is bounded (see mbar_wait): a wait that gives up records
-// MOE_ERR_TIMEOUT and the CTA unwinds, frees its TMEM and returns.
+// Every wait is bounded: a wait that gives up records MOE_ERR_TIMEOUT and the
+// CTA unwinds, drains its in-flight copies and MMAs, frees its TMEM and
+// returns.
 #include <cudaTypedefs.h>
 
 #include <algorithm>
@@ -43,32 +57,46 @@
 namespace moe {
 namespace {
 
-constexpr int BM = MOE_BLOCK_M;   // 128 rows per tile = TMEM lanes
-constexpr int BN = 256;           // MMA N
-constexpr int BKB = 128;          // bytes of K per stage (one 128-byte swizzle row)
-constexpr int STAGES = 4;
-constexpr int A_BYTES = BM * BKB;             // 16 KB
-constexpr int B_HALF_BYTES = 128 * BKB;       // 16 KB
-constexpr int STAGE_BYTES = A_BYTES + 2 * B_HALF_BYTES;
+constexpr int BM = MOE_BLOCK_M;  // 128 rows per M tile = TMEM lanes
+constexpr int BN = 256;          // MMA N
+constexpr int BKB = 128;         // bytes of K per stage (one 128-byte swizzle row)
+constexpr int A_BYTES = BM * BKB;        // 16 KB per M tile
+constexpr int B_HALF_BYTES = 128 * BKB;  // 16 KB per 128 weight rows
 constexpr int TMEM_COLS = 512;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*barriers, exchange*/ + 1024 /*alignment*/ + 2048;
+// epilogue warps: bf16 4 (one per TMEM lane quarter, all columns of its rows);
+// fp8 8 (two per lane quarter, half of the columns each: the promotion keeps
+// 128 fp32 accumulators per thread)
+template <bool kFP8>
+struct Warps {
+  static constexpr int EPI = kFP8 ? 8 : 4;
+  static constexpr int THREADS = 64 + EPI * 32;
+  static constexpr int EPI_THREADS = EPI * 32;
+};
+// Units are split across CTAs (stream-K) only when there are fewer than half as
+// many units as CTAs (decode-sized work); otherwise whole units are dealt
+// round-robin, where a short tail costs less than the split's fixed costs.
+constexpr int SPLIT_BELOW_UNITS_PER_CTA_X2 = 1;
+constexpr int L2_PREFETCH_AHEAD = 8;     // weight tiles prefetched into L2 ahead of the TMA loads
 
 enum Kind { kGemm1 = 0, kGemm2 = 1 };
 
-template <bool kFP8>
+template <bool kFP8, int kMG>
 struct Cfg {
-  static constexpr int kEpiWarps = kFP8 ? 8 : 4;
-  static constexpr int kThreads = 64 + kEpiWarps * 32;
+  static constexpr int MG = kMG;  // M tiles per unit
+  static constexpr int STAGES = kMG == 2 ? 3 : 4;
+  static constexpr int STAGE_BYTES = MG * A_BYTES + 2 * B_HALF_BYTES;
   static constexpr int kElemBytes = kFP8 ? 1 : 2;
   static constexpr int kBK = BKB / kElemBytes;  // K elements per stage
   static constexpr int kMmaK = kFP8 ? 32 : 16;  // K per tcgen05.mma
   static constexpr uint32_t kIdesc = make_idesc(kFP8 ? 0u : 1u, BM, BN);
+  static constexpr int PARTIAL_FLOATS = MG * BM * BN;  // one split-unit partial
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 4096 /*barriers, exchange*/ + 1024 /*align*/;
 };
 
 struct GemmParams {
   const int32_t* offsets;      // [E + 1]
-  const int32_t* tile_map;     // [num_tiles][2] (expert, first row)
-  const int32_t* num_tiles;    // [1]
+  const int32_t* group_map;    // [groups][2] (expert, first row), built by plan_kernel
+  const int32_t* num_groups;   // [1]
   const int32_t* sorted_slot;  // gemm2 scatter target rows; NULL = identity
   int K;                       // contraction depth (H for gemm1, I for gemm2)
   int NT;                      // N tiles per expert
@@ -80,48 +108,160 @@ struct GemmParams {
   const float* w_scale;        // fp8: [E][b_rows/128][K/128]
   void* out;                   // gemm1: h [rows][I]; gemm2: y [T*k][H] bf16
   float* out_scale_t;          // gemm1 fp8: [I/128][s_pad]
+  int allow_split;             // decode-sized problem: few units may be split across CTAs (bf16 only)
+  int* flags;                  // [units] arrivals on split units (zeroed by plan_kernel)
+  float* partials;             // [gridDim.x][PARTIAL_FLOATS] one split-segment partial per CTA
 };
 
-struct WorkItem {
-  int e, row0, row_end, n;
+struct Unit {
+  int e, row0, row_end, n;  // rows [row0, row_end) of expert e (at most MG*BM), N tile n
 };
 
-__device__ __forceinline__ WorkItem decode(const GemmParams& p, int w) {
-  WorkItem it;
-  const int mt_base = w / p.NT;  // an M tile of the item's expert
-  it.e = __ldg(p.tile_map + 2 * mt_base);
-  const int r0 = __ldg(p.tile_map + 2 * mt_base + 1);
+template <int MG>
+__device__ __forceinline__ Unit decode(const GemmParams& p, int u) {
+  Unit it;
+  const int gb = u / p.NT;  // a group of the unit's expert
+  it.e = __ldg(p.group_map + 2 * gb);
+  const int r0 = __ldg(p.group_map + 2 * gb + 1);
   const int off = __ldg(p.offsets + it.e);
-  it.row_end = __ldg(p.offsets + it.e + 1);
-  const int mstart = mt_base - (r0 - off) / BM;
-  const int mcnt = (it.row_end - off + BM - 1) / BM;
-  const int local = w - mstart * p.NT;
-  it.n = local / mcnt;
-  it.row0 = off + (local % mcnt) * BM;
+  const int end = __ldg(p.offsets + it.e + 1);
+  const int gstart = gb - (r0 - off) / (MG * BM);
+  const int gcnt = (end - off + MG * BM - 1) / (MG * BM);
+  const int local = u - gstart * p.NT;
+  it.n = local / gcnt;
+  it.row0 = off + (local % gcnt) * (MG * BM);
+  it.row_end = min(it.row0 + MG * BM, end);
   return it;
 }
+
+// The segments (unit, K blocks [kb0, kb1)) one CTA processes, in order.
+struct Sched {
+  bool rr;
+  int U, KB, G, c;
+  long long i, i1, total;
+  int u_next;
+  __device__ void init(int units, int kb, int grid, int cta, bool allow_split) {
+    U = units;
+    KB = kb;
+    c = cta;
+    total = (long long)units * kb;
+    rr = !allow_split || 2 * units >= SPLIT_BELOW_UNITS_PER_CTA_X2 * grid;
+    // stream-K uses at most one CTA per iteration, so that no range is empty
+    G = rr ? grid : (int)std::min<long long>(grid, std::max<long long>(total, 1));
+    u_next = cta;
+    if (rr || cta < G) {
+      i = total * cta / G;
+      i1 = total * (cta + 1) / G;
+    } else {
+      i = i1 = 0;
+    }
+  }
+  __device__ bool next(int& u, int& kb0, int& kb1) {
+    if (rr) {
+      if (u_next >= U) return false;
+      u = u_next;
+      kb0 = 0;
+      kb1 = KB;
+      u_next += G;
+      return true;
+    }
+    if (i >= i1) return false;
+    u = (int)(i / KB);
+    kb0 = (int)(i % KB);
+    kb1 = (int)std::min<long long>(KB, kb0 + (i1 - i));
+    i += kb1 - kb0;
+    return true;
+  }
+  // CTA whose range holds iteration `it` (stream-K mode)
+  __device__ int cta_of(long long it) const { return (int)(((it + 1) * G - 1) / total); }
+};
 
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity) {
   return __all_sync(0xffffffffu, mbar_wait(bar, parity));
 }
 
+// Bounded wait until *flag >= target (acquire).  False on timeout.
+__device__ __forceinline__ bool flag_wait(const int* flag, int target) {
+  auto load = [&]() {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
+    return v;
+  };
+  if (load() >= target) return true;
+  const uint64_t t0 = global_ns();
+  while (true) {
+    __nanosleep(64);
+    if (load() >= target) return true;
+    if (status_failed()) return false;
+    if (global_ns() - t0 > kWaitLimitNs) {
+      record_timeout();
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ float4 ldcg4(const float* p) { return __ldcg(reinterpret_cast<const float4*>(p)); }
+
+// Epilogue threads of the CTA that finishes a split unit: one thread polls the
+// unit's arrival count (the other threads polling the same L2 line would
+// crowd it), then releases the rest through a shared-memory barrier.  A CTA
+// finishes at most one split unit per launch (its last segment), so the
+// barrier's phase is always 0.  Bounded: false after a timeout.
+__device__ __forceinline__ bool wait_split_partials(const int* flag, int target, uint64_t* fixbar) {
+  if ((threadIdx.x >> 5) == 2) {
+    // the whole first epilogue warp polls in step (one lane loads, a shuffle shares
+    // the value): a lone polling lane would be starved by its warp-mates' waits
+    const int lane = threadIdx.x & 31;
+    const uint64_t t0 = global_ns();
+    while (true) {
+      int v = 0;
+      if (lane == 0) asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
+      v = __shfl_sync(0xffffffffu, v, 0);
+      if (v >= target) break;
+      if (status_failed()) break;
+      if (global_ns() - t0 > kWaitLimitNs) {
+        if (lane == 0) record_timeout();
+        break;
+      }
+      __nanosleep(100);
+    }
+    if (lane == 0) mbar_arrive(fixbar);  // on failure the status word is set; release the others anyway
+  }
+  const bool ok = mbar_wait(fixbar, 0);
+  return __all_sync(0xffffffffu, ok && !status_failed());
+}
+
+// A later segment's partial is written: every lane fences its own stores, then
+// one atomic per warp counts the warp's 32 threads.
+__device__ __forceinline__ void signal_split_partial(int* flag) {
+  __threadfence();
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) atomicAdd(flag, 32);
+}
+
 __device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + __expf(-g)) * u; }
 
-template <bool kFP8, int kKind>
-__global__ void __launch_bounds__(Cfg<kFP8>::kThreads, 1)
+template <bool kFP8, int kKind, int kMG>
+__global__ void __launch_bounds__(Warps<kFP8>::THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const GemmParams p) {
-  using C = Cfg<kFP8>;
+  using C = Cfg<kFP8, kMG>;
+  constexpr int EPI_WARPS = Warps<kFP8>::EPI;
+  constexpr int EPI_THREADS = Warps<kFP8>::EPI_THREADS;
+  constexpr int MG = C::MG;
+  constexpr int STAGES = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  uint8_t* ctrl = smem + STAGES * C::STAGE_BYTES;
+  uint64_t* full = reinterpret_cast<uint64_t*>(ctrl);
   uint64_t* empty = full + STAGES;
-  uint64_t* tfull = empty + STAGES;   // [2] accumulator ready
-  uint64_t* tempty = tfull + 2;       // [2] accumulator drained
-  uint64_t* xbar = tempty + 2;        // fp8 gemm1: row amax exchange between column halves
-  uint64_t* drain = xbar + 1;         // teardown after a failed wait: MMA pipe drained
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
-  float* amax_x = reinterpret_cast<float*>(smem + STAGES * STAGE_BYTES + 256);  // [2 items][2 halves][BM]
+  uint64_t* tfull = empty + STAGES;  // [2] accumulator ready
+  uint64_t* tempty = tfull + 2;      // [2] accumulator drained
+  uint64_t* xbar = tempty + 2;       // fp8 gemm1: row amax exchange between column halves
+  uint64_t* drain = xbar + 1;        // teardown after a failed wait
+  uint64_t* fixbar = drain + 1;      // stream-K: the later segments' partials of this CTA's split unit are in
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(fixbar + 1);
+  float* amax_x = reinterpret_cast<float*>(ctrl + 256);  // [2 items][2 halves][BM]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -131,10 +271,11 @@ __global__ void __launch_bounds__(Cfg<kFP8>::kThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], C::kEpiWarps * 32);
+      mbar_init(&tempty[a], EPI_WARPS);  // one arrival per epilogue warp
     }
-    mbar_init(xbar, C::kEpiWarps * 32);
+    mbar_init(xbar, EPI_WARPS);
     mbar_init(drain, 1);
+    mbar_init(fixbar, 1);
     fence_mbar_init();
     prefetch_tensormap(&tmA);
     prefetch_tensormap(&tmB);
@@ -148,36 +289,66 @@ __global__ void __launch_bounds__(Cfg<kFP8>::kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  const int total = __ldg(p.num_tiles) * p.NT;
+  const int units = __ldg(p.num_groups) * p.NT;
   const int KB = p.K / C::kBK;
+  Sched sched;
+  // fp8 units are never split: its register promotion leaves no room for the split logic
+  constexpr bool kSplit = !kFP8;
+  sched.init(units, KB, gridDim.x, blockIdx.x, kSplit && p.allow_split);
+  int u, kb0, kb1;
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     const uint64_t pol_a = policy_evict_last();
     const uint64_t pol_b = policy_evict_first();
+    // L2 prefetch cursor: walks the same (unit, K block) sequence L2_PREFETCH_AHEAD
+    // iterations ahead of the loads (lane 0 only), so more weight bytes are in
+    // flight from HBM than the shared-memory stages hold
+    Sched pfs = sched;
+    int pf_kb = 0, pf_kb1 = 0, pf_r0 = 0, pf_r1 = 0;
+    auto prefetch_next = [&]() {
+      if (pf_kb >= pf_kb1) {
+        int pu;
+        if (!pfs.next(pu, pf_kb, pf_kb1)) return;
+        const Unit pit = decode<MG>(p, pu);
+        pf_r0 = kKind == kGemm1 ? pit.e * p.b_rows + pit.n * 128 : pit.e * p.b_rows + pit.n * 256;
+        pf_r1 = kKind == kGemm1 ? pit.e * p.b_rows + p.I + pit.n * 128 : pf_r0 + 128;
+      }
+      tma_prefetch_2d(&tmB, pf_kb * C::kBK, pf_r0);
+      tma_prefetch_2d(&tmB, pf_kb * C::kBK, pf_r1);
+      ++pf_kb;
+    };
+    // (round-robin schedules already keep every SM streaming whole units; there the
+    // extra requests only cost, so the cursor runs in stream-K mode alone)
+    const bool l2_prefetch = !sched.rr;
+    if (lane == 0 && l2_prefetch)
+      for (int i = 0; i < L2_PREFETCH_AHEAD; ++i) prefetch_next();
     int stage = 0;
     uint32_t phase = 0;
     long long fills = 0;
     bool ok = true;
-    for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
-      const WorkItem it = decode(p, w);
+    while (ok && sched.next(u, kb0, kb1)) {
+      const Unit it = decode<MG>(p, u);
+      const int mcnt = (it.row_end - it.row0 + BM - 1) / BM;
       int brow0, brow1;
       if (kKind == kGemm1) {
-        brow0 = it.e * p.b_rows + it.n * 128;           // gate rows
-        brow1 = it.e * p.b_rows + p.I + it.n * 128;     // up rows
+        brow0 = it.e * p.b_rows + it.n * 128;        // gate rows
+        brow1 = it.e * p.b_rows + p.I + it.n * 128;  // up rows
       } else {
         brow0 = it.e * p.b_rows + it.n * 256;
         brow1 = brow0 + 128;
       }
-      for (int kb = 0; kb < KB; ++kb) {
+      for (int kb = kb0; kb < kb1; ++kb) {
         if (!(ok = warp_wait(&empty[stage], phase ^ 1))) break;
         if (lane == 0) {
-          uint8_t* sA = smem + stage * STAGE_BYTES;
-          mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
+          uint8_t* sA = smem + stage * C::STAGE_BYTES;
+          uint8_t* sB = sA + MG * A_BYTES;
+          mbar_arrive_expect_tx(&full[stage], mcnt * A_BYTES + 2 * B_HALF_BYTES);
           const int kx = kb * C::kBK;
-          tma_load_2d(sA, &tmA, kx, it.row0, &full[stage], pol_a);
-          tma_load_2d(sA + A_BYTES, &tmB, kx, brow0, &full[stage], pol_b);
-          tma_load_2d(sA + A_BYTES + B_HALF_BYTES, &tmB, kx, brow1, &full[stage], pol_b);
+          for (int m = 0; m < mcnt; ++m) tma_load_2d(sA + m * A_BYTES, &tmA, kx, it.row0 + m * BM, &full[stage], pol_a);
+          tma_load_2d(sB, &tmB, kx, brow0, &full[stage], pol_b);
+          tma_load_2d(sB + B_HALF_BYTES, &tmB, kx, brow1, &full[stage], pol_b);
+          if (l2_prefetch) prefetch_next();
         }
         __syncwarp();
         ++fills;
@@ -188,7 +359,7 @@ __global__ void __launch_bounds__(Cfg<kFP8>::kThreads, 1)
       }
     }
     if (status_failed() && lane == 0) {
-      // wait (bounded) for the copies this CTA still has in flight: the last fill of each stage
+      // wait (bounded) for the copies still in flight: the last fill of each stage
       for (long long i = fills - 1; i >= 0 && i >= fills - STAGES; --i)
         mbar_wait(&full[i % STAGES], (uint32_t)((i / STAGES) & 1), false, 100000000ull);
     }
@@ -197,15 +368,19 @@ __global__ void __launch_bounds__(Cfg<kFP8>::kThreads, 1)
     // ------------------------------------------------------------ MMA issuer
     int stage = 0;
     uint32_t phase = 0;
+    // fp8: ping-pong partial per K block; bf16 MG=1: ping-pong accumulator per
+    // unit; bf16 MG=2: one accumulator set of MG tiles
     int acc = 0;
     uint32_t acc_phase = 0;
     bool ok = true;
-    for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
+    while (ok && sched.next(u, kb0, kb1)) {
+      const Unit it = decode<MG>(p, u);
+      const int mcnt = (it.row_end - it.row0 + BM - 1) / BM;
       if (!kFP8) {
         if (!(ok = warp_wait(&tempty[acc], acc_phase ^ 1))) break;
         tc_fence_after();
       }
-      for (int kb = 0; kb < KB; ++kb) {
+      for (int kb = kb0; kb < kb1; ++kb) {
         if (kFP8) {
           if (!(ok = warp_wait(&tempty[acc], acc_phase ^ 1))) break;
           tc_fence_after();
@@ -213,17 +388,19 @@ __global__ void __launch_bounds__(Cfg<kFP8>::kThreads, 1)
         if (!(ok = warp_wait(&full[stage], phase))) break;
         tc_fence_after();
         if (lane == 0) {
-          const uint32_t a0 = smem_u32(smem + stage * STAGE_BYTES);
-          const uint32_t b0 = a0 + A_BYTES;
-          const uint32_t d = tmem + acc * BN;
+          const uint32_t a0 = smem_u32(smem + stage * C::STAGE_BYTES);
+          const uint32_t b0 = a0 + MG * A_BYTES;
+          for (int m = 0; m < mcnt; ++m) {
+            const uint32_t d = tmem + ((kFP8 || MG == 1) ? acc * BN : m * BN);
 #pragma unroll
-          for (int kk = 0; kk < BKB / (C::kMmaK * C::kElemBytes); ++kk) {
-            const uint32_t koff = kk * C::kMmaK * C::kElemBytes;
-            const uint32_t accum = kFP8 ? (kk > 0) : (kb > 0 || kk > 0);
-            if (kFP8)
-              mma_fp8(d, sw128_desc(a0 + koff), sw128_desc(b0 + koff), C::kIdesc, accum);
-            else
-              mma_bf16(d, sw128_desc(a0 + koff), sw128_desc(b0 + koff), C::kIdesc, accum);
+            for (int kk = 0; kk < BKB / (C::kMmaK * C::kElemBytes); ++kk) {
+              const uint32_t koff = kk * C::kMmaK * C::kElemBytes;
+              const uint32_t accum = kFP8 ? (kk > 0) : (kb > kb0 || kk > 0);
+              if (kFP8)
+                mma_fp8(d, sw128_desc(a0 + m * A_BYTES + koff), sw128_desc(b0 + koff), C::kIdesc, accum);
+              else
+                mma_bf16(d, sw128_desc(a0 + m * A_BYTES + koff), sw128_desc(b0 + koff), C::kIdesc, accum);
+            }
           }
           tc_commit(&empty[stage]);
           if (kFP8) tc_commit(&tfull[acc]);
@@ -241,90 +418,148 @@ __global__ void __launch_bounds__(Cfg<kFP8>::kThreads, 1)
       if (!kFP8 && ok) {
         if (lane == 0) tc_commit(&tfull[acc]);
         __syncwarp();
-        acc ^= 1;
+        if (MG == 1) acc ^= 1;
         if (acc == 0) acc_phase ^= 1;
       }
     }
   } else {
     // ------------------------------------------------------------ epilogue
     const int q = warp - 2;
-    const int quarter = warp & 3;      // TMEM lanes this warp may access
-    const int half = q / 4;            // fp8: which half of the columns
-    const int r = quarter * 32 + lane; // tile row == TMEM lane
+    const int quarter = warp & 3;        // TMEM lanes this warp may access
+    const int sub = q / 4;               // fp8: column half (bf16: always 0)
+    const int r = quarter * 32 + lane;   // row within an M tile == TMEM lane
     const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
+    float* my_partial = p.partials + (size_t)blockIdx.x * C::PARTIAL_FLOATS;  // [MG][BM][BN] (bf16) / [BM][2][128] (fp8)
     int acc = 0;
     uint32_t acc_phase = 0;
     int xbuf = 0;
     uint32_t xphase = 0;
     bool ok = true;
-    for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
-      const WorkItem it = decode(p, w);
-      const int prow = it.row0 + r;
+    while (ok && sched.next(u, kb0, kb1)) {
+      const Unit it = decode<MG>(p, u);
+      const int prow = it.row0 + r;  // row of the first M tile (fp8: the only one)
       const bool valid = prow < it.row_end;
+      // split-unit role: 0 whole, 1 first segment (finishes the unit), 2 later segment
+      const int role = !kSplit ? 0 : (kb0 == 0 && kb1 == KB) ? 0 : (kb0 == 0 ? 1 : 2);
+      int c_first = 0, c_last = -1;
+      if (role == 1) {
+        c_first = blockIdx.x + 1;
+        c_last = sched.cta_of((long long)u * KB + KB - 1);
+      }
+      // thread-private slot of a split-unit partial: bf16 256 columns of (M tile m, row r) at
+      // poff + m * BM * 256; fp8 128 values of (r, half)
+      const size_t poff = kFP8 ? ((size_t)r * 2 + sub) * 128 : (size_t)r * 256;
+
       if (!kFP8) {
+        // one warp per TMEM lane quarter: rows r of each M tile of the group, 8 chunks of
+        // 32 columns (gemm1: chunks 0-3 gate, 4-7 up)
         if (!(ok = warp_wait(&tfull[acc], acc_phase))) break;
         tc_fence_after();
-        const uint32_t tb = tmem + lane_addr + acc * BN;
-        if (kKind == kGemm1) {
-          __nv_bfloat16* hrow = static_cast<__nv_bfloat16*>(p.out) + (size_t)prow * p.I + it.n * 128;
+        if (role == 1) ok = wait_split_partials(p.flags + u, (c_last - c_first + 1) * EPI_THREADS, fixbar);
+        const int mcnt = (it.row_end - it.row0 + BM - 1) / BM;
+        for (int m = 0; m < mcnt; ++m) {
+          const int mrow = prow + m * BM;
+          const bool mvalid = mrow < it.row_end;
+          const size_t mpoff = poff + (size_t)m * BM * 256;
+          const uint32_t tb = tmem + lane_addr + (MG == 2 ? m * BN : acc * BN);
+          if (role == 2) {
+            // later segment: park the fp32 partial for the CTA that finishes the unit
 #pragma unroll 1
-          for (int c = 0; c < 4; ++c) {
-            float g[32], u[32];
-            tmem_ld32(tb + c * 32, g);
-            tmem_ld32(tb + 128 + c * 32, u);
-            tmem_ld_wait();
-            if (valid) {
-              uint4* dst = reinterpret_cast<uint4*>(hrow + c * 32);
+            for (int c = 0; c < 8; ++c) {
+              float v[32];
+              tmem_ld32(tb + c * 32, v);
+              tmem_ld_wait();
+              if (mvalid) {
+                float4* dst = reinterpret_cast<float4*>(my_partial + mpoff + c * 32);
 #pragma unroll
-              for (int v = 0; v < 4; ++v) {
-                uint4 o;
-                o.x = pack_bf16x2(silu_mul(g[8 * v + 0], u[8 * v + 0]), silu_mul(g[8 * v + 1], u[8 * v + 1]));
-                o.y = pack_bf16x2(silu_mul(g[8 * v + 2], u[8 * v + 2]), silu_mul(g[8 * v + 3], u[8 * v + 3]));
-                o.z = pack_bf16x2(silu_mul(g[8 * v + 4], u[8 * v + 4]), silu_mul(g[8 * v + 5], u[8 * v + 5]));
-                o.w = pack_bf16x2(silu_mul(g[8 * v + 6], u[8 * v + 6]), silu_mul(g[8 * v + 7], u[8 * v + 7]));
-                dst[v] = o;
+                for (int j = 0; j < 8; ++j) __stcg(dst + j, make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
               }
             }
-          }
-        } else {
-          const int f = valid ? (p.sorted_slot ? __ldg(p.sorted_slot + prow) : prow) : 0;
-          __nv_bfloat16* yrow = static_cast<__nv_bfloat16*>(p.out) + (size_t)f * p.H + it.n * 256;
-          const int ncols = min(256, p.H - it.n * 256);
+          } else if (kKind == kGemm1) {
+            __nv_bfloat16* hrow = static_cast<__nv_bfloat16*>(p.out) + (size_t)mrow * p.I + it.n * 128;
 #pragma unroll 1
-          for (int c = 0; c < 8; ++c) {
-            float v[32];
-            tmem_ld32(tb + c * 32, v);
-            tmem_ld_wait();
-            if (valid && c * 32 < ncols) {
-              uint4* dst = reinterpret_cast<uint4*>(yrow + c * 32);
+            for (int c = 0; c < 4; ++c) {
+              float g[32], uu[32];
+              tmem_ld32(tb + c * 32, g);
+              tmem_ld32(tb + 128 + c * 32, uu);
+              tmem_ld_wait();
+              if (role == 1 && mvalid && ok) {
+                for (int cc = c_first; cc <= c_last; ++cc) {
+                  const float* src = p.partials + (size_t)cc * C::PARTIAL_FLOATS + mpoff;
 #pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                uint4 o;
-                o.x = pack_bf16x2(v[8 * j + 0], v[8 * j + 1]);
-                o.y = pack_bf16x2(v[8 * j + 2], v[8 * j + 3]);
-                o.z = pack_bf16x2(v[8 * j + 4], v[8 * j + 5]);
-                o.w = pack_bf16x2(v[8 * j + 6], v[8 * j + 7]);
-                dst[j] = o;
+                  for (int j = 0; j < 8; ++j) {
+                    const float4 a = ldcg4(src + c * 32 + 4 * j), b = ldcg4(src + 128 + c * 32 + 4 * j);
+                    g[4 * j] += a.x; g[4 * j + 1] += a.y; g[4 * j + 2] += a.z; g[4 * j + 3] += a.w;
+                    uu[4 * j] += b.x; uu[4 * j + 1] += b.y; uu[4 * j + 2] += b.z; uu[4 * j + 3] += b.w;
+                  }
+                }
+              }
+              if (mvalid) {
+                uint4* dst = reinterpret_cast<uint4*>(hrow + c * 32);
+#pragma unroll
+                for (int v = 0; v < 4; ++v) {
+                  uint4 o;
+                  o.x = pack_bf16x2(silu_mul(g[8 * v + 0], uu[8 * v + 0]), silu_mul(g[8 * v + 1], uu[8 * v + 1]));
+                  o.y = pack_bf16x2(silu_mul(g[8 * v + 2], uu[8 * v + 2]), silu_mul(g[8 * v + 3], uu[8 * v + 3]));
+                  o.z = pack_bf16x2(silu_mul(g[8 * v + 4], uu[8 * v + 4]), silu_mul(g[8 * v + 5], uu[8 * v + 5]));
+                  o.w = pack_bf16x2(silu_mul(g[8 * v + 6], uu[8 * v + 6]), silu_mul(g[8 * v + 7], uu[8 * v + 7]));
+                  dst[v] = o;
+                }
+              }
+            }
+          } else {
+            const int f = mvalid ? (p.sorted_slot ? __ldg(p.sorted_slot + mrow) : mrow) : 0;
+            __nv_bfloat16* yrow = static_cast<__nv_bfloat16*>(p.out) + (size_t)f * p.H + it.n * 256;
+            const int ncols = min(256, p.H - it.n * 256);
+#pragma unroll 1
+            for (int c = 0; c < 8; ++c) {
+              float v[32];
+              tmem_ld32(tb + c * 32, v);
+              tmem_ld_wait();
+              if (role == 1 && mvalid && ok) {
+                for (int cc = c_first; cc <= c_last; ++cc) {
+                  const float* src = p.partials + (size_t)cc * C::PARTIAL_FLOATS + mpoff + c * 32;
+#pragma unroll
+                  for (int j = 0; j < 8; ++j) {
+                    const float4 a = ldcg4(src + 4 * j);
+                    v[4 * j] += a.x; v[4 * j + 1] += a.y; v[4 * j + 2] += a.z; v[4 * j + 3] += a.w;
+                  }
+                }
+              }
+              if (mvalid && c * 32 < ncols) {
+                uint4* dst = reinterpret_cast<uint4*>(yrow + c * 32);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                  uint4 o;
+                  o.x = pack_bf16x2(v[8 * j + 0], v[8 * j + 1]);
+                  o.y = pack_bf16x2(v[8 * j + 2], v[8 * j + 3]);
+                  o.z = pack_bf16x2(v[8 * j + 4], v[8 * j + 5]);
+                  o.w = pack_bf16x2(v[8 * j + 6], v[8 * j + 7]);
+                  dst[j] = o;
+                }
               }
             }
           }
         }
+        if (role == 2) signal_split_partial(p.flags + u);
         tc_fence_before();
-        mbar_arrive(&tempty[acc]);
-        acc ^= 1;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[acc]);
+        if (MG == 1) acc ^= 1;
         if (acc == 0) acc_phase ^= 1;
       } else {
         // fp8: promote every K block's partial into registers.
         // gemm1: this thread owns h columns [64 half, +64): gate TMEM columns
         //        [64 half, +64) and up columns [128 + 64 half, +64).
         // gemm2: this thread owns output columns [128 half, +128).
+        const int half = sub;
         float accv[128];
 #pragma unroll
         for (int i = 0; i < 128; ++i) accv[i] = 0.f;
         const int KBs = p.K / 128;
         const int nbw = p.b_rows / 128;
         const float* sw = p.w_scale + (size_t)it.e * nbw * KBs;
-        int wb0, wb1;  // weight-scale block rows for column groups 0..63 / 64..127 of accv
+        int wb0, wb1;  // weight-scale block rows of accv[0..63] / accv[64..127]
         if (kKind == kGemm1) {
           wb0 = it.n;
           wb1 = p.I / 128 + it.n;
@@ -332,7 +567,7 @@ __global__ void __launch_bounds__(Cfg<kFP8>::kThreads, 1)
           wb0 = wb1 = min(2 * it.n + half, nbw - 1);
         }
         const float* sa = p.a_scale_t + it.row0 + r;  // + kb * s_pad
-        for (int kb = 0; kb < KB; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!(ok = warp_wait(&tfull[acc], acc_phase))) break;
           tc_fence_after();
           const float a_s = __ldg(sa + (size_t)kb * p.s_pad);
@@ -352,11 +587,36 @@ __global__ void __launch_bounds__(Cfg<kFP8>::kThreads, 1)
             for (int i = 0; i < 32; ++i) accv[32 * c + i] = fmaf(v[i], sc, accv[32 * c + i]);
           }
           tc_fence_before();
-          mbar_arrive(&tempty[acc]);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&tempty[acc]);
           acc ^= 1;
           if (acc == 0) acc_phase ^= 1;
         }
         if (!ok) break;
+        if (role == 2) {
+          if (valid) {
+            float4* dst = reinterpret_cast<float4*>(my_partial + poff);
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              __stcg(dst + j, make_float4(accv[4 * j], accv[4 * j + 1], accv[4 * j + 2], accv[4 * j + 3]));
+          }
+          signal_split_partial(p.flags + u);
+          continue;
+        }
+        if (role == 1) {
+          ok = wait_split_partials(p.flags + u, (c_last - c_first + 1) * EPI_THREADS, fixbar);
+          if (!ok) break;
+          if (valid) {
+            for (int cc = c_first; cc <= c_last; ++cc) {
+              const float* src = p.partials + (size_t)cc * C::PARTIAL_FLOATS + poff;
+#pragma unroll
+              for (int j = 0; j < 32; ++j) {
+                const float4 a = ldcg4(src + 4 * j);
+                accv[4 * j] += a.x; accv[4 * j + 1] += a.y; accv[4 * j + 2] += a.z; accv[4 * j + 3] += a.w;
+              }
+            }
+          }
+        }
         if (kKind == kGemm1) {
           // h = silu(g) * u for 64 columns, then E4M3 G(128) over the 128 columns of this row
           float amax = 0.f;
@@ -368,7 +628,8 @@ __global__ void __launch_bounds__(Cfg<kFP8>::kThreads, 1)
           // exchange with the warp holding the other 64 columns of these rows (bounded wait)
           float* xb = amax_x + xbuf * 2 * BM;
           xb[half * BM + r] = amax;
-          mbar_arrive(xbar);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(xbar);
           if (!(ok = warp_wait(xbar, xphase))) break;
           amax = fmaxf(amax, xb[(1 - half) * BM + r]);
           xphase ^= 1;
@@ -430,6 +691,67 @@ __global__ void __launch_bounds__(Cfg<kFP8>::kThreads, 1)
   }
 }
 
+// Groups of MG tiles of one expert (expert, first row) and their count, from
+// the 128-row tile map.  Called by all threads of a 1024-thread block.
+__device__ void build_groups(const int32_t* __restrict__ tile_map, int n, const int32_t* __restrict__ offsets, int MG,
+                             int32_t* __restrict__ group_map, int32_t* __restrict__ num_groups) {
+  __shared__ int warp_tot[32];
+  __shared__ int carry;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (threadIdx.x == 0) carry = 0;
+  __syncthreads();
+  for (int base = 0; base < n; base += 1024) {
+    const int mt = base + threadIdx.x;
+    int e = 0, r0 = 0, start = 0;
+    if (mt < n) {
+      e = tile_map[2 * mt];
+      r0 = tile_map[2 * mt + 1];
+      start = ((r0 - offsets[e]) / BM) % MG == 0;
+    }
+    int x = start;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, off);
+      if (lane >= off) x += y;
+    }
+    if (lane == 31) warp_tot[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+      const int w = warp_tot[lane];
+      int wx = w;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, wx, off);
+        if (lane >= off) wx += y;
+      }
+      warp_tot[lane] = wx - w;
+    }
+    __syncthreads();
+    const int idx = carry + warp_tot[warp] + x - start;
+    if (start) {
+      group_map[2 * idx] = e;
+      group_map[2 * idx + 1] = r0;
+    }
+    __syncthreads();
+    if (threadIdx.x == 1023) carry = idx + start;
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) *num_groups = carry;
+  __syncthreads();
+}
+
+// plan: the group maps of both GEMMs and cleared split-unit flags.  One block.
+__global__ void __launch_bounds__(1024)
+    plan_kernel(const int32_t* __restrict__ tile_map, const int32_t* __restrict__ num_tiles,
+                const int32_t* __restrict__ offsets, int mg1, int mg2, int32_t* __restrict__ gmap1,
+                int32_t* __restrict__ ngroups1, int32_t* __restrict__ gmap2, int32_t* __restrict__ ngroups2,
+                int* __restrict__ flags, int nflags) {
+  const int n = *num_tiles;
+  build_groups(tile_map, n, offsets, mg1, gmap1, ngroups1);
+  build_groups(tile_map, n, offsets, mg2, gmap2, ngroups2);
+  for (int i = threadIdx.x; i < nflags; i += 1024) flags[i] = 0;
+}
+
 // gather: one warp per sorted row p.  Copies the row of token sorted_slot[p]/k
 // (unless codes are not wanted) and, for fp8, writes its scales transposed.
 __global__ void __launch_bounds__(256)
@@ -478,32 +800,37 @@ bool make_map(CUtensorMap* m, const void* base, bool fp8, long long k, long long
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <bool kFP8, int kKind>
+template <bool kFP8, int kKind, int kMG>
 cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p, int grid, cudaStream_t s) {
   static int configured[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_kernel<kFP8, kKind>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         SMEM_BYTES);
+    cudaError_t e = cudaFuncSetAttribute(gemm_kernel<kFP8, kKind, kMG>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<kFP8, kMG>::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     configured[dev] = 1;
   }
-  gemm_kernel<kFP8, kKind><<<grid, Cfg<kFP8>::kThreads, SMEM_BYTES, s>>>(a, b, p);
+  gemm_kernel<kFP8, kKind, kMG><<<grid, Warps<kFP8>::THREADS, Cfg<kFP8, kMG>::SMEM_BYTES, s>>>(a, b, p);
   return cudaGetLastError();
 }
 
 struct WsLayout {
-  size_t A, As, h, hs, total;
-  int s_pad;
+  size_t A, As, h, hs, gmap, ngroups, gmap2, ngroups2, flags1, flags2, partials, total;
+  int s_pad, cap_groups, nflags1, nflags2;
 };
 
 inline size_t al256(size_t x) { return (x + 255) & ~size_t(255); }
 
-WsLayout ws_layout(long long S, int H, int I, bool fp8) {
+WsLayout ws_layout(long long S, int H, int I, int E, bool fp8, int grid) {
   WsLayout L;
   const int esz = fp8 ? 1 : 2;
-  L.s_pad = (int)(((S + BM + 3) / 4) * 4);
+  const int MG = fp8 ? 1 : 2;  // the larger bound of either GEMM
+  L.s_pad = (int)(((S + MG * BM + 3) / 4) * 4);
+  L.cap_groups = std::max(1, moe_tile_map_capacity((int)S, E, BM));  // a group holds at least one tile
+  L.nflags1 = L.cap_groups * (I / 128);
+  L.nflags2 = L.cap_groups * ((H + 255) / 256);
+  const size_t partial_floats = (size_t)MG * BM * BN;
   size_t off = 0;
   L.A = off;
   off = al256(off + (size_t)S * H * esz);
@@ -513,9 +840,26 @@ WsLayout ws_layout(long long S, int H, int I, bool fp8) {
   off = al256(off + (size_t)S * I * esz);
   L.hs = off;
   off = al256(off + (fp8 ? (size_t)(I / 128) * L.s_pad * 4 : 0));
+  L.gmap = off;
+  off = al256(off + (size_t)L.cap_groups * 2 * 4);
+  L.ngroups = off;
+  off = al256(off + 4);
+  L.gmap2 = off;
+  off = al256(off + (size_t)L.cap_groups * 2 * 4);
+  L.ngroups2 = off;
+  off = al256(off + 4);
+  L.flags1 = off;
+  L.flags2 = L.flags1 + (size_t)L.nflags1 * 4;
+  off = al256(off + (size_t)(L.nflags1 + L.nflags2) * 4);
+  L.partials = off;
+  off = al256(off + (size_t)grid * partial_floats * 4);
   L.total = off;
   return L;
 }
+
+// Grid of the persistent GEMMs: one CTA per SM (the workspace holds one
+// split-unit partial per CTA, so its size depends on this).
+int gemm_grid() { return num_sms(); }
 
 }  // namespace
 
@@ -527,7 +871,7 @@ using namespace moe;
 
 extern "C" size_t moe_workspace_size(int T, int H, int I, int E, int top_k, const moe_quant_config* qc) {
   if (!qc || T < 0 || H <= 0 || I <= 0 || E < 1 || top_k < 1) return 0;
-  return ws_layout((long long)T * top_k, H, I, qc->act == MOE_DT_FP8_E4M3).total;
+  return ws_layout((long long)T * top_k, H, I, E, qc->act == MOE_DT_FP8_E4M3, gemm_grid()).total;
 }
 
 extern "C" moe_status_t moe_experts(const void* a1q, const float* a1q_scale, const void* w13, const float* w13_scale,
@@ -545,16 +889,16 @@ extern "C" moe_status_t moe_experts(const void* a1q, const float* a1q_scale, con
   }
   MOE_CHECK_ARG(H % 128 == 0 && I % 128 == 0);
   const long long S = (long long)T * top_k;
-  MOE_CHECK_ARG(fits_int32(S + 2 * BM) && fits_int32((long long)E * 2 * I) && fits_int32((long long)E * H));
+  MOE_CHECK_ARG(fits_int32(S + 4 * BM) && fits_int32((long long)E * 2 * I) && fits_int32((long long)E * H));
   if (S == 0) return MOE_OK;
   MOE_CHECK_ARG(a1q && w13 && w2 && expert_offsets && tile_map && num_tiles && fused_expert_output);
   MOE_CHECK_ARG(sorted_slot || (E == 1 && top_k == 1));
   MOE_CHECK_ARG(!fp8 || (a1q_scale && w13_scale && w2_scale));
   MOE_CHECK_ARG(aligned16(a1q) && aligned16(w13) && aligned16(w2) && aligned16(fused_expert_output));
-  const WsLayout L = ws_layout(S, H, I, fp8);
+  const int grid = gemm_grid();
+  const WsLayout L = ws_layout(S, H, I, E, fp8, grid);
   if (!ws || ws_bytes < L.total) return MOE_ERR_WORKSPACE;
   MOE_CHECK_ARG(aligned16(ws));
-  const int cap = moe_tile_map_capacity((int)S, E, BM);
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   uint8_t* wsb = static_cast<uint8_t*>(ws);
@@ -564,11 +908,44 @@ extern "C" moe_status_t moe_experts(const void* a1q, const float* a1q_scale, con
   float* As = fp8 ? reinterpret_cast<float*>(wsb + L.As) : nullptr;
   void* h = wsb + L.h;
   float* hs = fp8 ? reinterpret_cast<float*>(wsb + L.hs) : nullptr;
+  int32_t* gmap = reinterpret_cast<int32_t*>(wsb + L.gmap);
+  int32_t* ngroups = reinterpret_cast<int32_t*>(wsb + L.ngroups);
+  int* flags1 = reinterpret_cast<int*>(wsb + L.flags1);
+  int* flags2 = reinterpret_cast<int*>(wsb + L.flags2);
+  float* partials = reinterpret_cast<float*>(wsb + L.partials);
 
+  // Tiles per unit (host estimate of the unit count from the tile-map bound):
+  // one tile per unit, dealt round-robin so tiles sharing a weight tile run side
+  // by side -- unless two-tile units of full tiles fill between half a wave and
+  // one wave (a deep-K GEMM2): then each weight tile is read once, all units in
+  // one wave.  fp8 always uses one tile (its register promotion holds one).
+  // Decode-sized problems (at most 16 slots per expert, K of 32+ blocks) may
+  // split units across CTAs when there are too few of them for the SMs.
+  const int cap_tiles = std::max(1, moe_tile_map_capacity((int)S, E, BM));
+  const int grid_sms = grid;
+  const bool full_tiles = S >= (long long)BM * E;  // experts average a full 128-row tile or more
+  auto mg_for = [&](int nt) {
+    const long long units2 = (long long)((cap_tiles + 1) / 2) * nt;  // estimate with two tiles per unit
+    return (!fp8 && full_tiles && 2 * units2 >= grid_sms && units2 <= grid_sms) ? 2 : 1;
+  };
+  const int mg1 = mg_for(I / 128), mg2 = mg_for((H + 255) / 256);
+  int32_t* gmap2 = reinterpret_cast<int32_t*>(wsb + L.gmap2);
+  int32_t* ngroups2 = reinterpret_cast<int32_t*>(wsb + L.ngroups2);
+  const bool allow_split = !fp8 && S <= 16LL * E;  // decode-sized: units may be split across CTAs
+  const bool split1 = allow_split && H / (fp8 ? 128 : 64) >= 32, split2 = allow_split && I / (fp8 ? 128 : 64) >= 32;
+  if (mg1 == 2 || mg2 == 2 || split1 || split2) {
+    plan_kernel<<<1, 1024, 0, s>>>(tile_map, num_tiles, expert_offsets, mg1, mg2, gmap, ngroups, gmap2, ngroups2,
+                                   flags1, L.nflags1 + L.nflags2);
+    if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+  } else {
+    // one tile per unit and no split: the tile map is the group map
+    gmap = gmap2 = const_cast<int32_t*>(tile_map);
+    ngroups = ngroups2 = const_cast<int32_t*>(num_tiles);
+  }
   if (gather_rows || fp8) {
-    const unsigned grid = (unsigned)((S + 7) / 8);
-    gather_kernel<<<grid, 256, 0, s>>>(static_cast<const uint8_t*>(a1q), a1q_scale, sorted_slot, (int)S, top_k,
-                                       H * esz, H / 128, gather_rows ? wsb + L.A : nullptr, As, L.s_pad);
+    const unsigned g = (unsigned)((S + 7) / 8);
+    gather_kernel<<<g, 256, 0, s>>>(static_cast<const uint8_t*>(a1q), a1q_scale, sorted_slot, (int)S, top_k, H * esz,
+                                    H / 128, gather_rows ? wsb + L.A : nullptr, As, L.s_pad);
     if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
   }
 
@@ -577,11 +954,10 @@ extern "C" moe_status_t moe_experts(const void* a1q, const float* a1q_scale, con
       !make_map(&mA2, h, fp8, I, S) || !make_map(&mB2, w2, fp8, I, (long long)E * H))
     return MOE_ERR_CUDA;
 
-  const int nsm = num_sms();
   GemmParams p1 = {};
   p1.offsets = expert_offsets;
-  p1.tile_map = tile_map;
-  p1.num_tiles = num_tiles;
+  p1.group_map = gmap;
+  p1.num_groups = ngroups;
   p1.sorted_slot = sorted_slot;
   p1.K = H;
   p1.NT = I / 128;
@@ -593,9 +969,13 @@ extern "C" moe_status_t moe_experts(const void* a1q, const float* a1q_scale, con
   p1.w_scale = w13_scale;
   p1.out = h;
   p1.out_scale_t = hs;
-  const int grid1 = (int)std::min<long long>(nsm, (long long)cap * p1.NT);
+  p1.flags = flags1;
+  p1.partials = partials;
+  p1.allow_split = split1;
 
   GemmParams p2 = p1;
+  p2.group_map = gmap2;
+  p2.num_groups = ngroups2;
   p2.K = I;
   p2.NT = (H + 255) / 256;
   p2.b_rows = H;
@@ -603,15 +983,19 @@ extern "C" moe_status_t moe_experts(const void* a1q, const float* a1q_scale, con
   p2.w_scale = w2_scale;
   p2.out = fused_expert_output;
   p2.out_scale_t = nullptr;
-  const int grid2 = (int)std::min<long long>(nsm, (long long)cap * p2.NT);
+  p2.flags = flags2;
+  p2.allow_split = split2;  // (K of at least 32 blocks for a split to pay)
 
   cudaError_t e;
   if (fp8) {
-    e = launch_gemm<true, kGemm1>(mA1, mB1, p1, grid1, s);
-    if (e == cudaSuccess) e = launch_gemm<true, kGemm2>(mA2, mB2, p2, grid2, s);
+    e = launch_gemm<true, kGemm1, 1>(mA1, mB1, p1, grid, s);
+    if (e == cudaSuccess) e = launch_gemm<true, kGemm2, 1>(mA2, mB2, p2, grid, s);
   } else {
-    e = launch_gemm<false, kGemm1>(mA1, mB1, p1, grid1, s);
-    if (e == cudaSuccess) e = launch_gemm<false, kGemm2>(mA2, mB2, p2, grid2, s);
+    e = mg1 == 1 ? launch_gemm<false, kGemm1, 1>(mA1, mB1, p1, grid, s)
+                 : launch_gemm<false, kGemm1, 2>(mA1, mB1, p1, grid, s);
+    if (e == cudaSuccess)
+      e = mg2 == 1 ? launch_gemm<false, kGemm2, 1>(mA2, mB2, p2, grid, s)
+                   : launch_gemm<false, kGemm2, 2>(mA2, mB2, p2, grid, s);
   }
   return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

@@ -59,6 +59,10 @@ def _cfgs():
                                description="Mixtral-8x7B-like layer T512 H4096 I14336 E8 top2 bf16")
     c["deepseek"] = LayerConfig("deepseek", 4096, 7168, 2048, 256, 8, quant="fp8", shared_I=2048,
                                 description="DeepSeek-V3-like layer T4096 H7168 I2048 E256 top8 fp8 + bf16 shared I2048")
+    # same per-expert shape as the DeepSeek-V3-like layer (~128 rows per expert), a quarter of the
+    # experts: a small case for detailed profiles of the fp8 kernels
+    c["deepseek_e64"] = LayerConfig("deepseek_e64", 1024, 7168, 2048, 64, 8, quant="fp8", shared_I=2048,
+                                    description="DeepSeek-V3-shaped experts T1024 H7168 I2048 E64 top8 fp8 + bf16 shared")
     for T in (128, 512):
         c[f"finalize{T}"] = LayerConfig(f"finalize{T}", T, 7168, 0, 256, 4, finalize_only=True,
                                         residual=True, rms=True, nvfp4=True, shared_I=1,

@@ -1,7 +1,10 @@
 """GPU grouped expert GEMMs vs the oracle, fed identical prepared inputs.
 
 Sizes span several M, N and K tiles with ragged tails: experts of 0, 1, <128,
->128 and many-tile row counts, N tiles that run past H, deep K loops."""
+>128 and many-tile row counts, N tiles that run past H, deep K loops.  Small
+cases have few units, so their K loops are split across many CTAs and finished
+through the fp32 partials (stream-K); the 64-expert cases have at least four
+units per CTA and run the round-robin schedule."""
 import numpy as np
 import pytest
 import torch
@@ -49,6 +52,7 @@ def _ids(T, k, E, seed, skew=False):
     (700, 384, 256, 6, 2, True),      # skewed: a 5-tile expert, an empty one; GEMM2 N tile past H
     (130, 2048, 256, 3, 1, False),    # deep K (32 stages)
     (1, 256, 128, 8, 2, False),       # single token
+    (256, 256, 2048, 64, 4, False),   # 1024 units >= 4 per CTA: round-robin schedule
 ])
 def test_experts_bf16(cuda_dev, T, H, I, E, k, skew):
     inp = make_inputs(scaled(CONFIGS["tiny"], T=T, H=H, I=I, E=E, top_k=k))
@@ -61,6 +65,7 @@ def test_experts_bf16(cuda_dev, T, H, I, E, k, skew):
     (300, 512, 384, 4, 2, False),
     (500, 384, 256, 6, 2, True),
     (100, 1024, 512, 16, 4, False),
+    (256, 256, 2048, 64, 4, False),   # round-robin schedule
 ])
 def test_experts_fp8(cuda_dev, T, H, I, E, k, skew):
     inp = make_inputs(scaled(CONFIGS["deepseek"], T=T, H=H, I=I, E=E, top_k=k, shared_I=0))
