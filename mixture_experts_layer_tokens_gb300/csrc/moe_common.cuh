@@ -127,6 +127,16 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, bool b
   }
 }
 
+// ---- cp.async (4-byte global -> shared copies; completion tracked by an mbarrier)
+__device__ __forceinline__ void cp_async_4(void* smem_dst, const void* gmem_src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(smem_dst)), "l"(gmem_src) : "memory");
+}
+// Arrive on `bar` once every cp.async this thread issued so far has landed (the
+// barrier's expected count includes this arrival).
+__device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
 // ---- TMA (bulk tensor copies, global -> shared, completion on an mbarrier)
 __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* map, int x, int y, uint64_t* bar,
                                             uint64_t policy) {

@@ -90,7 +90,12 @@ struct Cfg {
   static constexpr int kMmaK = kFP8 ? 32 : 16;  // K per tcgen05.mma
   static constexpr uint32_t kIdesc = make_idesc(kFP8 ? 0u : 1u, BM, BN);
   static constexpr int PARTIAL_FLOATS = MG * BM * BN;  // one split-unit partial
-  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 4096 /*barriers, exchange*/ + 1024 /*align*/;
+  // fp8: ring of per-K-block scales (128 activation-row scales + 2 weight-block scales)
+  static constexpr int SCALE_SLOTS = 8;
+  static constexpr int SCALE_SLOT_FLOATS = 132;
+  static constexpr int SCALE_RING_BYTES = kFP8 ? SCALE_SLOTS * SCALE_SLOT_FLOATS * 4 : 0;
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 4096 /*barriers, exchange*/ + SCALE_RING_BYTES +
+                                    1024 /*align*/;
 };
 
 struct GemmParams {
@@ -260,7 +265,10 @@ __global__ void __launch_bounds__(Warps<kFP8>::THREADS, 1)
   uint64_t* xbar = tempty + 2;       // fp8 gemm1: row amax exchange between column halves
   uint64_t* drain = xbar + 1;        // teardown after a failed wait
   uint64_t* fixbar = drain + 1;      // stream-K: the later segments' partials of this CTA's split unit are in
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(fixbar + 1);
+  uint64_t* sfull = fixbar + 1;      // fp8 scale ring: [SCALE_SLOTS] slot filled
+  uint64_t* sempty = sfull + C::SCALE_SLOTS;  // [SCALE_SLOTS] slot read by every epilogue warp
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sempty + C::SCALE_SLOTS);
+  float* scale_ring = reinterpret_cast<float*>(ctrl + 4096);  // fp8: [SCALE_SLOTS][SCALE_SLOT_FLOATS]
   float* amax_x = reinterpret_cast<float*>(ctrl + 256);  // [2 items][2 halves][BM]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -276,6 +284,10 @@ __global__ void __launch_bounds__(Warps<kFP8>::THREADS, 1)
     mbar_init(xbar, EPI_WARPS);
     mbar_init(drain, 1);
     mbar_init(fixbar, 1);
+    for (int i = 0; i < C::SCALE_SLOTS; ++i) {
+      mbar_init(&sfull[i], 32);  // one cp.async arrival per producer lane
+      mbar_init(&sempty[i], EPI_WARPS);
+    }
     fence_mbar_init();
     prefetch_tensormap(&tmA);
     prefetch_tensormap(&tmB);
@@ -340,6 +352,25 @@ __global__ void __launch_bounds__(Warps<kFP8>::THREADS, 1)
       }
       for (int kb = kb0; kb < kb1; ++kb) {
         if (!(ok = warp_wait(&empty[stage], phase ^ 1))) break;
+        if (kFP8) {
+          // this K block's scales into the ring, copied asynchronously by all lanes:
+          // the activation scales of the tile's 128 rows and the two weight-block scales
+          const int slot = (int)(fills % C::SCALE_SLOTS);
+          if (!(ok = warp_wait(&sempty[slot], (uint32_t)(((fills / C::SCALE_SLOTS) & 1) ^ 1)))) break;
+          float* dst = scale_ring + slot * C::SCALE_SLOT_FLOATS;
+          const float* asrc = p.a_scale_t + (size_t)kb * p.s_pad + it.row0;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) cp_async_4(dst + lane * 4 + j, asrc + lane * 4 + j);
+          if (lane == 0) {
+            const int KBs = p.K / 128, nbw = p.b_rows / 128;
+            const float* sw = p.w_scale + (size_t)it.e * nbw * KBs;
+            const int wb0 = kKind == kGemm1 ? it.n : min(2 * it.n, nbw - 1);
+            const int wb1 = kKind == kGemm1 ? p.I / 128 + it.n : min(2 * it.n + 1, nbw - 1);
+            cp_async_4(dst + 128, sw + (size_t)wb0 * KBs + kb);
+            cp_async_4(dst + 129, sw + (size_t)wb1 * KBs + kb);
+          }
+          cp_async_arrive(&sfull[slot]);
+        }
         if (lane == 0) {
           uint8_t* sA = smem + stage * C::STAGE_BYTES;
           uint8_t* sB = sA + MG * A_BYTES;
@@ -434,6 +465,7 @@ __global__ void __launch_bounds__(Warps<kFP8>::THREADS, 1)
     uint32_t acc_phase = 0;
     int xbuf = 0;
     uint32_t xphase = 0;
+    long long sfill = 0;  // fp8: K blocks consumed from the scale ring
     bool ok = true;
     while (ok && sched.next(u, kb0, kb1)) {
       const Unit it = decode<MG>(p, u);
@@ -556,23 +588,20 @@ __global__ void __launch_bounds__(Warps<kFP8>::THREADS, 1)
         float accv[128];
 #pragma unroll
         for (int i = 0; i < 128; ++i) accv[i] = 0.f;
-        const int KBs = p.K / 128;
-        const int nbw = p.b_rows / 128;
-        const float* sw = p.w_scale + (size_t)it.e * nbw * KBs;
-        int wb0, wb1;  // weight-scale block rows of accv[0..63] / accv[64..127]
-        if (kKind == kGemm1) {
-          wb0 = it.n;
-          wb1 = p.I / 128 + it.n;
-        } else {
-          wb0 = wb1 = min(2 * it.n + half, nbw - 1);
-        }
-        const float* sa = p.a_scale_t + it.row0 + r;  // + kb * s_pad
         for (int kb = kb0; kb < kb1; ++kb) {
+          // scales of this K block from the ring the producer fills ahead of time
+          const int slot = (int)(sfill % C::SCALE_SLOTS);
+          if (!(ok = warp_wait(&sfull[slot], (uint32_t)((sfill / C::SCALE_SLOTS) & 1)))) break;
+          const float* ring = scale_ring + slot * C::SCALE_SLOT_FLOATS;
+          const float a_s = ring[r];
+          // gemm1: accv[0..63] gate block, accv[64..127] up block; gemm2: this half's block
+          const float s0 = a_s * ring[kKind == kGemm1 ? 128 : 128 + half];
+          const float s1 = a_s * ring[kKind == kGemm1 ? 129 : 128 + half];
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sempty[slot]);
+          ++sfill;
           if (!(ok = warp_wait(&tfull[acc], acc_phase))) break;
           tc_fence_after();
-          const float a_s = __ldg(sa + (size_t)kb * p.s_pad);
-          const float s0 = a_s * __ldg(sw + (size_t)wb0 * KBs + kb);
-          const float s1 = a_s * __ldg(sw + (size_t)wb1 * KBs + kb);
           const uint32_t tb = tmem + lane_addr + acc * BN;
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
