@@ -246,6 +246,15 @@ __device__ __forceinline__ void signal_split_partial(int* flag) {
 
 __device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + __expf(-g)) * u; }
 
+// (a0, a1) += (v0, v1) * s with one packed two-wide fp32 FMA (each lane an IEEE fma)
+__device__ __forceinline__ void fma2(float& a0, float& a1, float v0, float v1, float s) {
+  asm("{\n\t.reg .b64 a, v, s;\n\t"
+      "mov.b64 a, {%0, %1};\n\tmov.b64 v, {%2, %3};\n\tmov.b64 s, {%4, %4};\n\t"
+      "fma.rn.f32x2 a, v, s, a;\n\tmov.b64 {%0, %1}, a;\n\t}"
+      : "+f"(a0), "+f"(a1)
+      : "f"(v0), "f"(v1), "f"(s));
+}
+
 template <bool kFP8, int kKind, int kMG>
 __global__ void __launch_bounds__(Warps<kFP8>::THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -613,7 +622,7 @@ __global__ void __launch_bounds__(Warps<kFP8>::THREADS, 1)
             tmem_ld_wait();
             const float sc = (kKind == kGemm1 && c >= 2) ? s1 : s0;
 #pragma unroll
-            for (int i = 0; i < 32; ++i) accv[32 * c + i] = fmaf(v[i], sc, accv[32 * c + i]);
+            for (int i = 0; i < 32; i += 2) fma2(accv[32 * c + i], accv[32 * c + i + 1], v[i], v[i + 1], sc);
           }
           tc_fence_before();
           __syncwarp();

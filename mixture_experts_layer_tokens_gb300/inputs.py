@@ -59,6 +59,12 @@ def _cfgs():
                                description="Mixtral-8x7B-like layer T512 H4096 I14336 E8 top2 bf16")
     c["deepseek"] = LayerConfig("deepseek", 4096, 7168, 2048, 256, 8, quant="fp8", shared_I=2048,
                                 description="DeepSeek-V3-like layer T4096 H7168 I2048 E256 top8 fp8 + bf16 shared I2048")
+    # prefill sweeps where the expert GEMMs are tensor-bound (hundreds to thousands of rows per expert)
+    for T in (4096, 8192):
+        c[f"mixtral_T{T}"] = LayerConfig(f"mixtral_T{T}", T, 4096, 14336, 8, 2,
+                                         description=f"Mixtral-8x7B-like layer T{T} H4096 I14336 E8 top2 bf16 (prefill)")
+    c["deepseek_T16384"] = LayerConfig("deepseek_T16384", 16384, 7168, 2048, 256, 8, quant="fp8", shared_I=2048,
+                                       description="DeepSeek-V3-like layer T16384 H7168 I2048 E256 top8 fp8 + bf16 shared (prefill)")
     # same per-expert shape as the DeepSeek-V3-like layer (~128 rows per expert), a quarter of the
     # experts: a small case for detailed profiles of the fp8 kernels
     c["deepseek_e64"] = LayerConfig("deepseek_e64", 1024, 7168, 2048, 64, 8, quant="fp8", shared_I=2048,
