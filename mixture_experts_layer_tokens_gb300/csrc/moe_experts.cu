@@ -263,6 +263,10 @@ __global__ void __launch_bounds__(Warps<kFP8>::THREADS, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sempty + C::SCALE_SLOTS);
   float* scale_ring = reinterpret_cast<float*>(ctrl + 4096);  // fp8: [SCALE_SLOTS][SCALE_SLOT_FLOATS]
   float* amax_x = reinterpret_cast<float*>(ctrl + 256);  // [2 items][2 halves][BM]
+  // bf16 split units: the later segments' summed partials, [BM][FIX_STRIDE] over the stage buffers
+  constexpr int FIX_STRIDE = 257;  // odd stride: row-per-thread reads hit distinct banks
+  static_assert(BM * FIX_STRIDE * 4 <= STAGES * C::STAGE_BYTES, "fix-up sums must fit the stages");
+  float* fix = reinterpret_cast<float*>(smem);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -300,7 +304,8 @@ __global__ void __launch_bounds__(Warps<kFP8>::THREADS, 1)
   Sched sched;
   // fp8 units are never split: its register promotion leaves no room for the split logic
   constexpr bool kSplit = !kFP8;
-  sched.init(units, KB, gridDim.x, blockIdx.x, kSplit && p.allow_split);
+  // (split units have one M tile: the fix-up below sums one tile's rows)
+  sched.init(units, KB, gridDim.x, blockIdx.x, kSplit && MG == 1 && p.allow_split);
   int u, kb0, kb1;
 
   if (warp == 0) {
@@ -313,23 +318,25 @@ __global__ void __launch_bounds__(Warps<kFP8>::THREADS, 1)
     Sched pfs = sched;
     int pf_kb = 0, pf_kb1 = 0;
     Unit pit{};
-    auto prefetch_next = [&]() {
+    auto prefetch_next = [&](bool issue) {
       if (pf_kb >= pf_kb1) {
         int pu;
         if (!pfs.next(pu, pf_kb, pf_kb1)) return;
         pit = decode<MG>(p, pu);
       }
-      if (kKind == kGemm1)
-        tma_prefetch_3d(&tmB, pf_kb * C::kBK, pit.n * 128, 2 * pit.e);
-      else
-        tma_prefetch_2d(&tmB, pf_kb * C::kBK, pit.e * p.b_rows + pit.n * 256);
+      if (issue) {
+        if (kKind == kGemm1)
+          tma_prefetch_3d(&tmB, pf_kb * C::kBK, pit.n * 128, 2 * pit.e);
+        else
+          tma_prefetch_2d(&tmB, pf_kb * C::kBK, pit.e * p.b_rows + pit.n * 256);
+      }
       ++pf_kb;
     };
     // (round-robin schedules already keep every SM streaming whole units; there the
-    // extra requests only cost, so the cursor runs in stream-K mode alone)
+    // extra requests only cost, so the cursor runs in stream-K mode alone).  The cursor
+    // starts after the iterations the first STAGES fills load, and its first batch is
+    // issued after those loads, so that they are not queued behind it.
     const bool l2_prefetch = !sched.rr;
-    if (lane == 0 && l2_prefetch)
-      for (int i = 0; i < L2_PREFETCH_AHEAD; ++i) prefetch_next();
     int stage = 0;
     uint32_t phase = 0;
     long long fills = 0;
@@ -374,7 +381,14 @@ __global__ void __launch_bounds__(Warps<kFP8>::THREADS, 1)
             tma_load_3d(sB, &tmB, kx, brow, 2 * it.e, &full[stage], pol_b);
           else
             tma_load_2d(sB, &tmB, kx, brow, &full[stage], pol_b);
-          if (l2_prefetch) prefetch_next();
+          if (l2_prefetch) {
+            if (fills + 1 == STAGES) {
+              for (int i = 0; i < STAGES; ++i) prefetch_next(false);
+              for (int i = 0; i < L2_PREFETCH_AHEAD; ++i) prefetch_next(true);
+            } else if (fills + 1 > STAGES) {
+              prefetch_next(true);
+            }
+          }
         }
         __syncwarp();
         ++fills;
@@ -482,7 +496,37 @@ __global__ void __launch_bounds__(Warps<kFP8>::THREADS, 1)
         // 32 columns (gemm1: chunks 0-3 gate, 4-7 up)
         if (!(ok = warp_wait(&tfull[acc], acc_phase))) break;
         tc_fence_after();
-        if (role == 1) ok = wait_split_partials(p.flags + u, (c_last - c_first + 1) * EPI_THREADS, fixbar);
+        if (role == 1) {
+          ok = wait_split_partials(p.flags + u, (c_last - c_first + 1) * EPI_THREADS, fixbar);
+          // Sum the later segments' partials in segment order, column-parallel over all
+          // epilogue threads (every load independent), into shared memory: the stage
+          // buffers are free, as this segment is the CTA's last work and its MMAs are
+          // complete.  Split units have one M tile.  The epilogue below adds the sums
+          // to its own accumulator rows.
+          const int n = min(BM, it.row_end - it.row0) * 256;
+          const int tid = threadIdx.x - 64;
+          if (ok) {
+            for (int i0 = tid; i0 < n; i0 += 4 * EPI_THREADS) {
+              float a[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+              for (int cc = c_first; cc <= c_last; ++cc) {
+                const float* src = p.partials + (size_t)cc * C::PARTIAL_FLOATS;
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                  if (i0 + k * EPI_THREADS < n) a[k] += __ldcg(src + i0 + k * EPI_THREADS);
+              }
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                const int i = i0 + k * EPI_THREADS;
+                if (i < n) fix[(i >> 8) * FIX_STRIDE + (i & 255)] = a[k];
+              }
+            }
+          }
+          // every epilogue warp arrives, whatever its status, so that none waits in vain
+          __syncwarp();
+          if (lane == 0) mbar_arrive(xbar);
+          ok = warp_wait(xbar, 0) && ok;
+        }
         const int mcnt = (it.row_end - it.row0 + BM - 1) / BM;
         for (int m = 0; m < mcnt; ++m) {
           const int mrow = prow + m * BM;
@@ -511,14 +555,11 @@ __global__ void __launch_bounds__(Warps<kFP8>::THREADS, 1)
               tmem_ld32(tb + 128 + c * 32, uu);
               tmem_ld_wait();
               if (role == 1 && mvalid && ok) {
-                for (int cc = c_first; cc <= c_last; ++cc) {
-                  const float* src = p.partials + (size_t)cc * C::PARTIAL_FLOATS + mpoff;
+                const float* src = fix + r * FIX_STRIDE + c * 32;
 #pragma unroll
-                  for (int j = 0; j < 8; ++j) {
-                    const float4 a = ldcg4(src + c * 32 + 4 * j), b = ldcg4(src + 128 + c * 32 + 4 * j);
-                    g[4 * j] += a.x; g[4 * j + 1] += a.y; g[4 * j + 2] += a.z; g[4 * j + 3] += a.w;
-                    uu[4 * j] += b.x; uu[4 * j + 1] += b.y; uu[4 * j + 2] += b.z; uu[4 * j + 3] += b.w;
-                  }
+                for (int j = 0; j < 32; ++j) {
+                  g[j] += src[j];
+                  uu[j] += src[128 + j];
                 }
               }
               if (mvalid) {
@@ -544,14 +585,9 @@ __global__ void __launch_bounds__(Warps<kFP8>::THREADS, 1)
               tmem_ld32(tb + c * 32, v);
               tmem_ld_wait();
               if (role == 1 && mvalid && ok) {
-                for (int cc = c_first; cc <= c_last; ++cc) {
-                  const float* src = p.partials + (size_t)cc * C::PARTIAL_FLOATS + mpoff + c * 32;
+                const float* src = fix + r * FIX_STRIDE + c * 32;
 #pragma unroll
-                  for (int j = 0; j < 8; ++j) {
-                    const float4 a = ldcg4(src + 4 * j);
-                    v[4 * j] += a.x; v[4 * j + 1] += a.y; v[4 * j + 2] += a.z; v[4 * j + 3] += a.w;
-                  }
-                }
+                for (int j = 0; j < 32; ++j) v[j] += src[j];
               }
               if (mvalid && c * 32 < ncols) {
                 uint4* dst = reinterpret_cast<uint4*>(yrow + c * 32);

@@ -1,10 +1,12 @@
 """GPU grouped expert GEMMs vs the oracle, fed identical prepared inputs.
 
 Sizes span several M, N and K tiles with ragged tails: experts of 0, 1, <128,
->128 and many-tile row counts, N tiles that run past H, deep K loops.  Small
-cases have few units, so their K loops are split across many CTAs and finished
-through the fp32 partials (stream-K); the 64-expert cases have at least four
-units per CTA and run the round-robin schedule."""
+>128 and many-tile row counts, N tiles that run past H, deep K loops.  The
+decode-sized bf16 cases (at most 16 slots per expert, K of 32+ blocks, fewer
+units than half the SMs) split their K loops across many CTAs and finish each
+unit through the fp32 partials (stream-K): one or many valid rows per tile,
+units cut into 2 to 20 segments.  The 64-expert cases have at least four units
+per CTA and run the round-robin schedule."""
 import numpy as np
 import pytest
 import torch
@@ -53,6 +55,10 @@ def _ids(T, k, E, seed, skew=False):
     (130, 2048, 256, 3, 1, False),    # deep K (32 stages)
     (1, 256, 128, 8, 2, False),       # single token
     (256, 256, 2048, 64, 4, False),   # 1024 units >= 4 per CTA: round-robin schedule
+    (4, 2048, 2048, 16, 1, False),    # stream-K in both GEMMs, single-row tiles
+    (1, 4096, 1024, 8, 1, False),     # stream-K GEMM1: 8 units cut into ~19 segments each
+    (16, 2048, 4096, 1, 1, False),    # stream-K, 16 valid rows in one tile (the shared-expert shape)
+    (12, 2048, 2048, 8, 2, True),     # stream-K with skewed routing: one expert holds most rows
 ])
 def test_experts_bf16(cuda_dev, T, H, I, E, k, skew):
     inp = make_inputs(scaled(CONFIGS["tiny"], T=T, H=H, I=I, E=E, top_k=k))
