@@ -263,8 +263,9 @@ __global__ void __launch_bounds__(Warps<kFP8>::THREADS, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sempty + C::SCALE_SLOTS);
   float* scale_ring = reinterpret_cast<float*>(ctrl + 4096);  // fp8: [SCALE_SLOTS][SCALE_SLOT_FLOATS]
   float* amax_x = reinterpret_cast<float*>(ctrl + 256);  // [2 items][2 halves][BM]
-  // bf16 split units: the later segments' summed partials, [BM][FIX_STRIDE] over the stage buffers
-  constexpr int FIX_STRIDE = 257;  // odd stride: row-per-thread reads hit distinct banks
+  // bf16 split units: the finished rows (own accumulator + later segments' partials),
+  // [BM][FIX_STRIDE] fp32 over the stage buffers
+  constexpr int FIX_STRIDE = 257;  // odd stride: row-per-thread writes hit distinct banks
   static_assert(BM * FIX_STRIDE * 4 <= STAGES * C::STAGE_BYTES, "fix-up sums must fit the stages");
   float* fix = reinterpret_cast<float*>(smem);
 
@@ -497,17 +498,40 @@ __global__ void __launch_bounds__(Warps<kFP8>::THREADS, 1)
         if (!(ok = warp_wait(&tfull[acc], acc_phase))) break;
         tc_fence_after();
         if (role == 1) {
+          // The first segment of a split unit finishes it, column-parallel over all
+          // epilogue threads (decode-sized units have few valid rows, which a
+          // row-per-thread epilogue would leave to one thread): its own accumulator rows
+          // go to shared memory (the stage buffers are free: this segment is the CTA's
+          // last work and its MMAs are complete), the later segments' partials are added
+          // in segment order, every load independent, then the outputs are written.
+          // Split units have one M tile.  Every epilogue warp arrives at both barrier
+          // phases, whatever its status, so that none waits in vain.
           ok = wait_split_partials(p.flags + u, (c_last - c_first + 1) * EPI_THREADS, fixbar);
-          // Sum the later segments' partials in segment order, column-parallel over all
-          // epilogue threads (every load independent), into shared memory: the stage
-          // buffers are free, as this segment is the CTA's last work and its MMAs are
-          // complete.  Split units have one M tile.  The epilogue below adds the sums
-          // to its own accumulator rows.
-          const int n = min(BM, it.row_end - it.row0) * 256;
+          const int nrows = min(BM, it.row_end - it.row0);
           const int tid = threadIdx.x - 64;
+          const uint32_t tb = tmem + lane_addr + acc * BN;
+#pragma unroll 1
+          for (int c = 0; c < 8; ++c) {
+            float v[32];
+            tmem_ld32(tb + c * 32, v);
+            tmem_ld_wait();
+            if (r < nrows) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) fix[r * FIX_STRIDE + c * 32 + j] = v[j];
+            }
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(xbar);
+          ok = warp_wait(xbar, 0) && ok;
+          const int n = nrows * 256;
           if (ok) {
             for (int i0 = tid; i0 < n; i0 += 4 * EPI_THREADS) {
-              float a[4] = {0.f, 0.f, 0.f, 0.f};
+              float a[4];
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                const int i = i0 + k * EPI_THREADS;
+                a[k] = i < n ? fix[(i >> 8) * FIX_STRIDE + (i & 255)] : 0.f;
+              }
 #pragma unroll 4
               for (int cc = c_first; cc <= c_last; ++cc) {
                 const float* src = p.partials + (size_t)cc * C::PARTIAL_FLOATS;
@@ -522,10 +546,39 @@ __global__ void __launch_bounds__(Warps<kFP8>::THREADS, 1)
               }
             }
           }
-          // every epilogue warp arrives, whatever its status, so that none waits in vain
           __syncwarp();
           if (lane == 0) mbar_arrive(xbar);
-          ok = warp_wait(xbar, 0) && ok;
+          ok = warp_wait(xbar, 1) && ok;
+          if (ok) {
+            if (kKind == kGemm1) {
+              // h[row][128 n + col] = silu(gate) * up, two columns per thread and step
+              __nv_bfloat16* h = static_cast<__nv_bfloat16*>(p.out) + it.n * 128;
+              for (int i = tid; i < nrows * 64; i += EPI_THREADS) {
+                const int row = i >> 6, col = 2 * (i & 63);
+                const float* f = fix + row * FIX_STRIDE + col;
+                const uint32_t o = pack_bf16x2(silu_mul(f[0], f[128]), silu_mul(f[1], f[129]));
+                *reinterpret_cast<uint32_t*>(h + (size_t)(it.row0 + row) * p.I + col) = o;
+              }
+            } else {
+              // y[sorted_slot[row]][256 n + col], two columns per thread and step
+              const int ncols = min(256, p.H - it.n * 256);
+              for (int i = tid; i < nrows * 128; i += EPI_THREADS) {
+                const int row = i >> 7, col = 2 * (i & 127);
+                if (col >= ncols) continue;
+                const int mrow = it.row0 + row;
+                const int f = p.sorted_slot ? __ldg(p.sorted_slot + mrow) : mrow;
+                const float* x = fix + row * FIX_STRIDE + col;
+                *reinterpret_cast<uint32_t*>(static_cast<__nv_bfloat16*>(p.out) + (size_t)f * p.H + it.n * 256 + col) =
+                    pack_bf16x2(x[0], x[1]);
+              }
+            }
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&tempty[acc]);
+          if (MG == 1) acc ^= 1;
+          if (acc == 0) acc_phase ^= 1;
+          continue;
         }
         const int mcnt = (it.row_end - it.row0 + BM - 1) / BM;
         for (int m = 0; m < mcnt; ++m) {
@@ -554,14 +607,6 @@ __global__ void __launch_bounds__(Warps<kFP8>::THREADS, 1)
               tmem_ld32(tb + c * 32, g);
               tmem_ld32(tb + 128 + c * 32, uu);
               tmem_ld_wait();
-              if (role == 1 && mvalid && ok) {
-                const float* src = fix + r * FIX_STRIDE + c * 32;
-#pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                  g[j] += src[j];
-                  uu[j] += src[128 + j];
-                }
-              }
               if (mvalid) {
                 uint4* dst = reinterpret_cast<uint4*>(hrow + c * 32);
 #pragma unroll
@@ -584,11 +629,6 @@ __global__ void __launch_bounds__(Warps<kFP8>::THREADS, 1)
               float v[32];
               tmem_ld32(tb + c * 32, v);
               tmem_ld_wait();
-              if (role == 1 && mvalid && ok) {
-                const float* src = fix + r * FIX_STRIDE + c * 32;
-#pragma unroll
-                for (int j = 0; j < 32; ++j) v[j] += src[j];
-              }
               if (mvalid && c * 32 < ncols) {
                 uint4* dst = reinterpret_cast<uint4*>(yrow + c * 32);
 #pragma unroll
