@@ -5,7 +5,9 @@
 // deterministic.  expert_offsets is the unpadded exclusive prefix sum of the
 // per-expert counts; the tile map lists the block_m-row tiles of each expert.
 //
-// Three launches over chunks of kChunk slots:
+// Up to kChunk slots, one launch (align_small_kernel: one block counts, scans
+// and scatters with the same steps); beyond that three launches over chunks of
+// kChunk slots:
 //   1. count:   per-chunk histogram of expert ids              -> ws[chunk][E]
 //   2. scan:    one block turns the histograms into expert offsets, per-chunk
 //               bases (in place) and the tile map
@@ -164,6 +166,78 @@ __global__ void __launch_bounds__(kThreads)
   }
 }
 
+// Small problems (S <= kChunk): count, scan and stable scatter in one block of
+// kScanThreads threads, the scatter in rounds of kScanThreads slots ranked as in
+// align_scatter_kernel.  Dynamic shared memory: (1 + 32) * E ints.
+__global__ void __launch_bounds__(kScanThreads)
+    align_small_kernel(const int32_t* __restrict__ ids, int S, int E, int block_m, int32_t* __restrict__ offsets,
+                       int32_t* __restrict__ tile_map, int32_t* __restrict__ num_tiles,
+                       int32_t* __restrict__ sorted_slot, int32_t* __restrict__ inv_slot) {
+  constexpr int kW = kScanThreads / 32;
+  extern __shared__ int32_t sm[];
+  int32_t* h = sm;         // [E] counts, then the running row of each expert
+  int32_t* wcnt = sm + E;  // [kW][E] (round + 1) << 16 | count of the expert in that warp
+  __shared__ int warp_tot[32];
+  __shared__ int total_rows, total_tiles;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int i = threadIdx.x; i < E; i += kScanThreads) h[i] = 0;
+  for (int i = threadIdx.x; i < kW * E; i += kScanThreads) wcnt[i] = 0;
+  __syncthreads();
+  for (int f = threadIdx.x; f < S; f += kScanThreads) {
+    const int e = __ldg(ids + f);
+    if ((unsigned)e < (unsigned)E)
+      atomicAdd(&h[e], 1);
+    else
+      record_status((int)MOE_ERR_INVALID_ARG);  // the slot is left out of the permutation
+  }
+  __syncthreads();
+  const int e = threadIdx.x;
+  const int count = e < E ? h[e] : 0;
+  const int off = block_exclusive_scan(count, warp_tot, &total_rows);
+  const int ntile = e < E ? (count + block_m - 1) / block_m : 0;
+  const int tstart = block_exclusive_scan(ntile, warp_tot, &total_tiles);
+  if (e < E) {
+    offsets[e] = off;
+    h[e] = off;
+    for (int i = 0; i < ntile; ++i) {
+      tile_map[2 * (tstart + i)] = e;
+      tile_map[2 * (tstart + i) + 1] = off + i * block_m;
+    }
+  }
+  if (threadIdx.x == 0) {
+    offsets[E] = total_rows;
+    *num_tiles = total_tiles;
+  }
+  __syncthreads();
+  for (int r = 0; r * kScanThreads < S; ++r) {
+    const int f = r * kScanThreads + threadIdx.x;
+    int x = f < S ? __ldg(ids + f) : -1;
+    const bool valid = (unsigned)x < (unsigned)E;
+    if (!valid) x = -1;
+    const uint32_t peers = __match_any_sync(0xffffffffu, x);
+    const int in_warp = __popc(peers & ((1u << lane) - 1u));
+    const bool leader = in_warp == 0;
+    const int tag = (r + 1) << 16;
+    if (valid && leader) wcnt[warp * E + x] = tag | __popc(peers);
+    __syncthreads();
+    int before = 0, after = 0;
+    if (valid) {
+      for (int w = 0; w < kW; ++w) {
+        const int v = wcnt[w * E + x];
+        const int c = (v & 0xFFFF0000) == tag ? (v & 0xFFFF) : 0;
+        if (w < warp) before += c;
+        if (w > warp) after += c;
+      }
+      const int p = h[x] + before + in_warp;
+      sorted_slot[p] = f;
+      if (inv_slot) inv_slot[f] = p;
+    }
+    __syncthreads();
+    if (valid && leader && after == 0) h[x] += before + __popc(peers);
+    __syncthreads();
+  }
+}
+
 }  // namespace
 
 MOE_DEFINE_STATUS_READER(align_status)
@@ -200,6 +274,21 @@ extern "C" moe_status_t moe_align(const int32_t* topk_ids, int T, int top_k, int
     if (!ws || ws_bytes < moe_align_workspace_size(T, top_k, E)) return MOE_ERR_WORKSPACE;
   }
   const int nchunks = (S + kChunk - 1) / kChunk;
+  if (nchunks == 1) {
+    const size_t smem = (size_t)(1 + kScanThreads / 32) * E * sizeof(int32_t);  // <= 132 KB at E = 1024
+    static int configured[64] = {0};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 64 && !configured[dev]) {
+      if (cudaFuncSetAttribute(align_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)((1 + kScanThreads / 32) * kScanThreads * sizeof(int32_t))) != cudaSuccess)
+        return MOE_ERR_CUDA;
+      configured[dev] = 1;
+    }
+    align_small_kernel<<<1, kScanThreads, smem, s>>>(topk_ids, S, E, block_m, expert_offsets, tile_map, num_tiles,
+                                                     sorted_slot, inv_slot);
+    return launch_status();
+  }
   int32_t* hist = static_cast<int32_t*>(ws);
   if (nchunks > 0) align_count_kernel<<<nchunks, kThreads, E * sizeof(int32_t), s>>>(topk_ids, S, E, hist);
   align_scan_kernel<<<1, kScanThreads, 0, s>>>(hist, nchunks, E, block_m, expert_offsets, tile_map, num_tiles);

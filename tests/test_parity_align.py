@@ -37,7 +37,9 @@ def test_align_configs(cuda_dev, name):
 
 
 @pytest.mark.parametrize("T,k,E,bm", [(1, 1, 1, 128), (3, 2, 4, 1), (999, 3, 7, 128), (5000, 8, 1024, 128),
-                                      (2049, 1, 16, 64), (16384, 8, 256, 128)])
+                                      (2049, 1, 16, 64), (16384, 8, 256, 128),
+                                      # one-block path (at most 2048 slots): 1024 experts, exactly 2048 slots
+                                      (700, 2, 1024, 128), (1024, 2, 64, 16)])
 def test_align_random(cuda_dev, T, k, E, bm):
     _check(_random_ids(T, k, E, T + E), E, cuda_dev, bm)
 
