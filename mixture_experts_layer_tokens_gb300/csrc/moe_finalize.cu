@@ -75,6 +75,12 @@ __global__ void __launch_bounds__(kThreads)
   const size_t row = (size_t)t * H;
 
   if (threadIdx.x == 0) {
+    // one CTA per token: its expert rows 1..k-1 (row 0 is loaded at once; measured: with
+    // clusters, whose slices are short, the extra requests cost more than they save)
+    if (kC == 1)
+      for (int j = 1; j < top_k; ++j)
+        prefetch_l2(y + ((size_t)t * top_k + j) * H, (uint32_t)H * 2);
+    // then the shared and residual slices
     if (shared) prefetch_l2(shared + row + (size_t)v0 * 8, (uint32_t)vslice * 16);
     if (residual) prefetch_l2(residual + row + (size_t)v0 * 8, (uint32_t)vslice * 16);
   }
