@@ -221,14 +221,58 @@ def silu_and_mul(gu: torch.Tensor) -> torch.Tensor:
     return g / (1.0 + torch.exp(-g)) * u
 
 
-def expert_rows(A64: torch.Tensor, W13: torch.Tensor, W2: torch.Tensor, quant: str) -> torch.Tensor:
+# The activation column of the "Fused Experts Kernels" table (vLLM design doc)
+# lists silu, gelu, swigluoai, silu_no_mul and gelu_no_mul (triton row) and
+# gelu_tanh (cpu_moe row) without formulas.  Readings taken here:
+# * gated forms (silu, gelu, gelu_tanh): h = act(g) * u with g, u the gate and
+#   up halves of x = A w13^T (w13 rows 0..I-1 gate, I..2I-1 up);
+# * *_no_mul forms: w13 holds the I gate rows only and h = act(g);
+# * gelu is the exact form g * Phi(g) = g/2 (1 + erf(g / sqrt 2)); gelu_tanh is
+#   the usual tanh approximation g/2 (1 + tanh(sqrt(2/pi) (g + 0.044715 g^3)));
+# * swigluoai is the clamped SwiGLU of the gpt-oss models as published with them:
+#   g' = min(g, 7), u' = clamp(u, -7, 7), h = (u' + 1) * g' * sigmoid(1.702 g'),
+#   with the same gate-then-up layout of w13 as the other gated forms.
+ACTIVATIONS = ("silu", "gelu", "gelu_tanh", "swigluoai", "silu_no_mul", "gelu_no_mul")
+SWIGLUOAI_ALPHA = 1.702
+SWIGLUOAI_LIMIT = 7.0
+
+
+def activation_is_gated(activation: str) -> bool:
+    if activation not in ACTIVATIONS:
+        raise ValueError(f"unknown activation {activation!r}")
+    return not activation.endswith("_no_mul")
+
+
+def activation(x: torch.Tensor, name: str) -> torch.Tensor:
+    """h = act(x) between the two expert GEMMs, fp64, by the readings above.
+    Gated forms take x = [g | u] ([rows, 2I]); *_no_mul forms take x = g ([rows, I])."""
+    if activation_is_gated(name):
+        I = x.shape[1] // 2
+        g, u = x[:, :I], x[:, I:]
+    else:
+        g, u = x, None
+    if name == "swigluoai":
+        gc = torch.clamp(g, max=SWIGLUOAI_LIMIT)
+        uc = torch.clamp(u, min=-SWIGLUOAI_LIMIT, max=SWIGLUOAI_LIMIT)
+        return (uc + 1.0) * gc / (1.0 + torch.exp(-SWIGLUOAI_ALPHA * gc))
+    if name in ("silu", "silu_no_mul"):
+        a = g / (1.0 + torch.exp(-g))
+    elif name in ("gelu", "gelu_no_mul"):
+        a = 0.5 * g * (1.0 + torch.erf(g / math.sqrt(2.0)))
+    else:  # gelu_tanh
+        a = 0.5 * g * (1.0 + torch.tanh(math.sqrt(2.0 / math.pi) * (g + 0.044715 * g ** 3)))
+    return a if u is None else a * u
+
+
+def expert_rows(A64: torch.Tensor, W13: torch.Tensor, W2: torch.Tensor, quant: str,
+                act: str = "silu") -> torch.Tensor:
     """One expert on a block of (already dequantised) input rows.
 
-    g, u = A W13[:I]^T, A W13[I:]^T (fp64); h = silu(g) * u, stored the way the
-    intermediate is stored (bf16, or re-quantised to fp8 G(128) when the
-    activations are fp8); y = h W2^T in fp64, stored bf16.  Returns fp64 values
-    of the stored bf16 y."""
-    h = silu_and_mul(A64 @ W13.T)
+    g, u = A W13[:I]^T, A W13[I:]^T (fp64); h = silu(g) * u (or the activation
+    ``act``, see ``activation``), stored the way the intermediate is stored
+    (bf16, or re-quantised to fp8 G(128) when the activations are fp8);
+    y = h W2^T in fp64, stored bf16.  Returns fp64 values of the stored bf16 y."""
+    h = silu_and_mul(A64 @ W13.T) if act == "silu" else activation(A64 @ W13.T, act)
     hn = h.numpy()
     if quant == "bf16":
         h_st = codecs.round_bf16(hn)
@@ -251,7 +295,8 @@ def _act64(a1q, a1q_scale, rows, quant):
     return torch.from_numpy(dequant_fp8_g128(_np(a1q)[rows].astype(np.uint8), _np(a1q_scale)[rows]))
 
 
-def experts(a1q, a1q_scale, w13, w13_scale, w2, w2_scale, al: Alignment, top_k: int, quant: str) -> torch.Tensor:
+def experts(a1q, a1q_scale, w13, w13_scale, w2, w2_scale, al: Alignment, top_k: int, quant: str,
+            act: str = "silu") -> torch.Tensor:
     """Grouped expert computation: for every expert e and every sorted row
     p in [offsets[e], offsets[e+1]), slot f = sorted_slot[p] of token t = f // k
     gets y[f] = expert_e(a1q[t]).  Output: the unweighted expert rows in
@@ -269,17 +314,18 @@ def experts(a1q, a1q_scale, w13, w13_scale, w2, w2_scale, al: Alignment, top_k: 
         slots = order[p0:p1]
         A = _act64(a1q, a1q_scale, slots // top_k, quant)
         y[torch.from_numpy(slots.astype(np.int64))] = expert_rows(
-            A, _weights64(w13, w13_scale, e, quant), _weights64(w2, w2_scale, e, quant), quant)
+            A, _weights64(w13, w13_scale, e, quant), _weights64(w2, w2_scale, e, quant), quant, act)
     return y
 
 
-def token_expert_rows(a1q, a1q_scale, w13, w13_scale, w2, w2_scale, topk_ids, t: int, quant: str) -> torch.Tensor:
+def token_expert_rows(a1q, a1q_scale, w13, w13_scale, w2, w2_scale, topk_ids, t: int, quant: str,
+                      act: str = "silu") -> torch.Tensor:
     """The k expert rows of one token, y[t*k + j] for j < k (used to check
     sampled tokens of full-size layers one by one)."""
     ids = _np(topk_ids)[t]
     A = _act64(a1q, a1q_scale, np.array([t]), quant)
     return torch.cat([expert_rows(A, _weights64(w13, w13_scale, int(e), quant),
-                                  _weights64(w2, w2_scale, int(e), quant), quant) for e in ids], 0)
+                                  _weights64(w2, w2_scale, int(e), quant), quant, act) for e in ids], 0)
 
 
 def dense_mlp(x: torch.Tensor, w13: torch.Tensor, w2: torch.Tensor) -> torch.Tensor:
