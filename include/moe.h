@@ -63,6 +63,26 @@ typedef enum {
   MOE_SCORING_SIGMOID = 1         /* top-1, weight = sigmoid(logit)           */
 } moe_scoring_t;
 
+/* Activation between the two expert GEMMs: the activation column of the
+ * "Fused Experts Kernels" table (vLLM design doc), which names them without
+ * formulas.  With [g | u] = x . w13^T (gate rows first):
+ *   MOE_ACT_SILU         h = silu(g) * u,  silu(g) = g / (1 + exp(-g))
+ *   MOE_ACT_GELU         h = gelu(g) * u,  gelu(g) = g/2 (1 + erf(g / sqrt 2))
+ *   MOE_ACT_GELU_TANH    h = g/2 (1 + tanh(sqrt(2/pi) (g + 0.044715 g^3))) * u
+ *   MOE_ACT_SWIGLUOAI    the clamped SwiGLU of the gpt-oss models:
+ *                        g' = min(g, 7), u' = clamp(u, -7, 7),
+ *                        h = (u' + 1) * g' * sigmoid(1.702 g')
+ *   MOE_ACT_SILU_NO_MUL  h = silu(g); w13 holds the I gate rows only
+ *   MOE_ACT_GELU_NO_MUL  h = gelu(g); w13 holds the I gate rows only */
+typedef enum {
+  MOE_ACT_SILU = 0,
+  MOE_ACT_GELU = 1,
+  MOE_ACT_GELU_TANH = 2,
+  MOE_ACT_SWIGLUOAI = 3,
+  MOE_ACT_SILU_NO_MUL = 4,
+  MOE_ACT_GELU_NO_MUL = 5
+} moe_activation_t;
+
 /* Quantisation of the expert inputs and weights.
  *   bf16:  {MOE_DT_BF16, 0, MOE_DT_BF16, 0, 0}   -- "no quantisation type"
  *   fp8:   {MOE_DT_FP8_E4M3, 128, MOE_DT_FP8_E4M3, 128, 128}
@@ -185,6 +205,17 @@ moe_status_t moe_experts(const void *a1q, const float *a1q_scale, const void *w1
                          int I, int E, int top_k, const moe_quant_config *qc,
                          void *fused_expert_output, void *ws, size_t ws_bytes,
                          moe_stream_t stream);
+/* moe_experts with another activation (a moe_activation_t); moe_experts is
+ * this call with MOE_ACT_SILU.  For the *_NO_MUL activations w13 is [E, I, H]
+ * (fp8: w13_scale [E, I/128, H/128]).  Same arguments, workspace and errors
+ * otherwise; an unknown activation returns MOE_ERR_UNSUPPORTED. */
+moe_status_t moe_experts_act(const void *a1q, const float *a1q_scale, const void *w13,
+                             const float *w13_scale, const void *w2, const float *w2_scale,
+                             const int32_t *expert_offsets, const int32_t *sorted_slot,
+                             const int32_t *tile_map, const int32_t *num_tiles, int T, int H,
+                             int I, int E, int top_k, const moe_quant_config *qc, int activation,
+                             void *fused_expert_output, void *ws, size_t ws_bytes,
+                             moe_stream_t stream);
 size_t moe_workspace_size(int T, int H, int I, int E, int top_k, const moe_quant_config *qc);
 
 /* ------------------------------------------------------------------ finalize

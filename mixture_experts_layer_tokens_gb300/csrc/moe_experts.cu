@@ -228,7 +228,28 @@ __device__ __forceinline__ void signal_split_partial(int* flag) {
   if ((threadIdx.x & 31) == 0) atomicAdd(flag, 32);
 }
 
-__device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + __expf(-g)) * u; }
+// Activations between the two GEMMs (moe_activation_t): act_gate is the gate's
+// function alone (the *_NO_MUL forms), act_mul the gated form h(g, u).
+__device__ __forceinline__ float act_silu(float g) { return g / (1.0f + __expf(-g)); }
+__device__ __forceinline__ float act_gelu(float g) { return 0.5f * g * (1.0f + erff(g * 0.70710678118654752f)); }
+__device__ __forceinline__ float act_gelu_tanh(float g) {
+  return 0.5f * g * (1.0f + tanhf(0.79788456080286536f * (g + 0.044715f * g * g * g)));
+}
+template <int kAct>
+__device__ __forceinline__ float act_gate(float g) {
+  if (kAct == MOE_ACT_GELU || kAct == MOE_ACT_GELU_NO_MUL) return act_gelu(g);
+  if (kAct == MOE_ACT_GELU_TANH) return act_gelu_tanh(g);
+  return act_silu(g);
+}
+template <int kAct>
+__device__ __forceinline__ float act_mul(float g, float u) {
+  if (kAct == MOE_ACT_SWIGLUOAI) {
+    // gpt-oss SwiGLU: gate clamped above at 7, up clamped to [-7, 7], sigmoid(1.702 g)
+    const float gc = fminf(g, 7.0f), uc = fminf(fmaxf(u, -7.0f), 7.0f);
+    return (uc + 1.0f) * (gc / (1.0f + __expf(-1.702f * gc)));
+  }
+  return act_gate<kAct>(g) * u;
+}
 
 // (a0, a1) += (v0, v1) * s with one packed two-wide fp32 FMA (each lane an IEEE fma)
 __device__ __forceinline__ void fma2(float& a0, float& a1, float v0, float v1, float s) {
@@ -239,11 +260,15 @@ __device__ __forceinline__ void fma2(float& a0, float& a1, float v0, float v1, f
       : "f"(v0), "f"(v1), "f"(s));
 }
 
-template <bool kFP8, int kKind, int kMG>
+template <bool kFP8, int kKind, int kMG, int kAct>
 __global__ void __launch_bounds__(Warps<kFP8>::THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
                 const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
   using C = Cfg<kFP8, kMG>;
+  // gemm1 forms: a gated activation reads 128 gate + 128 up rows per unit (one 3-D
+  // box); a *_NO_MUL one reads 256 consecutive gate rows, like gemm2
+  constexpr bool kNoMul = kKind == kGemm1 && (kAct == MOE_ACT_SILU_NO_MUL || kAct == MOE_ACT_GELU_NO_MUL);
+  constexpr bool kPair = kKind == kGemm1 && !kNoMul;
   constexpr int EPI_WARPS = Warps<kFP8>::EPI;
   constexpr int EPI_THREADS = Warps<kFP8>::EPI_THREADS;
   constexpr int MG = C::MG;
@@ -326,7 +351,7 @@ __global__ void __launch_bounds__(Warps<kFP8>::THREADS, 1)
         pit = decode<MG>(p, pu);
       }
       if (issue) {
-        if (kKind == kGemm1)
+        if (kPair)
           tma_prefetch_3d(&tmB, pf_kb * C::kBK, pit.n * 128, 2 * pit.e);
         else
           tma_prefetch_2d(&tmB, pf_kb * C::kBK, pit.e * p.b_rows + pit.n * 256);
@@ -347,7 +372,7 @@ __global__ void __launch_bounds__(Warps<kFP8>::THREADS, 1)
       const int mcnt = (it.row_end - it.row0 + BM - 1) / BM;
       // gemm1: gate block n of expert e and the up block I rows further (3-D map
       // [2E][I][K], z = 2e gate, 2e + 1 up); gemm2: w2 rows [256 n, +256) of expert e
-      const int brow = kKind == kGemm1 ? it.n * 128 : it.e * p.b_rows + it.n * 256;
+      const int brow = kPair ? it.n * 128 : it.e * p.b_rows + it.n * 256;
       for (int kb = kb0; kb < kb1; ++kb) {
         if (!(ok = warp_wait(&empty[stage], phase ^ 1))) break;
         if (kFP8) {
@@ -362,8 +387,8 @@ __global__ void __launch_bounds__(Warps<kFP8>::THREADS, 1)
           if (lane == 0) {
             const int KBs = p.K / 128, nbw = p.b_rows / 128;
             const float* sw = p.w_scale + (size_t)it.e * nbw * KBs;
-            const int wb0 = kKind == kGemm1 ? it.n : min(2 * it.n, nbw - 1);
-            const int wb1 = kKind == kGemm1 ? p.I / 128 + it.n : min(2 * it.n + 1, nbw - 1);
+            const int wb0 = kPair ? it.n : min(2 * it.n, nbw - 1);
+            const int wb1 = kPair ? p.I / 128 + it.n : min(2 * it.n + 1, nbw - 1);
             cp_async_4(dst + 128, sw + (size_t)wb0 * KBs + kb);
             cp_async_4(dst + 129, sw + (size_t)wb1 * KBs + kb);
           }
@@ -378,7 +403,7 @@ __global__ void __launch_bounds__(Warps<kFP8>::THREADS, 1)
             tma_load_2d(sA, &tmA2, kx, it.row0, &full[stage], pol_a);  // both M tiles, one 256-row box
           else
             tma_load_2d(sA, &tmA, kx, it.row0, &full[stage], pol_a);
-          if (kKind == kGemm1)
+          if (kPair)
             tma_load_3d(sB, &tmB, kx, brow, 2 * it.e, &full[stage], pol_b);
           else
             tma_load_2d(sB, &tmB, kx, brow, &full[stage], pol_b);
@@ -550,14 +575,25 @@ __global__ void __launch_bounds__(Warps<kFP8>::THREADS, 1)
           if (lane == 0) mbar_arrive(xbar);
           ok = warp_wait(xbar, 1) && ok;
           if (ok) {
-            if (kKind == kGemm1) {
-              // h[row][128 n + col] = silu(gate) * up, two columns per thread and step
+            if (kPair) {
+              // h[row][128 n + col] = act(gate, up), two columns per thread and step
               __nv_bfloat16* h = static_cast<__nv_bfloat16*>(p.out) + it.n * 128;
               for (int i = tid; i < nrows * 64; i += EPI_THREADS) {
                 const int row = i >> 6, col = 2 * (i & 63);
                 const float* f = fix + row * FIX_STRIDE + col;
-                const uint32_t o = pack_bf16x2(silu_mul(f[0], f[128]), silu_mul(f[1], f[129]));
+                const uint32_t o = pack_bf16x2(act_mul<kAct>(f[0], f[128]), act_mul<kAct>(f[1], f[129]));
                 *reinterpret_cast<uint32_t*>(h + (size_t)(it.row0 + row) * p.I + col) = o;
+              }
+            } else if (kNoMul) {
+              // h[row][256 n + col] = act(gate)
+              __nv_bfloat16* h = static_cast<__nv_bfloat16*>(p.out) + it.n * 256;
+              const int ncols = min(256, p.I - it.n * 256);
+              for (int i = tid; i < nrows * 128; i += EPI_THREADS) {
+                const int row = i >> 7, col = 2 * (i & 127);
+                if (col >= ncols) continue;
+                const float* f = fix + row * FIX_STRIDE + col;
+                *reinterpret_cast<uint32_t*>(h + (size_t)(it.row0 + row) * p.I + col) =
+                    pack_bf16x2(act_gate<kAct>(f[0]), act_gate<kAct>(f[1]));
               }
             } else {
               // y[sorted_slot[row]][256 n + col], two columns per thread and step
@@ -599,7 +635,7 @@ __global__ void __launch_bounds__(Warps<kFP8>::THREADS, 1)
                 for (int j = 0; j < 8; ++j) __stcg(dst + j, make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
               }
             }
-          } else if (kKind == kGemm1) {
+          } else if (kPair) {
             __nv_bfloat16* hrow = static_cast<__nv_bfloat16*>(p.out) + (size_t)mrow * p.I + it.n * 128;
 #pragma unroll 1
             for (int c = 0; c < 4; ++c) {
@@ -612,11 +648,32 @@ __global__ void __launch_bounds__(Warps<kFP8>::THREADS, 1)
 #pragma unroll
                 for (int v = 0; v < 4; ++v) {
                   uint4 o;
-                  o.x = pack_bf16x2(silu_mul(g[8 * v + 0], uu[8 * v + 0]), silu_mul(g[8 * v + 1], uu[8 * v + 1]));
-                  o.y = pack_bf16x2(silu_mul(g[8 * v + 2], uu[8 * v + 2]), silu_mul(g[8 * v + 3], uu[8 * v + 3]));
-                  o.z = pack_bf16x2(silu_mul(g[8 * v + 4], uu[8 * v + 4]), silu_mul(g[8 * v + 5], uu[8 * v + 5]));
-                  o.w = pack_bf16x2(silu_mul(g[8 * v + 6], uu[8 * v + 6]), silu_mul(g[8 * v + 7], uu[8 * v + 7]));
+                  o.x = pack_bf16x2(act_mul<kAct>(g[8 * v + 0], uu[8 * v + 0]), act_mul<kAct>(g[8 * v + 1], uu[8 * v + 1]));
+                  o.y = pack_bf16x2(act_mul<kAct>(g[8 * v + 2], uu[8 * v + 2]), act_mul<kAct>(g[8 * v + 3], uu[8 * v + 3]));
+                  o.z = pack_bf16x2(act_mul<kAct>(g[8 * v + 4], uu[8 * v + 4]), act_mul<kAct>(g[8 * v + 5], uu[8 * v + 5]));
+                  o.w = pack_bf16x2(act_mul<kAct>(g[8 * v + 6], uu[8 * v + 6]), act_mul<kAct>(g[8 * v + 7], uu[8 * v + 7]));
                   dst[v] = o;
+                }
+              }
+            }
+          } else if (kNoMul) {
+            __nv_bfloat16* hrow = static_cast<__nv_bfloat16*>(p.out) + (size_t)mrow * p.I + it.n * 256;
+            const int ncols = min(256, p.I - it.n * 256);
+#pragma unroll 1
+            for (int c = 0; c < 8; ++c) {
+              float v[32];
+              tmem_ld32(tb + c * 32, v);
+              tmem_ld_wait();
+              if (mvalid && c * 32 < ncols) {
+                uint4* dst = reinterpret_cast<uint4*>(hrow + c * 32);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                  uint4 o;
+                  o.x = pack_bf16x2(act_gate<kAct>(v[8 * j + 0]), act_gate<kAct>(v[8 * j + 1]));
+                  o.y = pack_bf16x2(act_gate<kAct>(v[8 * j + 2]), act_gate<kAct>(v[8 * j + 3]));
+                  o.z = pack_bf16x2(act_gate<kAct>(v[8 * j + 4]), act_gate<kAct>(v[8 * j + 5]));
+                  o.w = pack_bf16x2(act_gate<kAct>(v[8 * j + 6]), act_gate<kAct>(v[8 * j + 7]));
+                  dst[j] = o;
                 }
               }
             }
@@ -666,8 +723,8 @@ __global__ void __launch_bounds__(Warps<kFP8>::THREADS, 1)
           const float* ring = scale_ring + slot * C::SCALE_SLOT_FLOATS;
           const float a_s = ring[r];
           // gemm1: accv[0..63] gate block, accv[64..127] up block; gemm2: this half's block
-          const float s0 = a_s * ring[kKind == kGemm1 ? 128 : 128 + half];
-          const float s1 = a_s * ring[kKind == kGemm1 ? 129 : 128 + half];
+          const float s0 = a_s * ring[kPair ? 128 : 128 + half];
+          const float s1 = a_s * ring[kPair ? 129 : 128 + half];
           __syncwarp();
           if (lane == 0) mbar_arrive(&sempty[slot]);
           ++sfill;
@@ -677,12 +734,12 @@ __global__ void __launch_bounds__(Warps<kFP8>::THREADS, 1)
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
             // gemm1: chunks 0,1 gate, 2,3 up; gemm2: 4 consecutive chunks
-            const int col = kKind == kGemm1 ? (c < 2 ? 64 * half + 32 * c : 128 + 64 * half + 32 * (c - 2))
+            const int col = kPair ? (c < 2 ? 64 * half + 32 * c : 128 + 64 * half + 32 * (c - 2))
                                             : 128 * half + 32 * c;
             float v[32];
             tmem_ld32(tb + col, v);
             tmem_ld_wait();
-            const float sc = (kKind == kGemm1 && c >= 2) ? s1 : s0;
+            const float sc = (kPair && c >= 2) ? s1 : s0;
 #pragma unroll
             for (int i = 0; i < 32; i += 2) fma2(accv[32 * c + i], accv[32 * c + i + 1], v[i], v[i + 1], sc);
           }
@@ -717,12 +774,40 @@ __global__ void __launch_bounds__(Warps<kFP8>::THREADS, 1)
             }
           }
         }
-        if (kKind == kGemm1) {
-          // h = silu(g) * u for 64 columns, then E4M3 G(128) over the 128 columns of this row
+        if (kNoMul) {
+          // h = act(g) for this thread's 128 columns, which are one G(128) group (2n + half)
+          const int grp = 2 * it.n + half;
+          float amax = 0.f;
+#pragma unroll
+          for (int i = 0; i < 128; ++i) {
+            accv[i] = act_gate<kAct>(accv[i]);
+            amax = fmaxf(amax, fabsf(accv[i]));
+          }
+          const float s = __fdiv_rn(fmaxf(amax, 1e-10f), 448.0f);
+          if (valid && grp * 128 < p.I) {
+            uint8_t* hrow = static_cast<uint8_t*>(p.out) + (size_t)prow * p.I + grp * 128;
+#pragma unroll
+            for (int v = 0; v < 8; ++v) {
+              uint32_t wds[4];
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                const int i0 = 16 * v + 4 * j;
+                const uint32_t lo = (uint32_t)__nv_cvt_float2_to_fp8x2(
+                    make_float2(__fdiv_rn(accv[i0], s), __fdiv_rn(accv[i0 + 1], s)), __NV_SATFINITE, __NV_E4M3);
+                const uint32_t hi = (uint32_t)__nv_cvt_float2_to_fp8x2(
+                    make_float2(__fdiv_rn(accv[i0 + 2], s), __fdiv_rn(accv[i0 + 3], s)), __NV_SATFINITE, __NV_E4M3);
+                wds[j] = lo | (hi << 16);
+              }
+              reinterpret_cast<uint4*>(hrow)[v] = make_uint4(wds[0], wds[1], wds[2], wds[3]);
+            }
+            p.out_scale_t[(size_t)grp * p.s_pad + prow] = s;
+          }
+        } else if (kPair) {
+          // h = act(g, u) for 64 columns, then E4M3 G(128) over the 128 columns of this row
           float amax = 0.f;
 #pragma unroll
           for (int i = 0; i < 64; ++i) {
-            accv[i] = silu_mul(accv[i], accv[64 + i]);
+            accv[i] = act_mul<kAct>(accv[i], accv[64 + i]);
             amax = fmaxf(amax, fabsf(accv[i]));
           }
           // exchange with the warp holding the other 64 columns of these rows (bounded wait)
@@ -916,20 +1001,35 @@ bool make_map_gate_up(CUtensorMap* m, const void* base, bool fp8, long long k, l
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <bool kFP8, int kKind, int kMG>
+template <bool kFP8, int kKind, int kMG, int kAct>
 cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& a2, const CUtensorMap& b, const GemmParams& p, int grid,
                         cudaStream_t s) {
   static int configured[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_kernel<kFP8, kKind, kMG>,
+    cudaError_t e = cudaFuncSetAttribute(gemm_kernel<kFP8, kKind, kMG, kAct>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<kFP8, kMG>::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     configured[dev] = 1;
   }
-  gemm_kernel<kFP8, kKind, kMG><<<grid, Warps<kFP8>::THREADS, Cfg<kFP8, kMG>::SMEM_BYTES, s>>>(a, a2, b, p);
+  gemm_kernel<kFP8, kKind, kMG, kAct><<<grid, Warps<kFP8>::THREADS, Cfg<kFP8, kMG>::SMEM_BYTES, s>>>(a, a2, b, p);
   return cudaGetLastError();
+}
+
+// gemm1 with the activation chosen at run time
+template <bool kFP8, int kMG>
+cudaError_t launch_gemm1(int act, const CUtensorMap& a, const CUtensorMap& a2, const CUtensorMap& b,
+                         const GemmParams& p, int grid, cudaStream_t s) {
+  switch (act) {
+    case MOE_ACT_SILU: return launch_gemm<kFP8, kGemm1, kMG, MOE_ACT_SILU>(a, a2, b, p, grid, s);
+    case MOE_ACT_GELU: return launch_gemm<kFP8, kGemm1, kMG, MOE_ACT_GELU>(a, a2, b, p, grid, s);
+    case MOE_ACT_GELU_TANH: return launch_gemm<kFP8, kGemm1, kMG, MOE_ACT_GELU_TANH>(a, a2, b, p, grid, s);
+    case MOE_ACT_SWIGLUOAI: return launch_gemm<kFP8, kGemm1, kMG, MOE_ACT_SWIGLUOAI>(a, a2, b, p, grid, s);
+    case MOE_ACT_SILU_NO_MUL: return launch_gemm<kFP8, kGemm1, kMG, MOE_ACT_SILU_NO_MUL>(a, a2, b, p, grid, s);
+    case MOE_ACT_GELU_NO_MUL: return launch_gemm<kFP8, kGemm1, kMG, MOE_ACT_GELU_NO_MUL>(a, a2, b, p, grid, s);
+  }
+  return cudaErrorInvalidValue;
 }
 
 struct WsLayout {
@@ -991,12 +1091,16 @@ extern "C" size_t moe_workspace_size(int T, int H, int I, int E, int top_k, cons
   return ws_layout((long long)T * top_k, H, I, E, qc->act == MOE_DT_FP8_E4M3, gemm_grid()).total;
 }
 
-extern "C" moe_status_t moe_experts(const void* a1q, const float* a1q_scale, const void* w13, const float* w13_scale,
-                                    const void* w2, const float* w2_scale, const int32_t* expert_offsets,
-                                    const int32_t* sorted_slot, const int32_t* tile_map, const int32_t* num_tiles,
-                                    int T, int H, int I, int E, int top_k, const moe_quant_config* qc,
-                                    void* fused_expert_output, void* ws, size_t ws_bytes, moe_stream_t stream) {
+extern "C" moe_status_t moe_experts_act(const void* a1q, const float* a1q_scale, const void* w13,
+                                        const float* w13_scale, const void* w2, const float* w2_scale,
+                                        const int32_t* expert_offsets, const int32_t* sorted_slot,
+                                        const int32_t* tile_map, const int32_t* num_tiles, int T, int H, int I, int E,
+                                        int top_k, const moe_quant_config* qc, int activation,
+                                        void* fused_expert_output, void* ws, size_t ws_bytes, moe_stream_t stream) {
   MOE_CHECK_ARG(qc && T >= 0 && H > 0 && I > 0 && E >= 1 && top_k >= 1 && top_k <= E);
+  if (activation < MOE_ACT_SILU || activation > MOE_ACT_GELU_NO_MUL) return MOE_ERR_UNSUPPORTED;
+  const bool no_mul = activation == MOE_ACT_SILU_NO_MUL || activation == MOE_ACT_GELU_NO_MUL;
+  const int nt1 = no_mul ? (I + 255) / 256 : I / 128;  // gemm1 N tiles: 256 gate rows, or 128 gate + 128 up
   const bool fp8 = qc->act == MOE_DT_FP8_E4M3;
   if (fp8) {
     if (qc->act_group != 128 || qc->weight != MOE_DT_FP8_E4M3 || qc->w_block_n != 128 || qc->w_block_k != 128)
@@ -1045,7 +1149,7 @@ extern "C" moe_status_t moe_experts(const void* a1q, const float* a1q_scale, con
     const long long units2 = (long long)((cap_tiles + 1) / 2) * nt;  // estimate with two tiles per unit
     return (!fp8 && full_tiles && 2 * units2 >= grid_sms && units2 <= grid_sms) ? 2 : 1;
   };
-  const int mg1 = mg_for(I / 128), mg2 = mg_for((H + 255) / 256);
+  const int mg1 = mg_for(nt1), mg2 = mg_for((H + 255) / 256);
   int32_t* gmap2 = reinterpret_cast<int32_t*>(wsb + L.gmap2);
   int32_t* ngroups2 = reinterpret_cast<int32_t*>(wsb + L.ngroups2);
   const bool allow_split = !fp8 && S <= 16LL * E;  // decode-sized: units may be split across CTAs
@@ -1070,8 +1174,9 @@ extern "C" moe_status_t moe_experts(const void* a1q, const float* a1q_scale, con
   // the last N tile of an expert with H % 256 == 128 reads 128 rows past it, which
   // land in discarded output columns, zero-filled past the last expert)
   CUtensorMap mA1, mA1x2, mB1, mA2, mA2x2, mB2;
-  if (!make_map(&mA1, A, fp8, H, S, 128) || !make_map(&mA1x2, A, fp8, H, S, 256) ||
-      !make_map_gate_up(&mB1, w13, fp8, H, I, E) || !make_map(&mA2, h, fp8, I, S, 128) ||
+  const bool b1_ok = no_mul ? make_map(&mB1, w13, fp8, H, (long long)E * I, 256) : make_map_gate_up(&mB1, w13, fp8, H, I, E);
+  if (!make_map(&mA1, A, fp8, H, S, 128) || !make_map(&mA1x2, A, fp8, H, S, 256) || !b1_ok ||
+      !make_map(&mA2, h, fp8, I, S, 128) ||
       !make_map(&mA2x2, h, fp8, I, S, 256) || !make_map(&mB2, w2, fp8, I, (long long)E * H, 256))
     return MOE_ERR_CUDA;
 
@@ -1081,10 +1186,10 @@ extern "C" moe_status_t moe_experts(const void* a1q, const float* a1q_scale, con
   p1.num_groups = ngroups;
   p1.sorted_slot = sorted_slot;
   p1.K = H;
-  p1.NT = I / 128;
+  p1.NT = nt1;
   p1.I = I;
   p1.H = H;
-  p1.b_rows = 2 * I;
+  p1.b_rows = no_mul ? I : 2 * I;
   p1.s_pad = L.s_pad;
   p1.a_scale_t = As;
   p1.w_scale = w13_scale;
@@ -1109,14 +1214,23 @@ extern "C" moe_status_t moe_experts(const void* a1q, const float* a1q_scale, con
 
   cudaError_t e;
   if (fp8) {
-    e = launch_gemm<true, kGemm1, 1>(mA1, mA1x2, mB1, p1, grid, s);
-    if (e == cudaSuccess) e = launch_gemm<true, kGemm2, 1>(mA2, mA2x2, mB2, p2, grid, s);
+    e = launch_gemm1<true, 1>(activation, mA1, mA1x2, mB1, p1, grid, s);
+    if (e == cudaSuccess) e = launch_gemm<true, kGemm2, 1, 0>(mA2, mA2x2, mB2, p2, grid, s);
   } else {
-    e = mg1 == 1 ? launch_gemm<false, kGemm1, 1>(mA1, mA1x2, mB1, p1, grid, s)
-                 : launch_gemm<false, kGemm1, 2>(mA1, mA1x2, mB1, p1, grid, s);
+    e = mg1 == 1 ? launch_gemm1<false, 1>(activation, mA1, mA1x2, mB1, p1, grid, s)
+                 : launch_gemm1<false, 2>(activation, mA1, mA1x2, mB1, p1, grid, s);
     if (e == cudaSuccess)
-      e = mg2 == 1 ? launch_gemm<false, kGemm2, 1>(mA2, mA2x2, mB2, p2, grid, s)
-                   : launch_gemm<false, kGemm2, 2>(mA2, mA2x2, mB2, p2, grid, s);
+      e = mg2 == 1 ? launch_gemm<false, kGemm2, 1, 0>(mA2, mA2x2, mB2, p2, grid, s)
+                   : launch_gemm<false, kGemm2, 2, 0>(mA2, mA2x2, mB2, p2, grid, s);
   }
   return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+extern "C" moe_status_t moe_experts(const void* a1q, const float* a1q_scale, const void* w13, const float* w13_scale,
+                                    const void* w2, const float* w2_scale, const int32_t* expert_offsets,
+                                    const int32_t* sorted_slot, const int32_t* tile_map, const int32_t* num_tiles,
+                                    int T, int H, int I, int E, int top_k, const moe_quant_config* qc,
+                                    void* fused_expert_output, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  return moe_experts_act(a1q, a1q_scale, w13, w13_scale, w2, w2_scale, expert_offsets, sorted_slot, tile_map,
+                         num_tiles, T, H, I, E, top_k, qc, MOE_ACT_SILU, fused_expert_output, ws, ws_bytes, stream);
 }

@@ -21,6 +21,8 @@ MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE, MOE_ERR_CUD
 MOE_DT_BF16, MOE_DT_FP8_E4M3, MOE_DT_NVFP4, MOE_DT_FP32 = range(4)
 MOE_SCORING_SOFTMAX_RENORM, MOE_SCORING_SIGMOID = 0, 1
 MOE_BLOCK_M = 128
+# moe_activation_t, by the names of the "Fused Experts Kernels" table
+ACTIVATIONS = {"silu": 0, "gelu": 1, "gelu_tanh": 2, "swigluoai": 3, "silu_no_mul": 4, "gelu_no_mul": 5}
 
 # (name, argtypes, restype) of every exported entry point
 _P, _I, _F, _Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
@@ -43,6 +45,7 @@ SIGNATURES = {
     "moe_tile_map_capacity": ([_I, _I, _I], _I),
     "moe_prepare": ([_P, _P, _P, _I, _I, _I, _I, _QCP, _P, _P, _P], _I),
     "moe_experts": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _QCP, _P, _P, _Z, _P], _I),
+    "moe_experts_act": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _QCP, _I, _P, _P, _Z, _P], _I),
     "moe_workspace_size": ([_I, _I, _I, _I, _I, _QCP], _Z),
     "moe_finalize": ([_P, _P, _P, _P, _P, _P, _P, _F, _I, _I, _I, _I, _I, _P, _F, _P, _P], _I),
     "moe_device_status": ([_I], _I),
@@ -200,9 +203,13 @@ def workspace_size(T: int, H: int, I: int, E: int, top_k: int, quant: str) -> in
 def moe_experts(a1q: torch.Tensor, a1q_scale: Optional[torch.Tensor], w13: torch.Tensor,
                 w13_scale: Optional[torch.Tensor], w2: torch.Tensor, w2_scale: Optional[torch.Tensor],
                 al: Alignment, quant: str, out: Optional[torch.Tensor] = None, ws: Optional[torch.Tensor] = None,
-                identity: bool = False, stream=None) -> torch.Tensor:
-    """Grouped SwiGLU experts.  ``identity=True`` (E == 1, top_k == 1) passes a
-    NULL sorted_slot: rows are the tokens in order."""
+                identity: bool = False, stream=None, activation: str = "silu") -> torch.Tensor:
+    """Grouped expert MLPs (``moe_experts_act``; SiLU-and-mul by default, see
+    ``ACTIVATIONS``; the *_no_mul activations take w13 [E, I, H]).
+    ``identity=True`` (E == 1, top_k == 1) passes a NULL sorted_slot: rows are
+    the tokens in order."""
+    if activation not in ACTIVATIONS:
+        raise ValueError(f"unknown activation {activation!r}")
     fp8 = quant == "fp8"
     _need(a1q, torch.uint8 if fp8 else torch.bfloat16, "a1q")
     _need(w13, torch.uint8 if fp8 else torch.bfloat16, "w13")
@@ -210,8 +217,8 @@ def moe_experts(a1q: torch.Tensor, a1q_scale: Optional[torch.Tensor], w13: torch
     for t, n in ((a1q_scale, "a1q_scale"), (w13_scale, "w13_scale"), (w2_scale, "w2_scale")):
         _need(t, torch.float32, n)
     T, H = a1q.shape
-    E, twoI, _ = w13.shape
-    I = twoI // 2
+    E, rows13, _ = w13.shape
+    I = rows13 if activation.endswith("_no_mul") else rows13 // 2
     k = al.top_k
     if out is None:
         out = torch.empty((T * k, H), dtype=torch.bfloat16, device=a1q.device)
@@ -219,10 +226,10 @@ def moe_experts(a1q: torch.Tensor, a1q_scale: Optional[torch.Tensor], w13: torch
     if ws is None:
         ws = torch.empty(max(workspace_size(T, H, I, E, k, quant), 16), dtype=torch.uint8, device=a1q.device)
     qc = QC_FP8 if fp8 else QC_BF16
-    _check("moe_experts", lib().moe_experts(
+    _check("moe_experts_act", lib().moe_experts_act(
         _ptr(a1q), _ptr(a1q_scale), _ptr(w13), _ptr(w13_scale), _ptr(w2), _ptr(w2_scale), _ptr(al.expert_offsets),
         None if identity else _ptr(al.sorted_slot), _ptr(al.tile_map), _ptr(al.num_tiles), T, H, I, E, k,
-        ctypes.byref(qc), _ptr(out), _ptr(ws), ws.numel(), _stream(stream)))
+        ctypes.byref(qc), ACTIVATIONS[activation], _ptr(out), _ptr(ws), ws.numel(), _stream(stream)))
     return out
 
 

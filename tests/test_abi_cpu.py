@@ -125,3 +125,17 @@ def test_finalize_rejects_bad_arguments(moelib):
     assert call(w=None) == moe.MOE_ERR_INVALID_ARG
     assert call(eps=-1.0) == moe.MOE_ERR_INVALID_ARG
     assert call(T=0) == moe.MOE_OK
+
+
+def test_experts_act_rejects_unknown_activation(moelib):
+    L = moelib
+    qb = ctypes.byref(moe.QC_BF16)
+
+    def call(act, T=16):
+        return L.moe_experts_act(FAKE, None, FAKE, None, FAKE, None, FAKE, FAKE, FAKE, FAKE, T, 256, 512, 8, 2, qb,
+                                 act, FAKE, FAKE, 1 << 30, None)
+
+    assert call(-1) == moe.MOE_ERR_UNSUPPORTED
+    assert call(6) == moe.MOE_ERR_UNSUPPORTED
+    assert call(moe.ACTIVATIONS["gelu"], T=0) == moe.MOE_OK   # nothing to do, no launch
+    assert sorted(moe.ACTIVATIONS.values()) == list(range(6))

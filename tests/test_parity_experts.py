@@ -14,27 +14,34 @@ import torch
 from mixture_experts_layer_tokens_gb300 import moe
 from mixture_experts_layer_tokens_gb300.inputs import CONFIGS, make_inputs, scaled
 from oracle import moe_ref
-from parity_util import check_bf16, check_fp8
+from parity_util import check_bf16, check_fp8, half_ulp_bf16, to64
 
 pytestmark = pytest.mark.gpu
 
 
-def _run(inp, ids, dev, quant, identity=False):
+def _run(inp, ids, dev, quant, identity=False, act="silu", w13=None, w13_scale=None):
     cfg = inp.cfg
     E, k = cfg.E, ids.shape[1]
-    w = torch.full(ids.shape, 1.0 / k)
+    w13 = inp.w13 if w13 is None else w13
+    w13_scale = inp.w13_scale if w13_scale is None else w13_scale
     al = moe.moe_align(ids.to(dev), E)
     a1q, sc = moe.moe_prepare(inp.a1.to(dev), None, k, False, quant)
     d = lambda t: None if t is None else t.to(dev)
-    y = moe.moe_experts(a1q, sc, d(inp.w13), d(inp.w13_scale), d(inp.w2), d(inp.w2_scale), al, quant,
-                        identity=identity)
+    y = moe.moe_experts(a1q, sc, d(w13), d(w13_scale), d(inp.w2), d(inp.w2_scale), al, quant,
+                        identity=identity, activation=act)
     torch.cuda.synchronize()
     assert moe.moe_device_status() == moe.MOE_OK
     ral = moe_ref.align(ids, E, 128)
     rq, rs = moe_ref.prepare(inp.a1, None, False, quant)
     assert torch.equal(a1q.cpu(), rq)
-    yref = moe_ref.experts(rq, rs, inp.w13, inp.w13_scale, inp.w2, inp.w2_scale, ral, k, quant)
+    yref = moe_ref.experts(rq, rs, w13, w13_scale, inp.w2, inp.w2_scale, ral, k, quant, act)
     return y, yref
+
+
+def _stored_pair_slack(yref):
+    """Both sides store y (and h) as bf16, so the oracle's stored value and the GPU's
+    can be neighbouring bf16 numbers: one ulp in all, half from each rounding."""
+    return half_ulp_bf16(to64(yref))
 
 
 def _ids(T, k, E, seed, skew=False):
@@ -63,7 +70,7 @@ def _ids(T, k, E, seed, skew=False):
 def test_experts_bf16(cuda_dev, T, H, I, E, k, skew):
     inp = make_inputs(scaled(CONFIGS["tiny"], T=T, H=H, I=I, E=E, top_k=k))
     y, yref = _run(inp, _ids(T, k, E, T + H, skew), cuda_dev, "bf16")
-    check_bf16(y, yref, "experts bf16")
+    check_bf16(y, yref, "experts bf16", slack=_stored_pair_slack(yref))
 
 
 @pytest.mark.parametrize("T,H,I,E,k,skew", [
@@ -84,7 +91,7 @@ def test_experts_identity_permutation(cuda_dev):
     inp = make_inputs(scaled(CONFIGS["tiny"], T=200, H=512, I=256, E=1, top_k=1))
     ids = torch.zeros((200, 1), dtype=torch.int32)
     y, yref = _run(inp, ids, cuda_dev, "bf16", identity=True)
-    check_bf16(y, yref, "identity")
+    check_bf16(y, yref, "identity", slack=_stored_pair_slack(yref))
 
 
 def test_experts_twice_same_bits(cuda_dev):
@@ -93,3 +100,55 @@ def test_experts_twice_same_bits(cuda_dev):
     y1, _ = _run(inp, ids, cuda_dev, "bf16")
     y2, _ = _run(inp, ids, cuda_dev, "bf16")
     assert torch.equal(y1, y2)
+
+
+@pytest.mark.parametrize("T,H,I,E,k,quant,act", [
+    (300, 512, 384, 4, 2, "bf16", "gelu"),
+    (300, 512, 384, 4, 2, "bf16", "gelu_tanh"),
+    (300, 512, 384, 4, 2, "bf16", "swigluoai"),
+    (300, 512, 384, 4, 2, "bf16", "silu_no_mul"),   # 384 gate rows: N tiles of 256 and 128
+    (300, 512, 384, 4, 2, "bf16", "gelu_no_mul"),
+    (4, 2048, 2048, 16, 1, "bf16", "swigluoai"),     # stream-K in both GEMMs
+    (4, 2048, 2048, 16, 1, "bf16", "gelu_no_mul"),   # stream-K, gate-only units
+    (256, 256, 2048, 64, 4, "bf16", "silu_no_mul"),  # round-robin schedule
+    (300, 512, 384, 4, 2, "fp8", "gelu"),
+    (300, 512, 384, 4, 2, "fp8", "swigluoai"),
+    (300, 512, 384, 4, 2, "fp8", "silu_no_mul"),    # three G(128) groups of h, the last alone in its tile
+    (100, 1024, 512, 16, 4, "fp8", "gelu_no_mul"),
+])
+def test_experts_activations(cuda_dev, T, H, I, E, k, quant, act):
+    base = CONFIGS["deepseek"] if quant == "fp8" else CONFIGS["tiny"]
+    inp = make_inputs(scaled(base, T=T, H=H, I=I, E=E, top_k=k, shared_I=0))
+    w13, w13_scale = inp.w13, inp.w13_scale
+    if act == "swigluoai" and quant == "bf16":
+        # gate and up values of a few units, so that both clamps at +-7 are reached
+        w13 = (w13.float() * 4).to(torch.bfloat16)
+    if act.endswith("_no_mul"):
+        w13 = w13[:, :I].contiguous()
+        w13_scale = None if w13_scale is None else w13_scale[:, :I // 128].contiguous()
+    y, yref = _run(inp, _ids(T, k, E, T + I + 7), cuda_dev, quant, act=act, w13=w13, w13_scale=w13_scale)
+    if quant == "fp8":
+        check_fp8(y, yref, f"experts fp8 {act}")
+    else:
+        check_bf16(y, yref, f"experts bf16 {act}", slack=_stored_pair_slack(yref))
+
+
+def test_experts_act_silu_is_moe_experts(cuda_dev):
+    # moe_experts is moe_experts_act with MOE_ACT_SILU: the same bits
+    inp = make_inputs(scaled(CONFIGS["tiny"], T=64, H=256, I=256, E=4, top_k=2))
+    ids = _ids(64, 2, 4, 99).to(cuda_dev)
+    al = moe.moe_align(ids, 4)
+    a1q, sc = moe.moe_prepare(inp.a1.to(cuda_dev), None, 2, False, "bf16")
+    w13, w2 = inp.w13.to(cuda_dev), inp.w2.to(cuda_dev)
+    y_act = moe.moe_experts(a1q, None, w13, None, w2, None, al, "bf16", activation="silu")
+    out = torch.empty_like(y_act)
+    ws = torch.empty(moe.workspace_size(64, 256, 256, 4, 2, "bf16"), dtype=torch.uint8, device=cuda_dev)
+    import ctypes
+    st = moe.lib().moe_experts(a1q.data_ptr(), None, w13.data_ptr(), None, w2.data_ptr(), None,
+                               al.expert_offsets.data_ptr(), al.sorted_slot.data_ptr(), al.tile_map.data_ptr(),
+                               al.num_tiles.data_ptr(), 64, 256, 256, 4, 2, ctypes.byref(moe.QC_BF16),
+                               out.data_ptr(), ws.data_ptr(), ws.numel(), None)
+    torch.cuda.synchronize()
+    assert st == moe.MOE_OK
+    assert torch.equal(out, y_act)
+
