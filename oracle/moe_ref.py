@@ -175,6 +175,40 @@ def dequant_fp8_g128(q: np.ndarray, s: np.ndarray, group: int = 128) -> np.ndarr
     return (codecs.e4m3_decode(q).reshape(R, C // group, group) * s.astype(np.float64)[:, :, None]).reshape(R, C)
 
 
+# The "A" (per activation token) and "T" (per tensor) quantisation formats of the
+# "Fused MoE Kernel Features" tables (table key: "A - Per activation token",
+# "T - Per tensor"), read with the G(128) rule above: one scale per row over all
+# its columns, or one scale over the whole tensor.
+def quantize_fp8_token(x64: np.ndarray):
+    """"A" format: s_r = fp32(max(amax_r, fp32(1e-10)) / 448) over row r,
+    q = e4m3_rn_satfinite(fp32(x / s_r)).  Returns (codes [R, C], scales fp32 [R])."""
+    amax = np.abs(x64).max(axis=1) if x64.shape[1] else np.zeros(x64.shape[0])
+    s = codecs.round_fp32(np.maximum(amax, AMAX_FLOOR) / 448.0)
+    q = codecs.e4m3_encode(codecs.round_fp32(x64 / s[:, None]))
+    return q, s.astype(np.float32)
+
+
+def quantize_fp8_tensor(x64: np.ndarray):
+    """"T" format: one s = fp32(max(amax, fp32(1e-10)) / 448) over all elements.
+    Returns (codes [R, C], scale fp32 [1])."""
+    amax = float(np.abs(x64).max()) if x64.size else 0.0
+    s = codecs.round_fp32(max(amax, AMAX_FLOOR) / 448.0)
+    q = codecs.e4m3_encode(codecs.round_fp32(x64 / s))
+    return q, np.array([s], dtype=np.float32)
+
+
+def dequant_fp8(q: np.ndarray, s: np.ndarray, quant: str) -> np.ndarray:
+    """codes x scale for the three fp8 formats (rows of q, with their scales)."""
+    if quant == "fp8":
+        return dequant_fp8_g128(q, s)
+    v = codecs.e4m3_decode(q)
+    if quant == "fp8_token":
+        return v * s.astype(np.float64)[:, None]
+    if quant == "fp8_tensor":
+        return v * float(s[0])
+    raise ValueError(quant)
+
+
 def prepare(a1: torch.Tensor, topk_weights: torch.Tensor, apply_router_weight_on_input: bool, quant: str):
     """Prepare step of the no-DP/EP prepare/finalize ("[vLLM] MoE Oracle &
     Prepare/Finalize" blog, "No DP/EP" section).
@@ -183,8 +217,9 @@ def prepare(a1: torch.Tensor, topk_weights: torch.Tensor, apply_router_weight_on
     input is first multiplied by the top-k weight cast to the activation type:
     a1 = bf16(a1 * bf16(w)).  Then the input is quantised: ``quant == 'bf16'``
     is "no quantisation type", a passthrough; ``quant == 'fp8'`` is the
-    per-token G(128) E4M3 format.  Returns (a1q, a1q_scale or None) with a1q a
-    bf16 tensor or a uint8 tensor of E4M3 codes.
+    per-token G(128) E4M3 format; ``'fp8_token'`` and ``'fp8_tensor'`` the "A"
+    and "T" formats.  Returns (a1q, a1q_scale or None) with a1q a bf16 tensor or
+    a uint8 tensor of E4M3 codes.
     """
     x = _np(a1)
     if apply_router_weight_on_input:
@@ -196,6 +231,12 @@ def prepare(a1: torch.Tensor, topk_weights: torch.Tensor, apply_router_weight_on
         return to_bf16_tensor(x), None
     if quant == "fp8":
         q, s = quantize_fp8_g128(x)
+        return torch.from_numpy(q), torch.from_numpy(s)
+    if quant == "fp8_token":
+        q, s = quantize_fp8_token(x)
+        return torch.from_numpy(q), torch.from_numpy(s)
+    if quant == "fp8_tensor":
+        q, s = quantize_fp8_tensor(x)
         return torch.from_numpy(q), torch.from_numpy(s)
     raise ValueError(quant)
 
@@ -276,9 +317,20 @@ def expert_rows(A64: torch.Tensor, W13: torch.Tensor, W2: torch.Tensor, quant: s
     hn = h.numpy()
     if quant == "bf16":
         h_st = codecs.round_bf16(hn)
-    else:
+    elif quant == "fp8":
         q, s = quantize_fp8_g128(codecs.round_fp32(hn))
         h_st = dequant_fp8_g128(q, s)
+    elif quant == "fp8_token":
+        # reading: with the "A" format the intermediate is stored in the activation
+        # type (bf16) and quantised per row like the input
+        q, s = quantize_fp8_token(codecs.round_bf16(hn))
+        h_st = dequant_fp8(q, s, quant)
+    else:
+        raise ValueError(f"{quant}: the per-tensor intermediate needs all experts (see experts())")
+    return _expert_out(h_st, W2)
+
+
+def _expert_out(h_st: np.ndarray, W2: torch.Tensor) -> torch.Tensor:
     y = torch.from_numpy(h_st) @ W2.T
     return torch.from_numpy(codecs.round_bf16(y.numpy()))
 
@@ -292,7 +344,9 @@ def _weights64(w, w_scale, e, quant):
 def _act64(a1q, a1q_scale, rows, quant):
     if quant == "bf16":
         return torch.from_numpy(_np(a1q)[rows])
-    return torch.from_numpy(dequant_fp8_g128(_np(a1q)[rows].astype(np.uint8), _np(a1q_scale)[rows]))
+    sc = _np(a1q_scale)
+    return torch.from_numpy(dequant_fp8(_np(a1q)[rows].astype(np.uint8), sc if quant == "fp8_tensor" else sc[rows],
+                                        quant))
 
 
 def experts(a1q, a1q_scale, w13, w13_scale, w2, w2_scale, al: Alignment, top_k: int, quant: str,
@@ -307,6 +361,31 @@ def experts(a1q, a1q_scale, w13, w13_scale, w2, w2_scale, al: Alignment, top_k: 
     S = int(offs[-1])
     H = a1q.shape[1]
     y = torch.zeros((S, H), dtype=F64)
+    if quant == "fp8_tensor":
+        # reading: the "T" intermediate is h of every expert stored in bf16, then one
+        # scale over all of it
+        hs, used = [], []
+        for e in range(len(offs) - 1):
+            p0, p1 = int(offs[e]), int(offs[e + 1])
+            if p0 == p1:
+                continue
+            slots = order[p0:p1]
+            A = _act64(a1q, a1q_scale, slots // top_k, quant)
+            W13 = _weights64(w13, w13_scale, e, quant)
+            h = silu_and_mul(A @ W13.T) if act == "silu" else activation(A @ W13.T, act)
+            hs.append(codecs.round_bf16(h.numpy()))
+            used.append((e, slots))
+        if not hs:
+            return y
+        q, s = quantize_fp8_tensor(np.concatenate(hs, 0))
+        h_all = dequant_fp8(q, s, quant)
+        r = 0
+        for (e, slots), h in zip(used, hs):
+            n = h.shape[0]
+            y[torch.from_numpy(slots.astype(np.int64))] = _expert_out(
+                h_all[r:r + n], _weights64(w2, w2_scale, e, quant))
+            r += n
+        return y
     for e in range(len(offs) - 1):
         p0, p1 = int(offs[e]), int(offs[e + 1])
         if p0 == p1:
