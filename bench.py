@@ -68,15 +68,18 @@ def experts_algorithmic(cfg, counts):
     that received tokens (+ fp8 block scales), the activations read once, the
     intermediate h written and read once, the output rows written once; FLOPs
     6 H I per token slot (no padded rows)."""
-    esz = 1 if cfg.quant == "fp8" else 2
+    fp8 = cfg.quant != "bf16"
+    esz = 1 if fp8 else 2
     touched = int((counts > 0).sum())
     w = touched * 3 * cfg.H * cfg.I * esz
-    if cfg.quant == "fp8":
+    if fp8:
         w += touched * 3 * (cfg.H // 128) * (cfg.I // 128) * 4
     S = cfg.T * cfg.top_k
     act = cfg.T * cfg.H * esz + 2 * S * cfg.I * esz + S * cfg.H * 2
     if cfg.quant == "fp8":
         act += cfg.T * (cfg.H // 128) * 4 + 2 * S * (cfg.I // 128) * 4
+    elif fp8:  # per-token / per-tensor: per-row scales, and h also stored in bf16 and read back
+        act += cfg.T * 4 + 2 * S * 4 + 2 * S * cfg.I * 2
     flops = 6.0 * S * cfg.H * cfg.I
     return w + act, flops
 
@@ -356,7 +359,7 @@ def run_gpu(args, ws, rank, local):
         torch.cuda.synchronize(dev)
         dom_ms = a.elapsed_time(b) / (reps * R)
         # the binding roof: HBM bytes or tensor FLOPs (fp8 peak = measured bf16 x the nominal 2x)
-        tensor_peak = bf16_peak * (2.0 if cfg.quant == "fp8" else 1.0)
+        tensor_peak = bf16_peak * (2.0 if cfg.quant != "bf16" else 1.0)
         t_hbm = nbytes / (hbm_peak * 1e9)
         t_tensor = flops / (tensor_peak * 1e12) if flops else 0.0
         if t_tensor > t_hbm:
@@ -364,7 +367,7 @@ def run_gpu(args, ws, rank, local):
             roofline = {"bound": "tensor", "achieved": round(achieved, 1), "peak": round(tensor_peak, 1),
                         "unit": "TFLOP/s", "frac": round(achieved / tensor_peak, 4), "traffic": None,
                         "kernel": dom_name, "algorithmic_flops": flops, "ms": round(dom_ms, 4),
-                        "peak_kind": peak_kind + (" bf16 x2 (nominal fp8:bf16)" if cfg.quant == "fp8" else "")}
+                        "peak_kind": peak_kind + (" bf16 x2 (nominal fp8:bf16)" if cfg.quant != "bf16" else "")}
             roofline["hbm_gbs"] = round(nbytes / (dom_ms * 1e-3) / 1e9, 1)
         else:
             achieved = nbytes / (dom_ms * 1e-3) / 1e9
@@ -432,7 +435,7 @@ def run_gpu(args, ws, rank, local):
                          f"({dt:.1f} s), CPU {cpu_model()}"}
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "fp8" if cfg.quant == "fp8" else "bf16", "data": "synthetic",
+            "vs_baseline": None, "dtype": "fp8" if cfg.quant != "bf16" else "bf16", "data": "synthetic",
             "config": {"workload": cfg.description, "T": cfg.T, "H": cfg.H, "I": cfg.I, "E": cfg.E,
                        "top_k": cfg.top_k, "parallelism": f"replicas{ws}",
                        "launch": "cuda_graph" if not args.no_graph else "eager",

@@ -83,11 +83,23 @@ typedef enum {
   MOE_ACT_GELU_NO_MUL = 5
 } moe_activation_t;
 
+/* act_group values for the quantisation formats of the "Fused MoE Kernel
+ * Features" tables besides G(128): "A" (per activation token) and "T" (per
+ * tensor). */
+#define MOE_GROUP_TOKEN (-1)  /* one scale per token over all H channels   */
+#define MOE_GROUP_TENSOR (-2) /* one scale over the whole activation tensor */
+
 /* Quantisation of the expert inputs and weights.
  *   bf16:  {MOE_DT_BF16, 0, MOE_DT_BF16, 0, 0}   -- "no quantisation type"
  *   fp8:   {MOE_DT_FP8_E4M3, 128, MOE_DT_FP8_E4M3, 128, 128}
- *          activations: one fp32 scale per token per 128 channels ("G(128)");
- *          weights: one fp32 scale per 128x128 block.
+ *          activations: one fp32 scale per token per 128 channels ("G(128)"),
+ *          a1q_scale [T, H/128]; weights: one fp32 scale per 128x128 block.
+ *   fp8 with act_group MOE_GROUP_TOKEN: a1q_scale [T] ("A");
+ *            act_group MOE_GROUP_TENSOR: a1q_scale [1] ("T").
+ *          Every scale is s = fp32(max(amax, 1e-10) / 448) over its group and
+ *          q = e4m3_rn_satfinite(fp32(x / s)).  In moe_experts the
+ *          intermediate h is quantised in the same format: G(128) from fp32 h;
+ *          A and T from h stored in bf16 (T: one scale over every expert's rows).
  * Other combinations return MOE_ERR_UNSUPPORTED. */
 typedef struct {
   moe_dtype_t act;
@@ -172,7 +184,11 @@ moe_status_t moe_align_noalloc(const int32_t *topk_ids, int T, int top_k, int E,
  *                    applied nothing is launched -- the passthrough);
  *   MOE_DT_FP8_E4M3: a1q [T, H] E4M3 codes (uint8), a1q_scale [T, H/128] fp32:
  *                    s = fp32(max(amax, 1e-10f) / 448) per 128 channels,
- *                    q = e4m3_rn_satfinite(x / s) (IEEE fp32 division).
+ *                    q = e4m3_rn_satfinite(x / s) (IEEE fp32 division);
+ *                    act_group MOE_GROUP_TOKEN: a1q_scale [T], one s per token;
+ *                    MOE_GROUP_TENSOR: a1q_scale [1], one s for the tensor
+ *                    (a1q_scale is also the reduction's scratch until the call's
+ *                    last launch writes the scale).
  * a1 [T, H] bf16.  topk_weights [T, top_k] fp32 (read only with the weight
  * flag).  topk_ids is accepted for parity with the pages' signature and unused
  * (may be NULL).  H % 128 == 0 for fp8, H % 8 == 0 for bf16. */
@@ -191,7 +207,8 @@ moe_status_t moe_prepare(const void *a1, const float *topk_weights, const int32_
  *   h       = silu(g) * u                 (bf16, or E4M3 G(128) with fp8)
  *   fused_expert_output[f] = h . w2[e]^T  (w2 [E, H, I]; bf16 [T*top_k, H],
  *                                          token-major, unweighted)
- * Accumulation is fp32.  fp8: a1q E4M3 + a1q_scale [T, H/128]; w13/w2 E4M3
+ * Accumulation is fp32.  fp8: a1q E4M3 + a1q_scale in the qc->act_group
+ * format (G(128) [T, H/128], A [T], T [1]); w13/w2 E4M3
  * with w13_scale [E, 2I/128, H/128] and w2_scale [E, H/128, I/128] fp32; each
  * 128-deep K block is scaled by a1q_scale * w_scale before it is added.
  * expert_offsets / sorted_slot / tile_map / num_tiles come from moe_align with

@@ -287,4 +287,54 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&b);
 }
 
+
+// ---- vector helpers of the quantisers
+// 8 bf16 values (one 16-byte read-only load) as fp32
+__device__ __forceinline__ void load_bf16x8(const void* p, float (&x)[8]) {
+  const uint4 v = __ldg(reinterpret_cast<const uint4*>(p));
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    x[2 * i] = bf16lo(w[i]);
+    x[2 * i + 1] = bf16hi(w[i]);
+  }
+}
+
+__device__ __forceinline__ float amax8(const float (&x)[8]) {
+  float a = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) a = fmaxf(a, fabsf(x[i]));
+  return a;
+}
+
+// 8 values -> 8 E4M3 codes with scale s: q = e4m3_rn_satfinite(fp32(x / s)), IEEE division
+__device__ __forceinline__ uint2 e4m3x8(const float (&x)[8], float s) {
+  uint32_t packed[2];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 r = make_float2(__fdiv_rn(x[2 * i], s), __fdiv_rn(x[2 * i + 1], s));
+    const uint32_t two = (uint32_t)__nv_cvt_float2_to_fp8x2(r, __NV_SATFINITE, __NV_E4M3);
+    if (i & 1)
+      packed[i >> 1] |= two << 16;
+    else
+      packed[i >> 1] = two;
+  }
+  return make_uint2(packed[0], packed[1]);
+}
+
+// Block-wide max of non-negative values over kThreads threads; every thread gets it.
+template <int kThreads>
+__device__ __forceinline__ float block_amax(float a) {
+  __shared__ float red[kThreads / 32];
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, off));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = a;
+  __syncthreads();
+  a = 0.f;
+#pragma unroll
+  for (int w = 0; w < kThreads / 32; ++w) a = fmaxf(a, red[w]);
+  __syncthreads();
+  return a;
+}
+
 }  // namespace moe

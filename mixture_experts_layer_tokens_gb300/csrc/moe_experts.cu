@@ -113,7 +113,8 @@ struct GemmParams {
   int H;                       // gemm2: output columns
   int b_rows;                  // rows of one expert's weight matrix (2I or H)
   int s_pad;                   // row stride of the transposed scale arrays
-  const float* a_scale_t;      // fp8: [K/128][s_pad] scales of the A rows
+  int a_kstride;               // fp8: stride of a_scale_t between K blocks (0: one scale per row)
+  const float* a_scale_t;      // fp8: [K/128][a_kstride] scales of the A rows
   const float* w_scale;        // fp8: [E][b_rows/128][K/128]
   void* out;                   // gemm1: h [rows][I]; gemm2: y [T*k][H] bf16
   float* out_scale_t;          // gemm1 fp8: [I/128][s_pad]
@@ -260,7 +261,7 @@ __device__ __forceinline__ void fma2(float& a0, float& a1, float v0, float v1, f
       : "f"(v0), "f"(v1), "f"(s));
 }
 
-template <bool kFP8, int kKind, int kMG, int kAct>
+template <bool kFP8, int kKind, int kMG, int kAct, bool kHB16>
 __global__ void __launch_bounds__(Warps<kFP8>::THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
                 const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
@@ -381,7 +382,7 @@ __global__ void __launch_bounds__(Warps<kFP8>::THREADS, 1)
           const int slot = (int)(fills % C::SCALE_SLOTS);
           if (!(ok = warp_wait(&sempty[slot], (uint32_t)(((fills / C::SCALE_SLOTS) & 1) ^ 1)))) break;
           float* dst = scale_ring + slot * C::SCALE_SLOT_FLOATS;
-          const float* asrc = p.a_scale_t + (size_t)kb * p.s_pad + it.row0;
+          const float* asrc = p.a_scale_t + (size_t)kb * p.a_kstride + it.row0;
 #pragma unroll
           for (int j = 0; j < 4; ++j) cp_async_4(dst + lane * 4 + j, asrc + lane * 4 + j);
           if (lane == 0) {
@@ -774,7 +775,27 @@ __global__ void __launch_bounds__(Warps<kFP8>::THREADS, 1)
             }
           }
         }
-        if (kNoMul) {
+        if (kHB16) {
+          // the "A"/"T" formats: h goes out in bf16 ([rows][I]); a later pass quantises it
+          const int hc0 = kNoMul ? (2 * it.n + half) * 128 : it.n * 128 + 64 * half;
+          const int nh = kNoMul ? 128 : 64;
+#pragma unroll
+          for (int i = 0; i < 128; ++i)
+            if (i < nh) accv[i] = kNoMul ? act_gate<kAct>(accv[i]) : act_mul<kAct>(accv[i], accv[64 + i]);
+          if (valid && hc0 < p.I) {
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + (size_t)prow * p.I + hc0);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              if (8 * j >= nh) break;
+              uint4 o;
+              o.x = pack_bf16x2(accv[8 * j + 0], accv[8 * j + 1]);
+              o.y = pack_bf16x2(accv[8 * j + 2], accv[8 * j + 3]);
+              o.z = pack_bf16x2(accv[8 * j + 4], accv[8 * j + 5]);
+              o.w = pack_bf16x2(accv[8 * j + 6], accv[8 * j + 7]);
+              dst[j] = o;
+            }
+          }
+        } else if (kNoMul) {
           // h = act(g) for this thread's 128 columns, which are one G(128) group (2n + half)
           const int grp = 2 * it.n + half;
           float amax = 0.f;
@@ -942,7 +963,7 @@ __global__ void __launch_bounds__(1024)
 __global__ void __launch_bounds__(256)
     gather_kernel(const uint8_t* __restrict__ a1q, const float* __restrict__ a1q_scale,
                   const int32_t* __restrict__ sorted_slot, int S, int top_k, int row_bytes, int ngroups,
-                  uint8_t* __restrict__ A, float* __restrict__ a_scale_t, int s_pad) {
+                  uint8_t* __restrict__ A, float* __restrict__ a_scale_t, int s_pad, int scale_stride) {
   const int p = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (p >= S) return;
@@ -954,7 +975,61 @@ __global__ void __launch_bounds__(256)
     for (int i = lane; i < nv; i += 32) dst[i] = __ldg(src + i);
   }
   if (a_scale_t)
-    for (int g = lane; g < ngroups; g += 32) a_scale_t[(size_t)g * s_pad + p] = __ldg(a1q_scale + (size_t)t * ngroups + g);
+    for (int g = lane; g < ngroups; g += 32)
+      a_scale_t[(size_t)g * s_pad + p] = __ldg(a1q_scale + (size_t)t * scale_stride + g);
+}
+
+// The "A" and "T" formats' intermediate: h rows [rows][I] in bf16 (rows =
+// expert_offsets[E]) -> E4M3 codes hq and one scale per row hs (for "T" the
+// tensor's scale repeated on every row, the layout gemm2 reads).
+__global__ void __launch_bounds__(256)
+    hquant_token_kernel(const __nv_bfloat16* __restrict__ hb, int I, const int32_t* __restrict__ offsets, int E,
+                        uint8_t* __restrict__ hq, float* __restrict__ hs) {
+  const int p = blockIdx.x;
+  if (p >= __ldg(offsets + E)) return;  // block-uniform: the whole block leaves
+  const int nv = I / 8;
+  const __nv_bfloat16* row = hb + (size_t)p * I;
+  float a = 0.f;
+  for (int v = threadIdx.x; v < nv; v += 256) {
+    float x[8];
+    load_bf16x8(row + (size_t)v * 8, x);
+    a = fmaxf(a, amax8(x));
+  }
+  const float sc = __fdiv_rn(fmaxf(block_amax<256>(a), 1e-10f), 448.0f);
+  uint2* out = reinterpret_cast<uint2*>(hq + (size_t)p * I);
+  for (int v = threadIdx.x; v < nv; v += 256) {
+    float x[8];
+    load_bf16x8(row + (size_t)v * 8, x);
+    out[v] = e4m3x8(x, sc);
+  }
+  if (threadIdx.x == 0) hs[p] = sc;
+}
+
+__global__ void __launch_bounds__(256)
+    hquant_tensor_amax_kernel(const __nv_bfloat16* __restrict__ hb, int I, const int32_t* __restrict__ offsets,
+                              int E, unsigned* __restrict__ amax_bits) {
+  const long long nvec = (long long)__ldg(offsets + E) * (I / 8);
+  float a = 0.f;
+  for (long long v = (long long)blockIdx.x * 256 + threadIdx.x; v < nvec; v += (long long)gridDim.x * 256) {
+    float x[8];
+    load_bf16x8(hb + v * 8, x);
+    a = fmaxf(a, amax8(x));
+  }
+  a = block_amax<256>(a);
+  if (threadIdx.x == 0) atomicMax(amax_bits, __float_as_uint(a));
+}
+
+__global__ void __launch_bounds__(256)
+    hquant_tensor_kernel(const __nv_bfloat16* __restrict__ hb, int I, const int32_t* __restrict__ offsets, int E,
+                         const unsigned* __restrict__ amax_bits, uint8_t* __restrict__ hq, float* __restrict__ hs) {
+  const long long v = (long long)blockIdx.x * 256 + threadIdx.x;
+  const int vpr = I / 8;
+  if (v >= (long long)__ldg(offsets + E) * vpr) return;
+  const float sc = __fdiv_rn(fmaxf(__uint_as_float(*amax_bits), 1e-10f), 448.0f);
+  float x[8];
+  load_bf16x8(hb + v * 8, x);
+  reinterpret_cast<uint2*>(hq)[v] = e4m3x8(x, sc);
+  if (v % vpr == 0) hs[v / vpr] = sc;
 }
 
 // ------------------------------------------------------------------ host side
@@ -1001,45 +1076,47 @@ bool make_map_gate_up(CUtensorMap* m, const void* base, bool fp8, long long k, l
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <bool kFP8, int kKind, int kMG, int kAct>
+template <bool kFP8, int kKind, int kMG, int kAct, bool kHB16 = false>
 cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& a2, const CUtensorMap& b, const GemmParams& p, int grid,
                         cudaStream_t s) {
   static int configured[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_kernel<kFP8, kKind, kMG, kAct>,
+    cudaError_t e = cudaFuncSetAttribute(gemm_kernel<kFP8, kKind, kMG, kAct, kHB16>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<kFP8, kMG>::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     configured[dev] = 1;
   }
-  gemm_kernel<kFP8, kKind, kMG, kAct><<<grid, Warps<kFP8>::THREADS, Cfg<kFP8, kMG>::SMEM_BYTES, s>>>(a, a2, b, p);
+  gemm_kernel<kFP8, kKind, kMG, kAct, kHB16><<<grid, Warps<kFP8>::THREADS, Cfg<kFP8, kMG>::SMEM_BYTES, s>>>(a, a2, b, p);
   return cudaGetLastError();
 }
 
-// gemm1 with the activation chosen at run time
-template <bool kFP8, int kMG>
+// gemm1 with the activation chosen at run time (kHB16: fp8 mainloop, bf16 h out)
+template <bool kFP8, int kMG, bool kHB16 = false>
 cudaError_t launch_gemm1(int act, const CUtensorMap& a, const CUtensorMap& a2, const CUtensorMap& b,
                          const GemmParams& p, int grid, cudaStream_t s) {
   switch (act) {
-    case MOE_ACT_SILU: return launch_gemm<kFP8, kGemm1, kMG, MOE_ACT_SILU>(a, a2, b, p, grid, s);
-    case MOE_ACT_GELU: return launch_gemm<kFP8, kGemm1, kMG, MOE_ACT_GELU>(a, a2, b, p, grid, s);
-    case MOE_ACT_GELU_TANH: return launch_gemm<kFP8, kGemm1, kMG, MOE_ACT_GELU_TANH>(a, a2, b, p, grid, s);
-    case MOE_ACT_SWIGLUOAI: return launch_gemm<kFP8, kGemm1, kMG, MOE_ACT_SWIGLUOAI>(a, a2, b, p, grid, s);
-    case MOE_ACT_SILU_NO_MUL: return launch_gemm<kFP8, kGemm1, kMG, MOE_ACT_SILU_NO_MUL>(a, a2, b, p, grid, s);
-    case MOE_ACT_GELU_NO_MUL: return launch_gemm<kFP8, kGemm1, kMG, MOE_ACT_GELU_NO_MUL>(a, a2, b, p, grid, s);
+    case MOE_ACT_SILU: return launch_gemm<kFP8, kGemm1, kMG, MOE_ACT_SILU, kHB16>(a, a2, b, p, grid, s);
+    case MOE_ACT_GELU: return launch_gemm<kFP8, kGemm1, kMG, MOE_ACT_GELU, kHB16>(a, a2, b, p, grid, s);
+    case MOE_ACT_GELU_TANH: return launch_gemm<kFP8, kGemm1, kMG, MOE_ACT_GELU_TANH, kHB16>(a, a2, b, p, grid, s);
+    case MOE_ACT_SWIGLUOAI: return launch_gemm<kFP8, kGemm1, kMG, MOE_ACT_SWIGLUOAI, kHB16>(a, a2, b, p, grid, s);
+    case MOE_ACT_SILU_NO_MUL: return launch_gemm<kFP8, kGemm1, kMG, MOE_ACT_SILU_NO_MUL, kHB16>(a, a2, b, p, grid, s);
+    case MOE_ACT_GELU_NO_MUL: return launch_gemm<kFP8, kGemm1, kMG, MOE_ACT_GELU_NO_MUL, kHB16>(a, a2, b, p, grid, s);
   }
   return cudaErrorInvalidValue;
 }
 
 struct WsLayout {
-  size_t A, As, h, hs, gmap, ngroups, gmap2, ngroups2, flags1, flags2, partials, total;
+  size_t A, As, h, hs, hb, hamax, gmap, ngroups, gmap2, ngroups2, flags1, flags2, partials, total;
   int s_pad, cap_groups, nflags1, nflags2;
 };
 
 inline size_t al256(size_t x) { return (x + 255) & ~size_t(255); }
 
-WsLayout ws_layout(long long S, int H, int I, int E, bool fp8, int grid) {
+// group: the fp8 activation format (128, MOE_GROUP_TOKEN or MOE_GROUP_TENSOR); the
+// "A"/"T" formats add the bf16 intermediate and the tensor format's amax word.
+WsLayout ws_layout(long long S, int H, int I, int E, bool fp8, int grid, int group) {
   WsLayout L;
   const int esz = fp8 ? 1 : 2;
   const int MG = fp8 ? 1 : 2;  // the larger bound of either GEMM
@@ -1057,6 +1134,11 @@ WsLayout ws_layout(long long S, int H, int I, int E, bool fp8, int grid) {
   off = al256(off + (size_t)S * I * esz);
   L.hs = off;
   off = al256(off + (fp8 ? (size_t)(I / 128) * L.s_pad * 4 : 0));
+  const bool hb16 = fp8 && group != 128;
+  L.hb = off;
+  off = al256(off + (hb16 ? (size_t)S * I * 2 : 0));
+  L.hamax = off;
+  off = al256(off + (hb16 ? 4 : 0));
   L.gmap = off;
   off = al256(off + (size_t)L.cap_groups * 2 * 4);
   L.ngroups = off;
@@ -1088,7 +1170,7 @@ using namespace moe;
 
 extern "C" size_t moe_workspace_size(int T, int H, int I, int E, int top_k, const moe_quant_config* qc) {
   if (!qc || T < 0 || H <= 0 || I <= 0 || E < 1 || top_k < 1) return 0;
-  return ws_layout((long long)T * top_k, H, I, E, qc->act == MOE_DT_FP8_E4M3, gemm_grid()).total;
+  return ws_layout((long long)T * top_k, H, I, E, qc->act == MOE_DT_FP8_E4M3, gemm_grid(), qc->act_group).total;
 }
 
 extern "C" moe_status_t moe_experts_act(const void* a1q, const float* a1q_scale, const void* w13,
@@ -1102,8 +1184,10 @@ extern "C" moe_status_t moe_experts_act(const void* a1q, const float* a1q_scale,
   const bool no_mul = activation == MOE_ACT_SILU_NO_MUL || activation == MOE_ACT_GELU_NO_MUL;
   const int nt1 = no_mul ? (I + 255) / 256 : I / 128;  // gemm1 N tiles: 256 gate rows, or 128 gate + 128 up
   const bool fp8 = qc->act == MOE_DT_FP8_E4M3;
+  const int group = qc->act_group;
   if (fp8) {
-    if (qc->act_group != 128 || qc->weight != MOE_DT_FP8_E4M3 || qc->w_block_n != 128 || qc->w_block_k != 128)
+    if ((group != 128 && group != MOE_GROUP_TOKEN && group != MOE_GROUP_TENSOR) || qc->weight != MOE_DT_FP8_E4M3 ||
+        qc->w_block_n != 128 || qc->w_block_k != 128)
       return MOE_ERR_UNSUPPORTED;
   } else if (qc->act != MOE_DT_BF16 || qc->weight != MOE_DT_BF16) {
     return MOE_ERR_UNSUPPORTED;
@@ -1117,7 +1201,8 @@ extern "C" moe_status_t moe_experts_act(const void* a1q, const float* a1q_scale,
   MOE_CHECK_ARG(!fp8 || (a1q_scale && w13_scale && w2_scale));
   MOE_CHECK_ARG(aligned16(a1q) && aligned16(w13) && aligned16(w2) && aligned16(fused_expert_output));
   const int grid = gemm_grid();
-  const WsLayout L = ws_layout(S, H, I, E, fp8, grid);
+  const WsLayout L = ws_layout(S, H, I, E, fp8, grid, group);
+  const bool hb16 = fp8 && group != 128;  // "A"/"T": bf16 h, then quantised per row or per tensor
   if (!ws || ws_bytes < L.total) return MOE_ERR_WORKSPACE;
   MOE_CHECK_ARG(aligned16(ws));
 
@@ -1166,7 +1251,8 @@ extern "C" moe_status_t moe_experts_act(const void* a1q, const float* a1q_scale,
   if (gather_rows || fp8) {
     const unsigned g = (unsigned)((S + 7) / 8);
     gather_kernel<<<g, 256, 0, s>>>(static_cast<const uint8_t*>(a1q), a1q_scale, sorted_slot, (int)S, top_k, H * esz,
-                                    H / 128, gather_rows ? wsb + L.A : nullptr, As, L.s_pad);
+                                    hb16 ? 1 : H / 128, gather_rows ? wsb + L.A : nullptr, As, L.s_pad,
+                                    group == 128 ? H / 128 : (group == MOE_GROUP_TOKEN ? 1 : 0));
     if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
   }
 
@@ -1191,10 +1277,11 @@ extern "C" moe_status_t moe_experts_act(const void* a1q, const float* a1q_scale,
   p1.H = H;
   p1.b_rows = no_mul ? I : 2 * I;
   p1.s_pad = L.s_pad;
+  p1.a_kstride = hb16 ? 0 : L.s_pad;  // "A"/"T": one scale per row for every K block
   p1.a_scale_t = As;
   p1.w_scale = w13_scale;
-  p1.out = h;
-  p1.out_scale_t = hs;
+  p1.out = hb16 ? (void*)(wsb + L.hb) : h;
+  p1.out_scale_t = hb16 ? nullptr : hs;
   p1.flags = flags1;
   p1.partials = partials;
   p1.allow_split = split1;
@@ -1214,7 +1301,25 @@ extern "C" moe_status_t moe_experts_act(const void* a1q, const float* a1q_scale,
 
   cudaError_t e;
   if (fp8) {
-    e = launch_gemm1<true, 1>(activation, mA1, mA1x2, mB1, p1, grid, s);
+    e = hb16 ? launch_gemm1<true, 1, true>(activation, mA1, mA1x2, mB1, p1, grid, s)
+             : launch_gemm1<true, 1>(activation, mA1, mA1x2, mB1, p1, grid, s);
+    if (e == cudaSuccess && hb16) {
+      const auto* hbp = reinterpret_cast<const __nv_bfloat16*>(wsb + L.hb);
+      uint8_t* hq = static_cast<uint8_t*>(h);
+      if (group == MOE_GROUP_TOKEN) {
+        hquant_token_kernel<<<(unsigned)S, 256, 0, s>>>(hbp, I, expert_offsets, E, hq, hs);
+      } else {
+        unsigned* amax = reinterpret_cast<unsigned*>(wsb + L.hamax);
+        e = cudaMemsetAsync(amax, 0, sizeof(unsigned), s);
+        const long long nvec = S * (I / 8);
+        const unsigned g = (unsigned)((nvec + 255) / 256);
+        if (e == cudaSuccess) {
+          hquant_tensor_amax_kernel<<<std::min<unsigned>(g, 4u * grid), 256, 0, s>>>(hbp, I, expert_offsets, E, amax);
+          hquant_tensor_kernel<<<g, 256, 0, s>>>(hbp, I, expert_offsets, E, amax, hq, hs);
+        }
+      }
+      if (e == cudaSuccess) e = cudaGetLastError();
+    }
     if (e == cudaSuccess) e = launch_gemm<true, kGemm2, 1, 0>(mA2, mA2x2, mB2, p2, grid, s);
   } else {
     e = mg1 == 1 ? launch_gemm1<false, 1>(activation, mA1, mA1x2, mB1, p1, grid, s)

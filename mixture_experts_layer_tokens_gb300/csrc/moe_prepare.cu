@@ -8,6 +8,15 @@
 // threads of a 128-channel group reduce their amax with shuffles.  The scale
 // and the codes use IEEE division (never a reciprocal multiply) so the codes
 // are exactly those of the definition.
+//
+// The "A" (per token) and "T" (per tensor) formats of the same tables use the
+// same rule over a whole row or the whole tensor: a block per token reduces the
+// row's amax and then quantises the row (read twice, the second time from L2);
+// the tensor format reduces block amaxes with one atomicMax on the scale word
+// (non-negative floats order like their bit patterns), quantises, and a last
+// one-thread launch turns that amax into the scale.
+#include <algorithm>
+
 #include "moe_common.cuh"
 
 namespace moe {
@@ -15,15 +24,6 @@ namespace {
 
 constexpr int kThreads = 256;
 
-__device__ __forceinline__ void load_bf16x8(const void* p, float (&x)[8]) {
-  const uint4 v = __ldg(reinterpret_cast<const uint4*>(p));
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    x[2 * i] = bf16lo(w[i]);
-    x[2 * i + 1] = bf16hi(w[i]);
-  }
-}
 
 __device__ __forceinline__ void apply_weight(float (&x)[8], const float* topk_weights, int t) {
   // a1 * topk_weights.to(a1.dtype): the weight is rounded to bf16 first; the
@@ -86,6 +86,71 @@ __global__ void __launch_bounds__(kThreads)
   if ((threadIdx.x & 15) == 0) a1q_scale[v / 16] = s;  // [T, H/128] row-major == group index
 }
 
+
+
+
+// "A": block t quantises token t with one scale over its H channels.
+template <bool kWeight>
+__global__ void __launch_bounds__(kThreads)
+    prepare_fp8_token_kernel(const __nv_bfloat16* __restrict__ a1, const float* __restrict__ topk_weights, int H,
+                             uint8_t* __restrict__ a1q, float* __restrict__ a1q_scale) {
+  const int t = blockIdx.x;
+  const int nv = H / 8;
+  const __nv_bfloat16* row = a1 + (size_t)t * H;
+  float a = 0.f;
+  for (int v = threadIdx.x; v < nv; v += kThreads) {
+    float x[8];
+    load_bf16x8(row + (size_t)v * 8, x);
+    if (kWeight) apply_weight(x, topk_weights, t);
+    a = fmaxf(a, amax8(x));
+  }
+  const float s = __fdiv_rn(fmaxf(block_amax<kThreads>(a), 1e-10f), 448.0f);
+  uint2* out = reinterpret_cast<uint2*>(a1q + (size_t)t * H);
+  for (int v = threadIdx.x; v < nv; v += kThreads) {
+    float x[8];
+    load_bf16x8(row + (size_t)v * 8, x);
+    if (kWeight) apply_weight(x, topk_weights, t);
+    out[v] = e4m3x8(x, s);
+  }
+  if (threadIdx.x == 0) a1q_scale[t] = s;
+}
+
+// "T", step 1: amax of the tensor into *amax_bits (zeroed before the launch).
+template <bool kWeight>
+__global__ void __launch_bounds__(kThreads)
+    prepare_fp8_tensor_amax_kernel(const __nv_bfloat16* __restrict__ a1, const float* __restrict__ topk_weights,
+                                   int H, long long nvec, unsigned* __restrict__ amax_bits) {
+  const int vpr = H / 8;
+  float a = 0.f;
+  for (long long v = (long long)blockIdx.x * kThreads + threadIdx.x; v < nvec; v += (long long)gridDim.x * kThreads) {
+    float x[8];
+    load_bf16x8(a1 + v * 8, x);
+    if (kWeight) apply_weight(x, topk_weights, (int)(v / vpr));
+    a = fmaxf(a, amax8(x));
+  }
+  a = block_amax<kThreads>(a);
+  if (threadIdx.x == 0) atomicMax(amax_bits, __float_as_uint(a));
+}
+
+// "T", step 2: codes with s = fp32(max(amax, 1e-10) / 448).
+template <bool kWeight>
+__global__ void __launch_bounds__(kThreads)
+    prepare_fp8_tensor_kernel(const __nv_bfloat16* __restrict__ a1, const float* __restrict__ topk_weights, int H,
+                              long long nvec, const unsigned* __restrict__ amax_bits, uint8_t* __restrict__ a1q) {
+  const long long v = (long long)blockIdx.x * kThreads + threadIdx.x;
+  if (v >= nvec) return;
+  const float s = __fdiv_rn(fmaxf(__uint_as_float(*amax_bits), 1e-10f), 448.0f);
+  float x[8];
+  load_bf16x8(a1 + v * 8, x);
+  if (kWeight) apply_weight(x, topk_weights, (int)(v / (H / 8)));
+  reinterpret_cast<uint2*>(a1q)[v] = e4m3x8(x, s);
+}
+
+// "T", step 3: the amax word becomes the scale.
+__global__ void prepare_fp8_tensor_scale_kernel(float* a1q_scale) {
+  a1q_scale[0] = __fdiv_rn(fmaxf(a1q_scale[0], 1e-10f), 448.0f);
+}
+
 }  // namespace
 }  // namespace moe
 
@@ -99,7 +164,8 @@ extern "C" moe_status_t moe_prepare(const void* a1, const float* topk_weights, c
   MOE_CHECK_ARG(!apply_router_weight_on_input || top_k == 1);  // the pages' `assert topk == 1`
   const bool fp8 = qc->act == MOE_DT_FP8_E4M3;
   if (!fp8 && qc->act != MOE_DT_BF16) return MOE_ERR_UNSUPPORTED;
-  if (fp8 && qc->act_group != 128) return MOE_ERR_UNSUPPORTED;
+  if (fp8 && qc->act_group != 128 && qc->act_group != MOE_GROUP_TOKEN && qc->act_group != MOE_GROUP_TENSOR)
+    return MOE_ERR_UNSUPPORTED;
   MOE_CHECK_ARG(fp8 ? H % 128 == 0 : H % 8 == 0);
   MOE_CHECK_ARG(fits_int32((long long)T * H / 8 + kThreads));
   if (T == 0) return MOE_OK;
@@ -118,6 +184,23 @@ extern "C" moe_status_t moe_prepare(const void* a1, const float* topk_weights, c
       return MOE_OK;
     }
     prepare_bf16_kernel<true><<<grid, kThreads, 0, s>>>(x, topk_weights, H, nvec, static_cast<__nv_bfloat16*>(a1q));
+  } else if (qc->act_group == MOE_GROUP_TOKEN) {
+    if (apply_router_weight_on_input)
+      prepare_fp8_token_kernel<true><<<T, kThreads, 0, s>>>(x, topk_weights, H, static_cast<uint8_t*>(a1q), a1q_scale);
+    else
+      prepare_fp8_token_kernel<false><<<T, kThreads, 0, s>>>(x, topk_weights, H, static_cast<uint8_t*>(a1q), a1q_scale);
+  } else if (qc->act_group == MOE_GROUP_TENSOR) {
+    unsigned* amax = reinterpret_cast<unsigned*>(a1q_scale);
+    if (cudaMemsetAsync(amax, 0, sizeof(unsigned), s) != cudaSuccess) return MOE_ERR_CUDA;
+    const unsigned agrid = (unsigned)std::min<long long>(grid, 4LL * num_sms());
+    if (apply_router_weight_on_input) {
+      prepare_fp8_tensor_amax_kernel<true><<<agrid, kThreads, 0, s>>>(x, topk_weights, H, nvec, amax);
+      prepare_fp8_tensor_kernel<true><<<grid, kThreads, 0, s>>>(x, topk_weights, H, nvec, amax, static_cast<uint8_t*>(a1q));
+    } else {
+      prepare_fp8_tensor_amax_kernel<false><<<agrid, kThreads, 0, s>>>(x, topk_weights, H, nvec, amax);
+      prepare_fp8_tensor_kernel<false><<<grid, kThreads, 0, s>>>(x, topk_weights, H, nvec, amax, static_cast<uint8_t*>(a1q));
+    }
+    prepare_fp8_tensor_scale_kernel<<<1, 1, 0, s>>>(a1q_scale);
   } else if (apply_router_weight_on_input) {
     prepare_fp8_kernel<true><<<grid, kThreads, 0, s>>>(x, topk_weights, H, nvec, static_cast<uint8_t*>(a1q), a1q_scale);
   } else {

@@ -40,7 +40,8 @@ class LayerConfig:
     I: int
     E: int
     top_k: int
-    quant: str = "bf16"            # "bf16" or "fp8" (E4M3 G(128) activations, 128x128 block weights)
+    quant: str = "bf16"            # "bf16"; "fp8" (E4M3 G(128) activations, 128x128 block weights);
+                                   # "fp8_token" / "fp8_tensor" (per-token / per-tensor activation scales)
     scoring: str = "softmax"       # "softmax" (renormalised top-k) or "sigmoid" (top-1)
     weight_on_input: bool = False  # apply the top-k weight to a1 in prepare (top_k == 1)
     shared_I: int = 0              # intermediate size of the bf16 shared expert, 0 = none
@@ -158,7 +159,7 @@ def make_inputs(cfg: LayerConfig, seed: int = 0, device="cpu") -> LayerInputs:
     logits = torch.randn((T, E), generator=gen, device=dev, dtype=torch.float32)
     a1 = torch.randn((T, H), generator=gen, device=dev).to(torch.bfloat16)
     inp = LayerInputs(cfg, logits, a1=a1)
-    if cfg.quant == "fp8":
+    if cfg.quant != "bf16":
         inp.w13, inp.w13_scale = _fp8_weights(gen, E, 2 * I, H, dev)
         inp.w2, inp.w2_scale = _fp8_weights(gen, E, H, I, dev)
     else:

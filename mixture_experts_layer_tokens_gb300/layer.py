@@ -29,12 +29,12 @@ class MoELayer:
         self.topk_ids = torch.empty((T, k), dtype=torch.int32, device=dev)
         self.topk_weights = torch.empty((T, k), dtype=torch.float32, device=dev)
         self.al = moe.Alignment(T, k, E, dev)
-        fp8 = cfg.quant == "fp8"
+        fp8 = cfg.quant != "bf16"
         # bf16 without weight-on-input: prepare is the passthrough (a1q is a1)
         self.passthrough = not fp8 and not cfg.weight_on_input
         self.a1q = None if self.passthrough else torch.empty((T, H), dtype=torch.uint8 if fp8 else torch.bfloat16,
                                                              device=dev)
-        self.a1q_scale = torch.empty((T, H // 128), dtype=torch.float32, device=dev) if fp8 else None
+        self.a1q_scale = torch.empty(moe.scale_shape(cfg.quant, T, H), dtype=torch.float32, device=dev) if fp8 else None
         self.y = torch.empty((T * k, H), dtype=torch.bfloat16, device=dev)
         self.ws = torch.empty(max(moe.workspace_size(T, H, I, E, k, cfg.quant), 16), dtype=torch.uint8, device=dev)
         self.out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)

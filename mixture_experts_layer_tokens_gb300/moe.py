@@ -35,6 +35,25 @@ class QuantConfig(ctypes.Structure):
 
 QC_BF16 = QuantConfig(MOE_DT_BF16, 0, MOE_DT_BF16, 0, 0)
 QC_FP8 = QuantConfig(MOE_DT_FP8_E4M3, 128, MOE_DT_FP8_E4M3, 128, 128)
+MOE_GROUP_TOKEN, MOE_GROUP_TENSOR = -1, -2
+# quant names: "bf16"; "fp8" (G(128) activations); "fp8_token" ("A"); "fp8_tensor" ("T")
+QUANT_CONFIGS = {
+    "bf16": QC_BF16,
+    "fp8": QC_FP8,
+    "fp8_token": QuantConfig(MOE_DT_FP8_E4M3, MOE_GROUP_TOKEN, MOE_DT_FP8_E4M3, 128, 128),
+    "fp8_tensor": QuantConfig(MOE_DT_FP8_E4M3, MOE_GROUP_TENSOR, MOE_DT_FP8_E4M3, 128, 128),
+}
+
+
+def _qc(quant: str) -> QuantConfig:
+    if quant not in QUANT_CONFIGS:
+        raise ValueError(f"unknown quantisation {quant!r}")
+    return QUANT_CONFIGS[quant]
+
+
+def scale_shape(quant: str, T: int, H: int):
+    """Shape of a1q_scale for each fp8 format (None for bf16)."""
+    return {"bf16": None, "fp8": (T, H // 128), "fp8_token": (T,), "fp8_tensor": (1,)}[quant]
 _QCP = ctypes.POINTER(QuantConfig)
 
 SIGNATURES = {
@@ -178,17 +197,19 @@ def moe_prepare(a1: torch.Tensor, topk_weights: Optional[torch.Tensor], top_k: i
                 apply_router_weight_on_input: bool, quant: str, a1q: Optional[torch.Tensor] = None,
                 a1q_scale: Optional[torch.Tensor] = None, topk_ids: Optional[torch.Tensor] = None,
                 stream=None):
-    """quant: "bf16" (no quantisation) or "fp8" (E4M3, per-token 128-group scales).
-    Passing ``a1q=a1`` with bf16 and no weight is the passthrough (nothing runs)."""
+    """quant: "bf16" (no quantisation), "fp8" (E4M3, per-token 128-group scales
+    [T, H/128]), "fp8_token" (one scale per token [T]) or "fp8_tensor" (one scale
+    [1]).  Passing ``a1q=a1`` with bf16 and no weight is the passthrough (nothing runs)."""
     _need(a1, torch.bfloat16, "a1")
     _need(topk_weights, torch.float32, "topk_weights")
     T, H = a1.shape
-    qc = QC_FP8 if quant == "fp8" else QC_BF16
+    qc = _qc(quant)
+    fp8 = quant != "bf16"
     if a1q is None:
-        a1q = torch.empty((T, H), dtype=torch.uint8 if quant == "fp8" else torch.bfloat16, device=a1.device)
-    if quant == "fp8" and a1q_scale is None:
-        a1q_scale = torch.empty((T, H // 128), dtype=torch.float32, device=a1.device)
-    _need(a1q, torch.uint8 if quant == "fp8" else torch.bfloat16, "a1q")
+        a1q = torch.empty((T, H), dtype=torch.uint8 if fp8 else torch.bfloat16, device=a1.device)
+    if fp8 and a1q_scale is None:
+        a1q_scale = torch.empty(scale_shape(quant, T, H), dtype=torch.float32, device=a1.device)
+    _need(a1q, torch.uint8 if fp8 else torch.bfloat16, "a1q")
     _need(a1q_scale, torch.float32, "a1q_scale")
     _check("moe_prepare", lib().moe_prepare(_ptr(a1), _ptr(topk_weights), _ptr(topk_ids), T, H, top_k,
                                             int(bool(apply_router_weight_on_input)), ctypes.byref(qc), _ptr(a1q),
@@ -197,7 +218,7 @@ def moe_prepare(a1: torch.Tensor, topk_weights: Optional[torch.Tensor], top_k: i
 
 
 def workspace_size(T: int, H: int, I: int, E: int, top_k: int, quant: str) -> int:
-    return int(lib().moe_workspace_size(T, H, I, E, top_k, ctypes.byref(QC_FP8 if quant == "fp8" else QC_BF16)))
+    return int(lib().moe_workspace_size(T, H, I, E, top_k, ctypes.byref(_qc(quant))))
 
 
 def moe_experts(a1q: torch.Tensor, a1q_scale: Optional[torch.Tensor], w13: torch.Tensor,
@@ -210,7 +231,7 @@ def moe_experts(a1q: torch.Tensor, a1q_scale: Optional[torch.Tensor], w13: torch
     the tokens in order."""
     if activation not in ACTIVATIONS:
         raise ValueError(f"unknown activation {activation!r}")
-    fp8 = quant == "fp8"
+    fp8 = quant != "bf16"
     _need(a1q, torch.uint8 if fp8 else torch.bfloat16, "a1q")
     _need(w13, torch.uint8 if fp8 else torch.bfloat16, "w13")
     _need(w2, torch.uint8 if fp8 else torch.bfloat16, "w2")
@@ -225,7 +246,7 @@ def moe_experts(a1q: torch.Tensor, a1q_scale: Optional[torch.Tensor], w13: torch
     _need(out, torch.bfloat16, "fused_expert_output")
     if ws is None:
         ws = torch.empty(max(workspace_size(T, H, I, E, k, quant), 16), dtype=torch.uint8, device=a1q.device)
-    qc = QC_FP8 if fp8 else QC_BF16
+    qc = _qc(quant)
     _check("moe_experts_act", lib().moe_experts_act(
         _ptr(a1q), _ptr(a1q_scale), _ptr(w13), _ptr(w13_scale), _ptr(w2), _ptr(w2_scale), _ptr(al.expert_offsets),
         None if identity else _ptr(al.sorted_slot), _ptr(al.tile_map), _ptr(al.num_tiles), T, H, I, E, k,

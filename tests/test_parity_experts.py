@@ -115,10 +115,17 @@ def test_experts_twice_same_bits(cuda_dev):
     (300, 512, 384, 4, 2, "fp8", "swigluoai"),
     (300, 512, 384, 4, 2, "fp8", "silu_no_mul"),    # three G(128) groups of h, the last alone in its tile
     (100, 1024, 512, 16, 4, "fp8", "gelu_no_mul"),
+    # per-token ("A") and per-tensor ("T") activation scales: h stored bf16, then quantised
+    (300, 512, 384, 4, 2, "fp8_token", "silu"),
+    (300, 512, 384, 4, 2, "fp8_tensor", "silu"),
+    (100, 1024, 512, 16, 4, "fp8_token", "gelu_no_mul"),
+    (100, 1024, 512, 16, 4, "fp8_tensor", "swigluoai"),
+    (256, 256, 2048, 64, 4, "fp8_token", "silu"),    # round-robin schedule
+    (500, 384, 256, 6, 2, "fp8_tensor", "silu_no_mul"),
 ])
 def test_experts_activations(cuda_dev, T, H, I, E, k, quant, act):
-    base = CONFIGS["deepseek"] if quant == "fp8" else CONFIGS["tiny"]
-    inp = make_inputs(scaled(base, T=T, H=H, I=I, E=E, top_k=k, shared_I=0))
+    base = CONFIGS["deepseek"] if quant != "bf16" else CONFIGS["tiny"]
+    inp = make_inputs(scaled(base, T=T, H=H, I=I, E=E, top_k=k, shared_I=0, quant=quant))
     w13, w13_scale = inp.w13, inp.w13_scale
     if act == "swigluoai" and quant == "bf16":
         # gate and up values of a few units, so that both clamps at +-7 are reached
@@ -127,8 +134,8 @@ def test_experts_activations(cuda_dev, T, H, I, E, k, quant, act):
         w13 = w13[:, :I].contiguous()
         w13_scale = None if w13_scale is None else w13_scale[:, :I // 128].contiguous()
     y, yref = _run(inp, _ids(T, k, E, T + I + 7), cuda_dev, quant, act=act, w13=w13, w13_scale=w13_scale)
-    if quant == "fp8":
-        check_fp8(y, yref, f"experts fp8 {act}")
+    if quant != "bf16":
+        check_fp8(y, yref, f"experts {quant} {act}")
     else:
         check_bf16(y, yref, f"experts bf16 {act}", slack=_stored_pair_slack(yref))
 

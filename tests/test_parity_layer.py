@@ -35,7 +35,12 @@ def oracle_tokens(inp, tokens, gpu_ids, gpu_w):
     a1q, sc = moe_ref.prepare(a1, w, cfg.weight_on_input, cfg.quant)
     n, H = len(tokens), cfg.H
     y = torch.zeros((n * k, H), dtype=torch.float64)
-    for e in sorted(set(ids.reshape(-1).tolist())):
+    if cfg.quant == "fp8_tensor":
+        # one scale over every expert's intermediate: the whole layer at once (all tokens)
+        assert n == cfg.T
+        y = moe_ref.experts(a1q, sc, inp.w13, inp.w13_scale, inp.w2, inp.w2_scale, moe_ref.align(ids, cfg.E, 128),
+                            k, cfg.quant)
+    for e in ([] if cfg.quant == "fp8_tensor" else sorted(set(ids.reshape(-1).tolist()))):
         slots = [(i, j) for i in range(n) for j in range(k) if int(ids[i, j]) == e]
         rows = np.array([i for i, _ in slots])
         A = moe_ref._act64(a1q, sc, rows, cfg.quant)
@@ -61,7 +66,7 @@ def oracle_tokens(inp, tokens, gpu_ids, gpu_w):
 
 def _check(cfg, out, ref, what):
     ref, slack = ref
-    if cfg.quant == "fp8":
+    if cfg.quant != "bf16":
         return check_fp8(out, ref, what)
     return check_bf16(out, ref, what, slack=slack)
 
@@ -70,6 +75,8 @@ SMALL = {
     "tiny": CONFIGS["tiny"],
     "mixtral_small": scaled(CONFIGS["mixtral"], T=200, H=512, I=768),
     "deepseek_small": scaled(CONFIGS["deepseek"], T=256, H=512, I=256, E=32, shared_I=256),
+    "deepseek_small_token": scaled(CONFIGS["deepseek"], T=256, H=512, I=256, E=32, shared_I=256, quant="fp8_token"),
+    "deepseek_small_tensor": scaled(CONFIGS["deepseek"], T=256, H=512, I=256, E=32, shared_I=256, quant="fp8_tensor"),
     "llama_small": scaled(CONFIGS["llama8"], T=100, H=384, I=512, shared_I=256),
     "llama_small_T1": scaled(CONFIGS["llama1"], H=384, I=512, shared_I=256),
     "residual_rms": scaled(CONFIGS["mixtral"], T=64, H=256, I=256, residual=True, rms=True),

@@ -18,7 +18,8 @@ def _a1(T, H, seed, wide=False):
     return x.to(torch.bfloat16)
 
 
-@pytest.mark.parametrize("quant,won", [("fp8", False), ("fp8", True), ("bf16", True)])
+@pytest.mark.parametrize("quant,won", [("fp8", False), ("fp8", True), ("bf16", True), ("fp8_token", False),
+                                       ("fp8_token", True), ("fp8_tensor", False), ("fp8_tensor", True)])
 @pytest.mark.parametrize("T,H", [(1, 128), (37, 512), (4096, 7168), (64, 5120)])
 def test_prepare_bit_exact(cuda_dev, quant, won, T, H):
     a1 = _a1(T, H, T + H)
@@ -29,7 +30,7 @@ def test_prepare_bit_exact(cuda_dev, quant, won, T, H):
     torch.cuda.synchronize()
     rq, rs = moe_ref.prepare(a1, w, won, quant)
     assert torch.equal(q.cpu(), rq)
-    if quant == "fp8":
+    if quant != "bf16":
         assert torch.equal(s.cpu(), rs)
 
 
