@@ -91,31 +91,70 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
     for (int i = 0; i < 8; ++i) o[u][i] = 0.f;
 
-  for (int j = 0; j < top_k; ++j) {
-    const float w = weights_on_input ? 1.0f : __ldg(topk_w + (size_t)t * top_k + j);
-    const __nv_bfloat16* yr = y + ((size_t)t * top_k + j) * H + (size_t)v0 * 8;
-    uint4 v[NV];
+  // Short slices (a few vectors per thread, the cluster launches of small T): every row's
+  // loads are issued before the first add, so the k + 2 rows cost one memory round trip
+  // instead of one each.  The adds keep the row order of the general path (same bits).
+  constexpr int kMaxBatchK = 8;
+  if (NV <= 2 && top_k <= kMaxBatchK) {
+    uint4 yv[kMaxBatchK][NV], sv[NV], rv[NV];
+    float wj[kMaxBatchK];
 #pragma unroll
-    for (int u = 0; u < NV; ++u) {
-      const int vi = threadIdx.x + u * kThreads;
-      if (vi < vslice) v[u] = ldg_nc(yr + (size_t)vi * 8);
+    for (int j = 0; j < kMaxBatchK; ++j) {
+      if (j < top_k) {
+        wj[j] = weights_on_input ? 1.0f : __ldg(topk_w + (size_t)t * top_k + j);
+        const __nv_bfloat16* yr = y + ((size_t)t * top_k + j) * H + (size_t)v0 * 8;
+#pragma unroll
+        for (int u = 0; u < NV; ++u) {
+          const int vi = threadIdx.x + u * kThreads;
+          if (vi < vslice) yv[j][u] = ldg_nc(yr + (size_t)vi * 8);
+        }
+      }
     }
 #pragma unroll
-    for (int u = 0; u < NV; ++u)
-      if (threadIdx.x + u * kThreads < vslice) add_bf16x8(o[u], v[u], w);
-  }
-  if (shared) {
-#pragma unroll
     for (int u = 0; u < NV; ++u) {
       const int vi = threadIdx.x + u * kThreads;
-      if (vi < vslice) add_bf16x8(o[u], ldg_nc(shared + row + (size_t)(v0 + vi) * 8), 1.0f);
+      if (shared && vi < vslice) sv[u] = ldg_nc(shared + row + (size_t)(v0 + vi) * 8);
+      if (residual && vi < vslice) rv[u] = ldg_nc(residual + row + (size_t)(v0 + vi) * 8);
     }
-  }
-  if (residual) {
+#pragma unroll
+    for (int j = 0; j < kMaxBatchK; ++j)
+      if (j < top_k)
+#pragma unroll
+        for (int u = 0; u < NV; ++u)
+          if (threadIdx.x + u * kThreads < vslice) add_bf16x8(o[u], yv[j][u], wj[j]);
 #pragma unroll
     for (int u = 0; u < NV; ++u) {
-      const int vi = threadIdx.x + u * kThreads;
-      if (vi < vslice) add_bf16x8(o[u], ldg_nc(residual + row + (size_t)(v0 + vi) * 8), 1.0f);
+      if (threadIdx.x + u * kThreads >= vslice) continue;
+      if (shared) add_bf16x8(o[u], sv[u], 1.0f);
+      if (residual) add_bf16x8(o[u], rv[u], 1.0f);
+    }
+  } else {
+    for (int j = 0; j < top_k; ++j) {
+      const float w = weights_on_input ? 1.0f : __ldg(topk_w + (size_t)t * top_k + j);
+      const __nv_bfloat16* yr = y + ((size_t)t * top_k + j) * H + (size_t)v0 * 8;
+      uint4 v[NV];
+#pragma unroll
+      for (int u = 0; u < NV; ++u) {
+        const int vi = threadIdx.x + u * kThreads;
+        if (vi < vslice) v[u] = ldg_nc(yr + (size_t)vi * 8);
+      }
+#pragma unroll
+      for (int u = 0; u < NV; ++u)
+        if (threadIdx.x + u * kThreads < vslice) add_bf16x8(o[u], v[u], w);
+    }
+    if (shared) {
+#pragma unroll
+      for (int u = 0; u < NV; ++u) {
+        const int vi = threadIdx.x + u * kThreads;
+        if (vi < vslice) add_bf16x8(o[u], ldg_nc(shared + row + (size_t)(v0 + vi) * 8), 1.0f);
+      }
+    }
+    if (residual) {
+#pragma unroll
+      for (int u = 0; u < NV; ++u) {
+        const int vi = threadIdx.x + u * kThreads;
+        if (vi < vslice) add_bf16x8(o[u], ldg_nc(residual + row + (size_t)(v0 + vi) * 8), 1.0f);
+      }
     }
   }
   if (residual_out) {
