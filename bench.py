@@ -48,6 +48,10 @@ def parse():
     ap.add_argument("--workload", default="mixtral", choices=sorted(CONFIGS))
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile-unit", action="store_true",
+                    help="for ncu --profile-from-start off: warm up, run the dominant unit (the roofline's "
+                         "kernel group) once between cudaProfilerStart and cudaProfilerStop, and exit")
+    ap.add_argument("--profile-step", action="store_true", help="the same with one layer step")
     ap.add_argument("--no-graph", action="store_true", help="launch the step's calls one by one instead of "
                     "replaying them as one captured CUDA graph")
     return ap.parse_args()
@@ -67,21 +71,50 @@ def experts_algorithmic(cfg, counts):
     """Bytes and FLOPs one expert pass must move/do: the weights of the experts
     that received tokens (+ fp8 block scales), the activations read once, the
     intermediate h written and read once, the output rows written once; FLOPs
-    6 H I per token slot (no padded rows)."""
+    2 H I per weight matrix (3 gated, 2 for *_no_mul) per token slot (no padded rows)."""
     fp8 = cfg.quant != "bf16"
     esz = 1 if fp8 else 2
     touched = int((counts > 0).sum())
-    w = touched * 3 * cfg.H * cfg.I * esz
+    mats = 2 if cfg.activation.endswith("_no_mul") else 3  # gate (+ up) and down projections
+    w = touched * mats * cfg.H * cfg.I * esz
     if fp8:
-        w += touched * 3 * (cfg.H // 128) * (cfg.I // 128) * 4
+        w += touched * mats * (cfg.H // 128) * (cfg.I // 128) * 4
     S = cfg.T * cfg.top_k
     act = cfg.T * cfg.H * esz + 2 * S * cfg.I * esz + S * cfg.H * 2
     if cfg.quant == "fp8":
         act += cfg.T * (cfg.H // 128) * 4 + 2 * S * (cfg.I // 128) * 4
     elif fp8:  # per-token / per-tensor: per-row scales, and h also stored in bf16 and read back
         act += cfg.T * 4 + 2 * S * 4 + 2 * S * cfg.I * 2
-    flops = 6.0 * S * cfg.H * cfg.I
+    flops = 2.0 * mats * S * cfg.H * cfg.I
     return w + act, flops
+
+
+def sources_digest() -> str:
+    """sha256 over the kernel sources (csrc/*.cu, *.cuh) and the public header."""
+    import hashlib
+    pkg = os.path.join(os.path.dirname(os.path.abspath(__file__)), "mixture_experts_layer_tokens_gb300", "csrc")
+    h = hashlib.sha256()
+    files = sorted(f for f in os.listdir(pkg) if f.endswith((".cu", ".cuh")))
+    for f in files + ["../../include/moe.h"]:
+        with open(os.path.join(pkg, f), "rb") as fh:
+            h.update(f.encode() + b"\0" + fh.read())
+    return h.hexdigest()
+
+
+def measured_traffic(workload: str):
+    """DRAM bytes (read + write) of one dominant-unit call from the committed ncu
+    capture (profiles/dram_traffic.json), scaled to this workload when the capture
+    was of a smaller case; None when there is none or the kernels changed since."""
+    path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "profiles", "dram_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+        e = rec["workloads"][workload]
+        if rec["sources_sha256"] != sources_digest():
+            return None
+        return int(e["bytes_per_call"])
+    except Exception:
+        return None
 
 
 def finalize_algorithmic(cfg, nvfp4):
@@ -162,8 +195,12 @@ def oracle_tokens_seconds(inp, tokens):
         ids, w = moe_ref.route_softmax_renorm(logits, cfg.top_k)
     a1 = inp.a1[tokens].cpu()
     a1q, sc = moe_ref.prepare(a1, w, cfg.weight_on_input, cfg.quant)
-    y = torch.cat([moe_ref.token_expert_rows(a1q, sc, inp.w13, inp.w13_scale, inp.w2, inp.w2_scale, ids, i,
-                                             cfg.quant) for i in range(len(tokens))], 0)
+    if cfg.quant == "fp8_tensor":  # one intermediate scale over every expert's rows of the sample
+        y = moe_ref.experts(a1q, sc, inp.w13, inp.w13_scale, inp.w2, inp.w2_scale, moe_ref.align(ids, cfg.E, 128),
+                            cfg.top_k, cfg.quant, cfg.activation)
+    else:
+        y = torch.cat([moe_ref.token_expert_rows(a1q, sc, inp.w13, inp.w13_scale, inp.w2, inp.w2_scale, ids, i,
+                                                 cfg.quant, cfg.activation) for i in range(len(tokens))], 0)
     shared = moe_ref.dense_mlp(a1, inp.shared_w13[0], inp.shared_w2[0]) if cfg.shared_I else None
     res = inp.residual[tokens].cpu() if inp.residual is not None else None
     moe_ref.finalize(y, w, cfg.top_k, cfg.weight_on_input, shared=shared, residual=res,
@@ -285,6 +322,39 @@ def run_gpu(args, ws, rank, local):
             step()
         torch.cuda.synchronize(dev)
         assert moe.moe_device_status() == moe.MOE_OK
+
+        # the dominant unit: the kernel group the roofline reports
+        if cfg.finalize_only:
+            dom_name = "moe_finalize (NVFP4 out)"
+            nbytes = finalize_algorithmic(cfg, True)
+            flops = 0.0
+            step_obj.weights()
+
+            def dom_call():
+                step_obj.finalize(True)
+        else:
+            dom_name = f"moe_experts (plan + gather + GEMM1 {cfg.activation} + GEMM2 scatter)"
+            layer.forward(inp.logits, inp.a1)  # route/align/prepare state for the experts call
+            counts = torch.diff(layer.al.expert_offsets).cpu().numpy()
+            nbytes, flops = experts_algorithmic(cfg, counts)
+            a1q_dom = inp.a1 if layer.passthrough else layer.a1q
+
+            def dom_call():
+                moe.moe_experts(a1q_dom, layer.a1q_scale, inp.w13, inp.w13_scale, inp.w2, inp.w2_scale, layer.al,
+                                cfg.quant, out=layer.y, ws=layer.ws, activation=cfg.activation)
+        if args.profile_unit or args.profile_step:
+            # one call between profiler start and stop (ncu --profile-from-start off), then exit
+            (dom_call if args.profile_unit else step)()
+            torch.cuda.synchronize(dev)
+            torch.cuda.profiler.start()
+            (dom_call if args.profile_unit else step)()
+            torch.cuda.synchronize(dev)
+            torch.cuda.profiler.stop()
+            assert moe.moe_device_status() == moe.MOE_OK
+            if rank == 0:
+                print(json.dumps({"profiled": "unit" if args.profile_unit else "step", "workload": cfg.name,
+                                  "kernel": dom_name}), flush=True)
+            return
         graph = None
         if not args.no_graph:
             # the step's library calls captured once and replayed: same kernels, no per-call host work
@@ -316,24 +386,6 @@ def run_gpu(args, ws, rank, local):
         # ---- dominant unit: R back-to-back calls captured in one graph, replayed;
         # CUDA events on the launching stream give the device time per call
         R = 10
-        if cfg.finalize_only:
-            dom_name = "moe_finalize (NVFP4 out)"
-            nbytes = finalize_algorithmic(cfg, True)
-            flops = 0.0
-            step_obj.weights()
-
-            def dom_call():
-                step_obj.finalize(True)
-        else:
-            dom_name = "moe_experts (plan + gather + GEMM1 SiLU + GEMM2 scatter)"
-            layer.forward(inp.logits, inp.a1)  # route/align/prepare state for the experts call
-            counts = torch.diff(layer.al.expert_offsets).cpu().numpy()
-            nbytes, flops = experts_algorithmic(cfg, counts)
-            a1q_dom = inp.a1 if layer.passthrough else layer.a1q
-
-            def dom_call():
-                moe.moe_experts(a1q_dom, layer.a1q_scale, inp.w13, inp.w13_scale, inp.w2, inp.w2_scale, layer.al,
-                                cfg.quant, out=layer.y, ws=layer.ws)
         for _ in range(3):
             dom_call()
         torch.cuda.synchronize(dev)
@@ -365,14 +417,16 @@ def run_gpu(args, ws, rank, local):
         if t_tensor > t_hbm:
             achieved = flops / (dom_ms * 1e-3) / 1e12
             roofline = {"bound": "tensor", "achieved": round(achieved, 1), "peak": round(tensor_peak, 1),
-                        "unit": "TFLOP/s", "frac": round(achieved / tensor_peak, 4), "traffic": None,
+                        "unit": "TFLOP/s", "frac": round(achieved / tensor_peak, 4),
+                        "traffic": measured_traffic(cfg.name),
                         "kernel": dom_name, "algorithmic_flops": flops, "ms": round(dom_ms, 4),
                         "peak_kind": peak_kind + (" bf16 x2 (nominal fp8:bf16)" if cfg.quant != "bf16" else "")}
             roofline["hbm_gbs"] = round(nbytes / (dom_ms * 1e-3) / 1e9, 1)
         else:
             achieved = nbytes / (dom_ms * 1e-3) / 1e9
             roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
-                        "frac": round(achieved / hbm_peak, 4), "traffic": None, "kernel": dom_name,
+                        "frac": round(achieved / hbm_peak, 4), "traffic": measured_traffic(cfg.name),
+                        "kernel": dom_name,
                         "algorithmic_bytes": int(nbytes), "ms": round(dom_ms, 4), "peak_kind": peak_kind}
             if flops:
                 roofline["tflops"] = round(flops / (dom_ms * 1e-3) / 1e12, 1)
