@@ -89,28 +89,31 @@ def experts_algorithmic(cfg, counts):
     return w + act, flops
 
 
-def sources_digest() -> str:
-    """sha256 over the kernel sources (csrc/*.cu, *.cuh) and the public header."""
+# kernel sources of each dominant unit (csrc/ files; the public header always counts)
+UNIT_SOURCES = {"experts": ["moe_experts.cu", "moe_common.cuh"], "finalize": ["moe_finalize.cu", "moe_common.cuh"]}
+
+
+def sources_digest(files) -> str:
+    """sha256 over the given csrc/ files and the public header."""
     import hashlib
-    pkg = os.path.join(os.path.dirname(os.path.abspath(__file__)), "mixture_experts_layer_tokens_gb300", "csrc")
+    csrc = os.path.join(os.path.dirname(os.path.abspath(__file__)), "mixture_experts_layer_tokens_gb300", "csrc")
     h = hashlib.sha256()
-    files = sorted(f for f in os.listdir(pkg) if f.endswith((".cu", ".cuh")))
-    for f in files + ["../../include/moe.h"]:
-        with open(os.path.join(pkg, f), "rb") as fh:
+    for f in sorted(files) + ["../../include/moe.h"]:
+        with open(os.path.join(csrc, f), "rb") as fh:
             h.update(f.encode() + b"\0" + fh.read())
     return h.hexdigest()
 
 
 def measured_traffic(workload: str):
     """DRAM bytes (read + write) of one dominant-unit call from the committed ncu
-    capture (profiles/dram_traffic.json), scaled to this workload when the capture
-    was of a smaller case; None when there is none or the kernels changed since."""
+    capture (profiles/dram_traffic.json; for a workload too large to capture, the
+    recorded scaling of a smaller case); None when there is none or the unit's
+    kernel sources changed since."""
     path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "profiles", "dram_traffic.json")
     try:
         with open(path) as f:
-            rec = json.load(f)
-        e = rec["workloads"][workload]
-        if rec["sources_sha256"] != sources_digest():
+            e = json.load(f)["workloads"][workload]
+        if e["sources_sha256"] != sources_digest(UNIT_SOURCES[e["unit"]]):
             return None
         return int(e["bytes_per_call"])
     except Exception:

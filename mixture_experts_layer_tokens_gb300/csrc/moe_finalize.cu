@@ -319,15 +319,17 @@ extern "C" moe_status_t moe_finalize(void* output, const void* fused_expert_outp
   MOE_CHECK_ARG(out_dtype != MOE_DT_NVFP4 || out_scale);
   MOE_CHECK_ARG(aligned16(shared) && aligned16(residual) && aligned16(rms_weight) && aligned16(residual_out));
   // Cluster size: the smallest of 1, 2, 4 whose row slices fit one CTA's
-  // registers (8 vectors per thread), grown while the grid would still leave
-  // SMs idle.  With NVFP4 output the slices are whole 16-element groups.
+  // registers (8 vectors per thread), grown while the grid has fewer than 4
+  // CTAs per SM (measured: T=512 at H=7168 is 3% faster with 2-CTA clusters
+  // than with one CTA per token).  With NVFP4 output the slices are whole
+  // 16-element groups.
   const int nsm = num_sms();
   const int grp = out_dtype == MOE_DT_NVFP4 ? 16 : 8;
   auto slice_ok = [&](int c) { return H % (grp * c) == 0 && (H / 8) / c <= 8 * kThreads; };
   int C = 1;
   while (C < 4 && !slice_ok(C)) C *= 2;
   if (!slice_ok(C)) return MOE_ERR_UNSUPPORTED;
-  while (C < 4 && (long long)T * C < 2LL * nsm && slice_ok(2 * C) && (H / 8) / (2 * C) >= kThreads) C *= 2;
+  while (C < 4 && (long long)T * C < 4LL * nsm && slice_ok(2 * C) && (H / 8) / (2 * C) >= kThreads) C *= 2;
   const int per_cta = (H / 8) / C;
   const int nv = (per_cta + kThreads - 1) / kThreads;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
