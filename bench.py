@@ -336,15 +336,21 @@ def run_gpu(args, ws, rank, local):
             def dom_call():
                 step_obj.finalize(True)
         else:
-            dom_name = f"moe_experts (plan + gather + GEMM1 {cfg.activation} + GEMM2 scatter)"
+            # the routed experts and, when the layer has one, the shared expert (one
+            # moe_experts_multi call when they share launches, else two calls)
+            dom_name = (f"moe_experts (plan + gather + GEMM1 {cfg.activation} + GEMM2 scatter)"
+                        + ("" if not cfg.shared_I else
+                           " + shared expert" + (" in the same launches" if layer.fused_shared else "")))
             layer.forward(inp.logits, inp.a1)  # route/align/prepare state for the experts call
             counts = torch.diff(layer.al.expert_offsets).cpu().numpy()
             nbytes, flops = experts_algorithmic(cfg, counts)
+            if cfg.shared_I:
+                nbytes += 3 * cfg.H * cfg.shared_I * 2 + 2 * cfg.T * cfg.H * 2 + 2 * cfg.T * cfg.shared_I * 2
+                flops += 6.0 * cfg.T * cfg.H * cfg.shared_I
             a1q_dom = inp.a1 if layer.passthrough else layer.a1q
 
             def dom_call():
-                moe.moe_experts(a1q_dom, layer.a1q_scale, inp.w13, inp.w13_scale, inp.w2, inp.w2_scale, layer.al,
-                                cfg.quant, out=layer.y, ws=layer.ws, activation=cfg.activation)
+                layer.experts(a1q_dom, layer.a1q_scale, inp.a1)
         if args.profile_unit or args.profile_step:
             # one call between profiler start and stop (ncu --profile-from-start off), then exit
             (dom_call if args.profile_unit else step)()

@@ -235,6 +235,37 @@ moe_status_t moe_experts_act(const void *a1q, const float *a1q_scale, const void
                              moe_stream_t stream);
 size_t moe_workspace_size(int T, int H, int I, int E, int top_k, const moe_quant_config *qc);
 
+/* Several expert problems with the same hidden size H in the same two GEMM
+ * launches -- typically a layer's routed experts and its shared expert (E = 1,
+ * top_k = 1, sorted_slot NULL).  Not in the pages: their shared-expert row is a
+ * separate MLP the finalize adds; computing both in one pass of launches saves
+ * each GEMM's start-up and tail once (decode-sized layers spend a large share
+ * of a GEMM there).  Each problem as for moe_experts_act, all with the same
+ * activation and qc.  num_problems is 1 or 2; two problems need bf16 (qc) and
+ * the same I (the second GEMM's depth), else MOE_ERR_UNSUPPORTED.  Problems
+ * with no rows (T == 0) are skipped.  ws: moe_workspace_size_multi(...) bytes;
+ * every output and error as for moe_experts. */
+typedef struct {
+  const void *a1q;
+  const float *a1q_scale;
+  const void *w13;
+  const float *w13_scale;
+  const void *w2;
+  const float *w2_scale;
+  const int32_t *expert_offsets;
+  const int32_t *sorted_slot;
+  const int32_t *tile_map;
+  const int32_t *num_tiles;
+  int T, I, E, top_k;
+  void *fused_expert_output;
+} moe_experts_problem;
+
+moe_status_t moe_experts_multi(const moe_experts_problem *problems, int num_problems, int H,
+                               const moe_quant_config *qc, int activation, void *ws,
+                               size_t ws_bytes, moe_stream_t stream);
+size_t moe_workspace_size_multi(const moe_experts_problem *problems, int num_problems, int H,
+                                const moe_quant_config *qc);
+
 /* ------------------------------------------------------------------ finalize
  * Finalize: the top-k weight-and-reduce of the "No DP/EP" listing followed by
  * the single-GPU part of the flashinfer finalize fusion (introduction of its

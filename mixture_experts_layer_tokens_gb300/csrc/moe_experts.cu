@@ -123,6 +123,16 @@ struct GemmParams {
   float* partials;             // [gridDim.x][PARTIAL_FLOATS] one split-segment partial per CTA
 };
 
+// Up to two expert problems in one launch (moe_experts_multi: typically a layer's
+// routed experts and its shared expert).  Their units are numbered one after the
+// other, problem 0 first, and share the schedule, the K depth and the per-CTA
+// split partials.
+constexpr int kMaxProblems = 2;
+struct GemmProblems {
+  GemmParams p[kMaxProblems];
+  int nprob;
+};
+
 struct Unit {
   int e, row0, row_end, n;  // rows [row0, row_end) of expert e (at most MG*BM), N tile n
 };
@@ -264,7 +274,9 @@ __device__ __forceinline__ void fma2(float& a0, float& a1, float v0, float v1, f
 template <bool kFP8, int kKind, int kMG, int kAct, bool kHB16>
 __global__ void __launch_bounds__(Warps<kFP8>::THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
-                const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
+                const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmA_1,
+                const __grid_constant__ CUtensorMap tmA2_1, const __grid_constant__ CUtensorMap tmB_1,
+                const __grid_constant__ GemmProblems pp) {
   using C = Cfg<kFP8, kMG>;
   // gemm1 forms: a gated activation reads 128 gate + 128 up rows per unit (one 3-D
   // box); a *_NO_MUL one reads 256 consecutive gate rows, like gemm2
@@ -316,6 +328,11 @@ __global__ void __launch_bounds__(Warps<kFP8>::THREADS, 1)
     prefetch_tensormap(&tmA);
     if (MG == 2) prefetch_tensormap(&tmA2);
     prefetch_tensormap(&tmB);
+    if (pp.nprob > 1) {
+      prefetch_tensormap(&tmA_1);
+      if (MG == 2) prefetch_tensormap(&tmA2_1);
+      prefetch_tensormap(&tmB_1);
+    }
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, TMEM_COLS);
@@ -326,13 +343,15 @@ __global__ void __launch_bounds__(Warps<kFP8>::THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  const int units = __ldg(p.num_groups) * p.NT;
-  const int KB = p.K / C::kBK;
+  const GemmParams& p0 = pp.p[0];
+  const int units0 = __ldg(p0.num_groups) * p0.NT;  // problem 1's units follow problem 0's
+  const int units = units0 + (pp.nprob > 1 ? __ldg(pp.p[1].num_groups) * pp.p[1].NT : 0);
+  const int KB = p0.K / C::kBK;
   Sched sched;
   // fp8 units are never split: its register promotion leaves no room for the split logic
   constexpr bool kSplit = !kFP8;
   // (split units have one M tile: the fix-up below sums one tile's rows)
-  sched.init(units, KB, gridDim.x, blockIdx.x, kSplit && MG == 1 && p.allow_split);
+  sched.init(units, KB, gridDim.x, blockIdx.x, kSplit && MG == 1 && p0.allow_split);
   int u, kb0, kb1;
 
   if (warp == 0) {
@@ -343,19 +362,21 @@ __global__ void __launch_bounds__(Warps<kFP8>::THREADS, 1)
     // iterations ahead of the loads (lane 0 only), so more weight bytes are in
     // flight from HBM than the shared-memory stages hold
     Sched pfs = sched;
-    int pf_kb = 0, pf_kb1 = 0;
+    int pf_kb = 0, pf_kb1 = 0, pf_prob = 0;
     Unit pit{};
     auto prefetch_next = [&](bool issue) {
       if (pf_kb >= pf_kb1) {
         int pu;
         if (!pfs.next(pu, pf_kb, pf_kb1)) return;
-        pit = decode<MG>(p, pu);
+        pf_prob = pu >= units0;
+        pit = decode<MG>(pp.p[pf_prob], pu - (pf_prob ? units0 : 0));
       }
       if (issue) {
+        const CUtensorMap* mB = pf_prob ? &tmB_1 : &tmB;
         if (kPair)
-          tma_prefetch_3d(&tmB, pf_kb * C::kBK, pit.n * 128, 2 * pit.e);
+          tma_prefetch_3d(mB, pf_kb * C::kBK, pit.n * 128, 2 * pit.e);
         else
-          tma_prefetch_2d(&tmB, pf_kb * C::kBK, pit.e * p.b_rows + pit.n * 256);
+          tma_prefetch_2d(mB, pf_kb * C::kBK, pit.e * pp.p[pf_prob].b_rows + pit.n * 256);
       }
       ++pf_kb;
     };
@@ -369,7 +390,12 @@ __global__ void __launch_bounds__(Warps<kFP8>::THREADS, 1)
     long long fills = 0;
     bool ok = true;
     while (ok && sched.next(u, kb0, kb1)) {
-      const Unit it = decode<MG>(p, u);
+      const int prob = u >= units0;
+      const GemmParams& p = pp.p[prob];
+      const CUtensorMap* mA = prob ? &tmA_1 : &tmA;
+      const CUtensorMap* mA2 = prob ? &tmA2_1 : &tmA2;
+      const CUtensorMap* mB = prob ? &tmB_1 : &tmB;
+      const Unit it = decode<MG>(p, u - (prob ? units0 : 0));
       const int mcnt = (it.row_end - it.row0 + BM - 1) / BM;
       // gemm1: gate block n of expert e and the up block I rows further (3-D map
       // [2E][I][K], z = 2e gate, 2e + 1 up); gemm2: w2 rows [256 n, +256) of expert e
@@ -401,13 +427,13 @@ __global__ void __launch_bounds__(Warps<kFP8>::THREADS, 1)
           mbar_arrive_expect_tx(&full[stage], mcnt * A_BYTES + 2 * B_HALF_BYTES);
           const int kx = kb * C::kBK;
           if (MG == 2 && mcnt == 2)
-            tma_load_2d(sA, &tmA2, kx, it.row0, &full[stage], pol_a);  // both M tiles, one 256-row box
+            tma_load_2d(sA, mA2, kx, it.row0, &full[stage], pol_a);  // both M tiles, one 256-row box
           else
-            tma_load_2d(sA, &tmA, kx, it.row0, &full[stage], pol_a);
+            tma_load_2d(sA, mA, kx, it.row0, &full[stage], pol_a);
           if (kPair)
-            tma_load_3d(sB, &tmB, kx, brow, 2 * it.e, &full[stage], pol_b);
+            tma_load_3d(sB, mB, kx, brow, 2 * it.e, &full[stage], pol_b);
           else
-            tma_load_2d(sB, &tmB, kx, brow, &full[stage], pol_b);
+            tma_load_2d(sB, mB, kx, brow, &full[stage], pol_b);
           if (l2_prefetch) {
             if (fills + 1 == STAGES) {
               for (int i = 0; i < STAGES; ++i) prefetch_next(false);
@@ -441,7 +467,8 @@ __global__ void __launch_bounds__(Warps<kFP8>::THREADS, 1)
     uint32_t acc_phase = 0;
     bool ok = true;
     while (ok && sched.next(u, kb0, kb1)) {
-      const Unit it = decode<MG>(p, u);
+      const int prob = u >= units0;
+      const Unit it = decode<MG>(pp.p[prob], u - (prob ? units0 : 0));
       const int mcnt = (it.row_end - it.row0 + BM - 1) / BM;
       if (!kFP8) {
         if (!(ok = warp_wait(&tempty[acc], acc_phase ^ 1))) break;
@@ -496,7 +523,7 @@ __global__ void __launch_bounds__(Warps<kFP8>::THREADS, 1)
     const int sub = q / 4;               // fp8: column half (bf16: always 0)
     const int r = quarter * 32 + lane;   // row within an M tile == TMEM lane
     const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
-    float* my_partial = p.partials + (size_t)blockIdx.x * C::PARTIAL_FLOATS;  // [MG][BM][BN] (bf16) / [BM][2][128] (fp8)
+    float* my_partial = p0.partials + (size_t)blockIdx.x * C::PARTIAL_FLOATS;  // [MG][BM][BN] (bf16) / [BM][2][128] (fp8)
     int acc = 0;
     uint32_t acc_phase = 0;
     int xbuf = 0;
@@ -504,7 +531,10 @@ __global__ void __launch_bounds__(Warps<kFP8>::THREADS, 1)
     long long sfill = 0;  // fp8: K blocks consumed from the scale ring
     bool ok = true;
     while (ok && sched.next(u, kb0, kb1)) {
-      const Unit it = decode<MG>(p, u);
+      const int prob = u >= units0;
+      const GemmParams& p = pp.p[prob];
+      const int lu = u - (prob ? units0 : 0);  // the unit within its problem (split flags)
+      const Unit it = decode<MG>(p, lu);
       const int prow = it.row0 + r;  // row of the first M tile (fp8: the only one)
       const bool valid = prow < it.row_end;
       // split-unit role: 0 whole, 1 first segment (finishes the unit), 2 later segment
@@ -532,7 +562,7 @@ __global__ void __launch_bounds__(Warps<kFP8>::THREADS, 1)
           // in segment order, every load independent, then the outputs are written.
           // Split units have one M tile.  Every epilogue warp arrives at both barrier
           // phases, whatever its status, so that none waits in vain.
-          ok = wait_split_partials(p.flags + u, (c_last - c_first + 1) * EPI_THREADS, fixbar);
+          ok = wait_split_partials(p.flags + lu, (c_last - c_first + 1) * EPI_THREADS, fixbar);
           const int nrows = min(BM, it.row_end - it.row0);
           const int tid = threadIdx.x - 64;
           const uint32_t tb = tmem + lane_addr + acc * BN;
@@ -702,7 +732,7 @@ __global__ void __launch_bounds__(Warps<kFP8>::THREADS, 1)
             }
           }
         }
-        if (role == 2) signal_split_partial(p.flags + u);
+        if (role == 2) signal_split_partial(p.flags + lu);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&tempty[acc]);
@@ -758,11 +788,11 @@ __global__ void __launch_bounds__(Warps<kFP8>::THREADS, 1)
             for (int j = 0; j < 32; ++j)
               __stcg(dst + j, make_float4(accv[4 * j], accv[4 * j + 1], accv[4 * j + 2], accv[4 * j + 3]));
           }
-          signal_split_partial(p.flags + u);
+          signal_split_partial(p.flags + lu);
           continue;
         }
         if (role == 1) {
-          ok = wait_split_partials(p.flags + u, (c_last - c_first + 1) * EPI_THREADS, fixbar);
+          ok = wait_split_partials(p.flags + lu, (c_last - c_first + 1) * EPI_THREADS, fixbar);
           if (!ok) break;
           if (valid) {
             for (int cc = c_first; cc <= c_last; ++cc) {
@@ -946,15 +976,17 @@ __device__ void build_groups(const int32_t* __restrict__ tile_map, int n, const 
   __syncthreads();
 }
 
-// plan: the group maps of both GEMMs and cleared split-unit flags.  One block.
+// plan: the two-tile group maps of the GEMMs that use them and cleared split-unit
+// flags (of every problem of the call).  One block.
 __global__ void __launch_bounds__(1024)
     plan_kernel(const int32_t* __restrict__ tile_map, const int32_t* __restrict__ num_tiles,
                 const int32_t* __restrict__ offsets, int mg1, int mg2, int32_t* __restrict__ gmap1,
                 int32_t* __restrict__ ngroups1, int32_t* __restrict__ gmap2, int32_t* __restrict__ ngroups2,
                 int* __restrict__ flags, int nflags) {
   const int n = *num_tiles;
-  build_groups(tile_map, n, offsets, mg1, gmap1, ngroups1);
-  build_groups(tile_map, n, offsets, mg2, gmap2, ngroups2);
+  // (a GEMM of one-tile units reads the tile map itself)
+  if (mg1 == 2) build_groups(tile_map, n, offsets, mg1, gmap1, ngroups1);
+  if (mg2 == 2) build_groups(tile_map, n, offsets, mg2, gmap2, ngroups2);
   for (int i = threadIdx.x; i < nflags; i += 1024) flags[i] = 0;
 }
 
@@ -1076,9 +1108,13 @@ bool make_map_gate_up(CUtensorMap* m, const void* base, bool fp8, long long k, l
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Tensor maps of one problem for one GEMM: A with one-tile and two-tile boxes, weights.
+struct GemmMaps {
+  CUtensorMap a, a2, b;
+};
+
 template <bool kFP8, int kKind, int kMG, int kAct, bool kHB16 = false>
-cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& a2, const CUtensorMap& b, const GemmParams& p, int grid,
-                        cudaStream_t s) {
+cudaError_t launch_gemm(const GemmMaps* m, const GemmProblems& pp, int grid, cudaStream_t s) {
   static int configured[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -1088,70 +1124,91 @@ cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& a2, const CUten
     if (e != cudaSuccess) return e;
     configured[dev] = 1;
   }
-  gemm_kernel<kFP8, kKind, kMG, kAct, kHB16><<<grid, Warps<kFP8>::THREADS, Cfg<kFP8, kMG>::SMEM_BYTES, s>>>(a, a2, b, p);
+  const GemmMaps& m1 = pp.nprob > 1 ? m[1] : m[0];
+  gemm_kernel<kFP8, kKind, kMG, kAct, kHB16><<<grid, Warps<kFP8>::THREADS, Cfg<kFP8, kMG>::SMEM_BYTES, s>>>(
+      m[0].a, m[0].a2, m[0].b, m1.a, m1.a2, m1.b, pp);
   return cudaGetLastError();
 }
 
 // gemm1 with the activation chosen at run time (kHB16: fp8 mainloop, bf16 h out)
 template <bool kFP8, int kMG, bool kHB16 = false>
-cudaError_t launch_gemm1(int act, const CUtensorMap& a, const CUtensorMap& a2, const CUtensorMap& b,
-                         const GemmParams& p, int grid, cudaStream_t s) {
+cudaError_t launch_gemm1(int act, const GemmMaps* m, const GemmProblems& pp, int grid, cudaStream_t s) {
   switch (act) {
-    case MOE_ACT_SILU: return launch_gemm<kFP8, kGemm1, kMG, MOE_ACT_SILU, kHB16>(a, a2, b, p, grid, s);
-    case MOE_ACT_GELU: return launch_gemm<kFP8, kGemm1, kMG, MOE_ACT_GELU, kHB16>(a, a2, b, p, grid, s);
-    case MOE_ACT_GELU_TANH: return launch_gemm<kFP8, kGemm1, kMG, MOE_ACT_GELU_TANH, kHB16>(a, a2, b, p, grid, s);
-    case MOE_ACT_SWIGLUOAI: return launch_gemm<kFP8, kGemm1, kMG, MOE_ACT_SWIGLUOAI, kHB16>(a, a2, b, p, grid, s);
-    case MOE_ACT_SILU_NO_MUL: return launch_gemm<kFP8, kGemm1, kMG, MOE_ACT_SILU_NO_MUL, kHB16>(a, a2, b, p, grid, s);
-    case MOE_ACT_GELU_NO_MUL: return launch_gemm<kFP8, kGemm1, kMG, MOE_ACT_GELU_NO_MUL, kHB16>(a, a2, b, p, grid, s);
+    case MOE_ACT_SILU: return launch_gemm<kFP8, kGemm1, kMG, MOE_ACT_SILU, kHB16>(m, pp, grid, s);
+    case MOE_ACT_GELU: return launch_gemm<kFP8, kGemm1, kMG, MOE_ACT_GELU, kHB16>(m, pp, grid, s);
+    case MOE_ACT_GELU_TANH: return launch_gemm<kFP8, kGemm1, kMG, MOE_ACT_GELU_TANH, kHB16>(m, pp, grid, s);
+    case MOE_ACT_SWIGLUOAI: return launch_gemm<kFP8, kGemm1, kMG, MOE_ACT_SWIGLUOAI, kHB16>(m, pp, grid, s);
+    case MOE_ACT_SILU_NO_MUL: return launch_gemm<kFP8, kGemm1, kMG, MOE_ACT_SILU_NO_MUL, kHB16>(m, pp, grid, s);
+    case MOE_ACT_GELU_NO_MUL: return launch_gemm<kFP8, kGemm1, kMG, MOE_ACT_GELU_NO_MUL, kHB16>(m, pp, grid, s);
   }
   return cudaErrorInvalidValue;
 }
 
-struct WsLayout {
-  size_t A, As, h, hs, hb, hamax, gmap, ngroups, gmap2, ngroups2, flags1, flags2, partials, total;
-  int s_pad, cap_groups, nflags1, nflags2;
-};
-
 inline size_t al256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Workspace of one call: per problem its gathered rows, transposed scales,
+// intermediate and group maps; then the split flags of every problem and GEMM,
+// contiguous so that one plan launch clears them; then one split partial per CTA.
+struct ProbLayout {
+  size_t A, As, h, hs, hb, hamax, gmap, ngroups, gmap2, ngroups2, flags1, flags2;
+  int s_pad, nflags1, nflags2;
+};
+struct WsLayout {
+  ProbLayout p[kMaxProblems];
+  size_t flags, partials, total;
+  int nflags;
+};
 
 // group: the fp8 activation format (128, MOE_GROUP_TOKEN or MOE_GROUP_TENSOR); the
 // "A"/"T" formats add the bf16 intermediate and the tensor format's amax word.
-WsLayout ws_layout(long long S, int H, int I, int E, bool fp8, int grid, int group) {
-  WsLayout L;
+WsLayout ws_layout(const moe_experts_problem* pr, int n, int H, bool fp8, int grid, int group) {
+  WsLayout L{};
   const int esz = fp8 ? 1 : 2;
   const int MG = fp8 ? 1 : 2;  // the larger bound of either GEMM
-  L.s_pad = (int)(((S + MG * BM + 3) / 4) * 4);
-  L.cap_groups = std::max(1, moe_tile_map_capacity((int)S, E, BM));  // a group holds at least one tile
-  L.nflags1 = L.cap_groups * (I / 128);
-  L.nflags2 = L.cap_groups * ((H + 255) / 256);
-  const size_t partial_floats = (size_t)MG * BM * BN;
   size_t off = 0;
-  L.A = off;
-  off = al256(off + (size_t)S * H * esz);
-  L.As = off;
-  off = al256(off + (fp8 ? (size_t)(H / 128) * L.s_pad * 4 : 0));
-  L.h = off;
-  off = al256(off + (size_t)S * I * esz);
-  L.hs = off;
-  off = al256(off + (fp8 ? (size_t)(I / 128) * L.s_pad * 4 : 0));
-  const bool hb16 = fp8 && group != 128;
-  L.hb = off;
-  off = al256(off + (hb16 ? (size_t)S * I * 2 : 0));
-  L.hamax = off;
-  off = al256(off + (hb16 ? 4 : 0));
-  L.gmap = off;
-  off = al256(off + (size_t)L.cap_groups * 2 * 4);
-  L.ngroups = off;
-  off = al256(off + 4);
-  L.gmap2 = off;
-  off = al256(off + (size_t)L.cap_groups * 2 * 4);
-  L.ngroups2 = off;
-  off = al256(off + 4);
-  L.flags1 = off;
-  L.flags2 = L.flags1 + (size_t)L.nflags1 * 4;
-  off = al256(off + (size_t)(L.nflags1 + L.nflags2) * 4);
+  L.nflags = 0;
+  for (int i = 0; i < n; ++i) {
+    ProbLayout& P = L.p[i];
+    const long long S = (long long)pr[i].T * pr[i].top_k;
+    const int I = pr[i].I, E = pr[i].E;
+    P.s_pad = (int)(((S + MG * BM + 3) / 4) * 4);
+    const int cap_groups = std::max(1, moe_tile_map_capacity((int)S, E, BM));  // a group holds at least one tile
+    P.nflags1 = cap_groups * (I / 128);
+    P.nflags2 = cap_groups * ((H + 255) / 256);
+    L.nflags += P.nflags1 + P.nflags2;
+    P.A = off;
+    off = al256(off + (size_t)S * H * esz);
+    P.As = off;
+    off = al256(off + (fp8 ? (size_t)(H / 128) * P.s_pad * 4 : 0));
+    P.h = off;
+    off = al256(off + (size_t)S * I * esz);
+    P.hs = off;
+    off = al256(off + (fp8 ? (size_t)(I / 128) * P.s_pad * 4 : 0));
+    const bool hb16 = fp8 && group != 128;
+    P.hb = off;
+    off = al256(off + (hb16 ? (size_t)S * I * 2 : 0));
+    P.hamax = off;
+    off = al256(off + (hb16 ? 4 : 0));
+    P.gmap = off;
+    off = al256(off + (size_t)cap_groups * 2 * 4);
+    P.ngroups = off;
+    off = al256(off + 4);
+    P.gmap2 = off;
+    off = al256(off + (size_t)cap_groups * 2 * 4);
+    P.ngroups2 = off;
+    off = al256(off + 4);
+  }
+  L.flags = off;
+  size_t f = off;
+  for (int i = 0; i < n; ++i) {
+    L.p[i].flags1 = f;
+    f += (size_t)L.p[i].nflags1 * 4;
+    L.p[i].flags2 = f;
+    f += (size_t)L.p[i].nflags2 * 4;
+  }
+  off = al256(f);
   L.partials = off;
-  off = al256(off + (size_t)grid * partial_floats * 4);
+  off = al256(off + (size_t)grid * MG * BM * BN * 4);
   L.total = off;
   return L;
 }
@@ -1159,6 +1216,206 @@ WsLayout ws_layout(long long S, int H, int I, int E, bool fp8, int grid, int gro
 // Grid of the persistent GEMMs: one CTA per SM (the workspace holds one
 // split-unit partial per CTA, so its size depends on this).
 int gemm_grid() { return num_sms(); }
+
+bool quant_ok(const moe_quant_config* qc) {
+  if (qc->act == MOE_DT_FP8_E4M3)
+    return (qc->act_group == 128 || qc->act_group == MOE_GROUP_TOKEN || qc->act_group == MOE_GROUP_TENSOR) &&
+           qc->weight == MOE_DT_FP8_E4M3 && qc->w_block_n == 128 && qc->w_block_k == 128;
+  return qc->act == MOE_DT_BF16 && qc->weight == MOE_DT_BF16;
+}
+
+// The experts of one or more problems in the same launches.
+moe_status_t experts_run(const moe_experts_problem* probs, int nprob, int H, const moe_quant_config* qc,
+                         int activation, void* ws, size_t ws_bytes, cudaStream_t s) {
+  MOE_CHECK_ARG(qc && probs && nprob >= 1 && nprob <= kMaxProblems && H > 0);
+  if (activation < MOE_ACT_SILU || activation > MOE_ACT_GELU_NO_MUL || !quant_ok(qc)) return MOE_ERR_UNSUPPORTED;
+  const bool no_mul = activation == MOE_ACT_SILU_NO_MUL || activation == MOE_ACT_GELU_NO_MUL;
+  const bool fp8 = qc->act == MOE_DT_FP8_E4M3;
+  const int group = qc->act_group;
+  const bool hb16 = fp8 && group != 128;  // "A"/"T": bf16 h, then quantised per row or per tensor
+  MOE_CHECK_ARG(H % 128 == 0 && fits_int32((long long)H * 8));
+  // the problems with rows; several share the launches only in bf16 and with one K depth per GEMM
+  moe_experts_problem pr[kMaxProblems];
+  int n = 0;
+  for (int i = 0; i < nprob; ++i) {
+    const moe_experts_problem& q = probs[i];
+    MOE_CHECK_ARG(q.T >= 0 && q.I > 0 && q.I % 128 == 0 && q.E >= 1 && q.top_k >= 1 && q.top_k <= q.E);
+    const long long S = (long long)q.T * q.top_k;
+    MOE_CHECK_ARG(fits_int32(S + 4 * BM) && fits_int32((long long)q.E * 2 * q.I) && fits_int32((long long)q.E * H));
+    if (S == 0) continue;
+    MOE_CHECK_ARG(q.a1q && q.w13 && q.w2 && q.expert_offsets && q.tile_map && q.num_tiles && q.fused_expert_output);
+    MOE_CHECK_ARG(q.sorted_slot || (q.E == 1 && q.top_k == 1));
+    MOE_CHECK_ARG(!fp8 || (q.a1q_scale && q.w13_scale && q.w2_scale));
+    MOE_CHECK_ARG(aligned16(q.a1q) && aligned16(q.w13) && aligned16(q.w2) && aligned16(q.fused_expert_output));
+    pr[n++] = q;
+  }
+  if (n == 0) return MOE_OK;
+  if (n > 1 && (fp8 || pr[0].I != pr[1].I)) return MOE_ERR_UNSUPPORTED;
+  const int grid = gemm_grid();
+  const WsLayout L = ws_layout(pr, n, H, fp8, grid, group);
+  if (!ws || ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+  MOE_CHECK_ARG(aligned16(ws));
+  uint8_t* wsb = static_cast<uint8_t*>(ws);
+  const int esz = fp8 ? 1 : 2;
+  const int nt1 = no_mul ? (pr[0].I + 255) / 256 : pr[0].I / 128;  // gemm1 N tiles: 256 gate rows, or 128 gate + 128 up
+
+  // Tiles per unit (host estimate of the unit count from the tile-map bound):
+  // one tile per unit, dealt round-robin so tiles sharing a weight tile run side
+  // by side -- unless two-tile units of full tiles fill between half a wave and
+  // one wave (a deep-K GEMM2): then each weight tile is read once, all units in
+  // one wave.  fp8 and several problems use one tile (the fp8 register promotion
+  // holds one).  Decode-sized problems (at most 16 slots per expert, K of 32+
+  // blocks) may split units across CTAs when there are too few of them for the SMs.
+  int mg1 = 1, mg2 = 1;
+  bool allow_split = !fp8;
+  for (int i = 0; i < n; ++i) allow_split = allow_split && (long long)pr[i].T * pr[i].top_k <= 16LL * pr[i].E;
+  if (n == 1 && !fp8) {
+    const long long S = (long long)pr[0].T * pr[0].top_k;
+    const int cap_tiles = std::max(1, moe_tile_map_capacity((int)S, pr[0].E, BM));
+    const bool full_tiles = S >= (long long)BM * pr[0].E;  // experts average a full 128-row tile or more
+    auto mg_for = [&](int nt) {
+      const long long units2 = (long long)((cap_tiles + 1) / 2) * nt;  // estimate with two tiles per unit
+      return (full_tiles && 2 * units2 >= grid && units2 <= grid) ? 2 : 1;
+    };
+    mg1 = mg_for(nt1);
+    mg2 = mg_for((H + 255) / 256);
+  }
+  const bool split1 = allow_split && H / 64 >= 32, split2 = allow_split && pr[0].I / 64 >= 32;
+
+  GemmMaps maps1[kMaxProblems], maps2[kMaxProblems];
+  GemmProblems g1 = {}, g2 = {};
+  g1.nprob = g2.nprob = n;
+  int* flags_all = reinterpret_cast<int*>(wsb + L.flags);
+  if (mg1 == 2 || mg2 == 2 || split1 || split2) {
+    // clears every problem's flags; builds problem 0's two-tile group maps (n == 1 when mg > 1)
+    const ProbLayout& P = L.p[0];
+    plan_kernel<<<1, 1024, 0, s>>>(pr[0].tile_map, pr[0].num_tiles, pr[0].expert_offsets, mg1, mg2,
+                                   reinterpret_cast<int32_t*>(wsb + P.gmap), reinterpret_cast<int32_t*>(wsb + P.ngroups),
+                                   reinterpret_cast<int32_t*>(wsb + P.gmap2), reinterpret_cast<int32_t*>(wsb + P.ngroups2),
+                                   flags_all, L.nflags);
+    if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  for (int i = 0; i < n; ++i) {
+    const moe_experts_problem& q = pr[i];
+    const ProbLayout& P = L.p[i];
+    const long long S = (long long)q.T * q.top_k;
+    const int I = q.I, E = q.E;
+    const bool gather_rows = q.sorted_slot != nullptr;
+    const void* A = gather_rows ? (const void*)(wsb + P.A) : q.a1q;
+    float* As = fp8 ? reinterpret_cast<float*>(wsb + P.As) : nullptr;
+    void* h = wsb + P.h;
+    float* hs = fp8 ? reinterpret_cast<float*>(wsb + P.hs) : nullptr;
+    if (gather_rows || fp8) {
+      const unsigned gb = (unsigned)((S + 7) / 8);
+      gather_kernel<<<gb, 256, 0, s>>>(static_cast<const uint8_t*>(q.a1q), q.a1q_scale, q.sorted_slot, (int)S,
+                                       q.top_k, H * esz, hb16 ? 1 : H / 128, gather_rows ? wsb + P.A : nullptr, As,
+                                       P.s_pad, group == 128 ? H / 128 : (group == MOE_GROUP_TOKEN ? 1 : 0));
+      if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+    }
+    // A maps with one-tile and two-tile boxes; weight maps with 256-row boxes (gemm2:
+    // the last N tile of an expert with H % 256 == 128 reads 128 rows past it, which
+    // land in discarded output columns, zero-filled past the last expert)
+    const bool b1_ok = no_mul ? make_map(&maps1[i].b, q.w13, fp8, H, (long long)E * I, 256)
+                              : make_map_gate_up(&maps1[i].b, q.w13, fp8, H, I, E);
+    if (!b1_ok || !make_map(&maps1[i].a, A, fp8, H, S, 128) || !make_map(&maps1[i].a2, A, fp8, H, S, 256) ||
+        !make_map(&maps2[i].a, h, fp8, I, S, 128) || !make_map(&maps2[i].a2, h, fp8, I, S, 256) ||
+        !make_map(&maps2[i].b, q.w2, fp8, I, (long long)E * H, 256))
+      return MOE_ERR_CUDA;
+
+    GemmParams& p1 = g1.p[i];
+    p1.offsets = q.expert_offsets;
+    p1.group_map = mg1 == 2 ? reinterpret_cast<int32_t*>(wsb + P.gmap) : q.tile_map;
+    p1.num_groups = mg1 == 2 ? reinterpret_cast<int32_t*>(wsb + P.ngroups) : q.num_tiles;
+    p1.sorted_slot = q.sorted_slot;
+    p1.K = H;
+    p1.NT = nt1;
+    p1.I = I;
+    p1.H = H;
+    p1.b_rows = no_mul ? I : 2 * I;
+    p1.s_pad = P.s_pad;
+    p1.a_kstride = hb16 ? 0 : P.s_pad;  // "A"/"T": one scale per row for every K block
+    p1.a_scale_t = As;
+    p1.w_scale = q.w13_scale;
+    p1.out = hb16 ? (void*)(wsb + P.hb) : h;
+    p1.out_scale_t = hb16 ? nullptr : hs;
+    p1.flags = reinterpret_cast<int*>(wsb + P.flags1);
+    p1.partials = reinterpret_cast<float*>(wsb + L.partials);
+    p1.allow_split = split1;
+
+    GemmParams& p2 = g2.p[i];
+    p2 = p1;
+    p2.group_map = mg2 == 2 ? reinterpret_cast<int32_t*>(wsb + P.gmap2) : q.tile_map;
+    p2.num_groups = mg2 == 2 ? reinterpret_cast<int32_t*>(wsb + P.ngroups2) : q.num_tiles;
+    p2.K = I;
+    p2.NT = (H + 255) / 256;
+    p2.b_rows = H;
+    p2.a_scale_t = hs;
+    p2.w_scale = q.w2_scale;
+    p2.out = q.fused_expert_output;
+    p2.out_scale_t = nullptr;
+    p2.flags = reinterpret_cast<int*>(wsb + P.flags2);
+    p2.allow_split = split2;  // (K of at least 32 blocks for a split to pay)
+  }
+
+  cudaError_t e;
+  if (fp8) {  // one problem
+    const moe_experts_problem& q = pr[0];
+    const ProbLayout& P = L.p[0];
+    e = hb16 ? launch_gemm1<true, 1, true>(activation, maps1, g1, grid, s)
+             : launch_gemm1<true, 1>(activation, maps1, g1, grid, s);
+    if (e == cudaSuccess && hb16) {
+      const long long S = (long long)q.T * q.top_k;
+      const auto* hbp = reinterpret_cast<const __nv_bfloat16*>(wsb + P.hb);
+      uint8_t* hq = wsb + P.h;
+      float* hs = reinterpret_cast<float*>(wsb + P.hs);
+      if (group == MOE_GROUP_TOKEN) {
+        hquant_token_kernel<<<(unsigned)S, 256, 0, s>>>(hbp, q.I, q.expert_offsets, q.E, hq, hs);
+      } else {
+        unsigned* amax = reinterpret_cast<unsigned*>(wsb + P.hamax);
+        e = cudaMemsetAsync(amax, 0, sizeof(unsigned), s);
+        const long long nvec = S * (q.I / 8);
+        const unsigned gb = (unsigned)((nvec + 255) / 256);
+        if (e == cudaSuccess) {
+          hquant_tensor_amax_kernel<<<std::min<unsigned>(gb, 4u * grid), 256, 0, s>>>(hbp, q.I, q.expert_offsets, q.E,
+                                                                                     amax);
+          hquant_tensor_kernel<<<gb, 256, 0, s>>>(hbp, q.I, q.expert_offsets, q.E, amax, hq, hs);
+        }
+      }
+      if (e == cudaSuccess) e = cudaGetLastError();
+    }
+    if (e == cudaSuccess) e = launch_gemm<true, kGemm2, 1, 0>(maps2, g2, grid, s);
+  } else {
+    e = mg1 == 1 ? launch_gemm1<false, 1>(activation, maps1, g1, grid, s)
+                 : launch_gemm1<false, 2>(activation, maps1, g1, grid, s);
+    if (e == cudaSuccess)
+      e = mg2 == 1 ? launch_gemm<false, kGemm2, 1, 0>(maps2, g2, grid, s)
+                   : launch_gemm<false, kGemm2, 2, 0>(maps2, g2, grid, s);
+  }
+  return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+moe_experts_problem one_problem(const void* a1q, const float* a1q_scale, const void* w13, const float* w13_scale,
+                                const void* w2, const float* w2_scale, const int32_t* expert_offsets,
+                                const int32_t* sorted_slot, const int32_t* tile_map, const int32_t* num_tiles, int T,
+                                int I, int E, int top_k, void* out) {
+  moe_experts_problem q;
+  q.a1q = a1q;
+  q.a1q_scale = a1q_scale;
+  q.w13 = w13;
+  q.w13_scale = w13_scale;
+  q.w2 = w2;
+  q.w2_scale = w2_scale;
+  q.expert_offsets = expert_offsets;
+  q.sorted_slot = sorted_slot;
+  q.tile_map = tile_map;
+  q.num_tiles = num_tiles;
+  q.T = T;
+  q.I = I;
+  q.E = E;
+  q.top_k = top_k;
+  q.fused_expert_output = out;
+  return q;
+}
 
 }  // namespace
 
@@ -1170,7 +1427,23 @@ using namespace moe;
 
 extern "C" size_t moe_workspace_size(int T, int H, int I, int E, int top_k, const moe_quant_config* qc) {
   if (!qc || T < 0 || H <= 0 || I <= 0 || E < 1 || top_k < 1) return 0;
-  return ws_layout((long long)T * top_k, H, I, E, qc->act == MOE_DT_FP8_E4M3, gemm_grid(), qc->act_group).total;
+  const moe_experts_problem q = one_problem(nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
+                                            nullptr, nullptr, T, I, E, top_k, nullptr);
+  return ws_layout(&q, 1, H, qc->act == MOE_DT_FP8_E4M3, gemm_grid(), qc->act_group).total;
+}
+
+extern "C" size_t moe_workspace_size_multi(const moe_experts_problem* problems, int num_problems, int H,
+                                           const moe_quant_config* qc) {
+  if (!qc || !problems || num_problems < 1 || num_problems > kMaxProblems || H <= 0) return 0;
+  for (int i = 0; i < num_problems; ++i)
+    if (problems[i].T < 0 || problems[i].I <= 0 || problems[i].E < 1 || problems[i].top_k < 1) return 0;
+  return ws_layout(problems, num_problems, H, qc->act == MOE_DT_FP8_E4M3, gemm_grid(), qc->act_group).total;
+}
+
+extern "C" moe_status_t moe_experts_multi(const moe_experts_problem* problems, int num_problems, int H,
+                                          const moe_quant_config* qc, int activation, void* ws, size_t ws_bytes,
+                                          moe_stream_t stream) {
+  return experts_run(problems, num_problems, H, qc, activation, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
 }
 
 extern "C" moe_status_t moe_experts_act(const void* a1q, const float* a1q_scale, const void* w13,
@@ -1179,156 +1452,9 @@ extern "C" moe_status_t moe_experts_act(const void* a1q, const float* a1q_scale,
                                         const int32_t* tile_map, const int32_t* num_tiles, int T, int H, int I, int E,
                                         int top_k, const moe_quant_config* qc, int activation,
                                         void* fused_expert_output, void* ws, size_t ws_bytes, moe_stream_t stream) {
-  MOE_CHECK_ARG(qc && T >= 0 && H > 0 && I > 0 && E >= 1 && top_k >= 1 && top_k <= E);
-  if (activation < MOE_ACT_SILU || activation > MOE_ACT_GELU_NO_MUL) return MOE_ERR_UNSUPPORTED;
-  const bool no_mul = activation == MOE_ACT_SILU_NO_MUL || activation == MOE_ACT_GELU_NO_MUL;
-  const int nt1 = no_mul ? (I + 255) / 256 : I / 128;  // gemm1 N tiles: 256 gate rows, or 128 gate + 128 up
-  const bool fp8 = qc->act == MOE_DT_FP8_E4M3;
-  const int group = qc->act_group;
-  if (fp8) {
-    if ((group != 128 && group != MOE_GROUP_TOKEN && group != MOE_GROUP_TENSOR) || qc->weight != MOE_DT_FP8_E4M3 ||
-        qc->w_block_n != 128 || qc->w_block_k != 128)
-      return MOE_ERR_UNSUPPORTED;
-  } else if (qc->act != MOE_DT_BF16 || qc->weight != MOE_DT_BF16) {
-    return MOE_ERR_UNSUPPORTED;
-  }
-  MOE_CHECK_ARG(H % 128 == 0 && I % 128 == 0);
-  const long long S = (long long)T * top_k;
-  MOE_CHECK_ARG(fits_int32(S + 4 * BM) && fits_int32((long long)E * 2 * I) && fits_int32((long long)E * H));
-  if (S == 0) return MOE_OK;
-  MOE_CHECK_ARG(a1q && w13 && w2 && expert_offsets && tile_map && num_tiles && fused_expert_output);
-  MOE_CHECK_ARG(sorted_slot || (E == 1 && top_k == 1));
-  MOE_CHECK_ARG(!fp8 || (a1q_scale && w13_scale && w2_scale));
-  MOE_CHECK_ARG(aligned16(a1q) && aligned16(w13) && aligned16(w2) && aligned16(fused_expert_output));
-  const int grid = gemm_grid();
-  const WsLayout L = ws_layout(S, H, I, E, fp8, grid, group);
-  const bool hb16 = fp8 && group != 128;  // "A"/"T": bf16 h, then quantised per row or per tensor
-  if (!ws || ws_bytes < L.total) return MOE_ERR_WORKSPACE;
-  MOE_CHECK_ARG(aligned16(ws));
-
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  uint8_t* wsb = static_cast<uint8_t*>(ws);
-  const int esz = fp8 ? 1 : 2;
-  const bool gather_rows = sorted_slot != nullptr;
-  const void* A = gather_rows ? (const void*)(wsb + L.A) : a1q;
-  float* As = fp8 ? reinterpret_cast<float*>(wsb + L.As) : nullptr;
-  void* h = wsb + L.h;
-  float* hs = fp8 ? reinterpret_cast<float*>(wsb + L.hs) : nullptr;
-  int32_t* gmap = reinterpret_cast<int32_t*>(wsb + L.gmap);
-  int32_t* ngroups = reinterpret_cast<int32_t*>(wsb + L.ngroups);
-  int* flags1 = reinterpret_cast<int*>(wsb + L.flags1);
-  int* flags2 = reinterpret_cast<int*>(wsb + L.flags2);
-  float* partials = reinterpret_cast<float*>(wsb + L.partials);
-
-  // Tiles per unit (host estimate of the unit count from the tile-map bound):
-  // one tile per unit, dealt round-robin so tiles sharing a weight tile run side
-  // by side -- unless two-tile units of full tiles fill between half a wave and
-  // one wave (a deep-K GEMM2): then each weight tile is read once, all units in
-  // one wave.  fp8 always uses one tile (its register promotion holds one).
-  // Decode-sized problems (at most 16 slots per expert, K of 32+ blocks) may
-  // split units across CTAs when there are too few of them for the SMs.
-  const int cap_tiles = std::max(1, moe_tile_map_capacity((int)S, E, BM));
-  const int grid_sms = grid;
-  const bool full_tiles = S >= (long long)BM * E;  // experts average a full 128-row tile or more
-  auto mg_for = [&](int nt) {
-    const long long units2 = (long long)((cap_tiles + 1) / 2) * nt;  // estimate with two tiles per unit
-    return (!fp8 && full_tiles && 2 * units2 >= grid_sms && units2 <= grid_sms) ? 2 : 1;
-  };
-  const int mg1 = mg_for(nt1), mg2 = mg_for((H + 255) / 256);
-  int32_t* gmap2 = reinterpret_cast<int32_t*>(wsb + L.gmap2);
-  int32_t* ngroups2 = reinterpret_cast<int32_t*>(wsb + L.ngroups2);
-  const bool allow_split = !fp8 && S <= 16LL * E;  // decode-sized: units may be split across CTAs
-  const bool split1 = allow_split && H / (fp8 ? 128 : 64) >= 32, split2 = allow_split && I / (fp8 ? 128 : 64) >= 32;
-  if (mg1 == 2 || mg2 == 2 || split1 || split2) {
-    plan_kernel<<<1, 1024, 0, s>>>(tile_map, num_tiles, expert_offsets, mg1, mg2, gmap, ngroups, gmap2, ngroups2,
-                                   flags1, L.nflags1 + L.nflags2);
-    if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
-  } else {
-    // one tile per unit and no split: the tile map is the group map
-    gmap = gmap2 = const_cast<int32_t*>(tile_map);
-    ngroups = ngroups2 = const_cast<int32_t*>(num_tiles);
-  }
-  if (gather_rows || fp8) {
-    const unsigned g = (unsigned)((S + 7) / 8);
-    gather_kernel<<<g, 256, 0, s>>>(static_cast<const uint8_t*>(a1q), a1q_scale, sorted_slot, (int)S, top_k, H * esz,
-                                    hb16 ? 1 : H / 128, gather_rows ? wsb + L.A : nullptr, As, L.s_pad,
-                                    group == 128 ? H / 128 : (group == MOE_GROUP_TOKEN ? 1 : 0));
-    if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
-  }
-
-  // A maps with one-tile and two-tile boxes; weight maps with 256-row boxes (gemm2:
-  // the last N tile of an expert with H % 256 == 128 reads 128 rows past it, which
-  // land in discarded output columns, zero-filled past the last expert)
-  CUtensorMap mA1, mA1x2, mB1, mA2, mA2x2, mB2;
-  const bool b1_ok = no_mul ? make_map(&mB1, w13, fp8, H, (long long)E * I, 256) : make_map_gate_up(&mB1, w13, fp8, H, I, E);
-  if (!make_map(&mA1, A, fp8, H, S, 128) || !make_map(&mA1x2, A, fp8, H, S, 256) || !b1_ok ||
-      !make_map(&mA2, h, fp8, I, S, 128) ||
-      !make_map(&mA2x2, h, fp8, I, S, 256) || !make_map(&mB2, w2, fp8, I, (long long)E * H, 256))
-    return MOE_ERR_CUDA;
-
-  GemmParams p1 = {};
-  p1.offsets = expert_offsets;
-  p1.group_map = gmap;
-  p1.num_groups = ngroups;
-  p1.sorted_slot = sorted_slot;
-  p1.K = H;
-  p1.NT = nt1;
-  p1.I = I;
-  p1.H = H;
-  p1.b_rows = no_mul ? I : 2 * I;
-  p1.s_pad = L.s_pad;
-  p1.a_kstride = hb16 ? 0 : L.s_pad;  // "A"/"T": one scale per row for every K block
-  p1.a_scale_t = As;
-  p1.w_scale = w13_scale;
-  p1.out = hb16 ? (void*)(wsb + L.hb) : h;
-  p1.out_scale_t = hb16 ? nullptr : hs;
-  p1.flags = flags1;
-  p1.partials = partials;
-  p1.allow_split = split1;
-
-  GemmParams p2 = p1;
-  p2.group_map = gmap2;
-  p2.num_groups = ngroups2;
-  p2.K = I;
-  p2.NT = (H + 255) / 256;
-  p2.b_rows = H;
-  p2.a_scale_t = hs;
-  p2.w_scale = w2_scale;
-  p2.out = fused_expert_output;
-  p2.out_scale_t = nullptr;
-  p2.flags = flags2;
-  p2.allow_split = split2;  // (K of at least 32 blocks for a split to pay)
-
-  cudaError_t e;
-  if (fp8) {
-    e = hb16 ? launch_gemm1<true, 1, true>(activation, mA1, mA1x2, mB1, p1, grid, s)
-             : launch_gemm1<true, 1>(activation, mA1, mA1x2, mB1, p1, grid, s);
-    if (e == cudaSuccess && hb16) {
-      const auto* hbp = reinterpret_cast<const __nv_bfloat16*>(wsb + L.hb);
-      uint8_t* hq = static_cast<uint8_t*>(h);
-      if (group == MOE_GROUP_TOKEN) {
-        hquant_token_kernel<<<(unsigned)S, 256, 0, s>>>(hbp, I, expert_offsets, E, hq, hs);
-      } else {
-        unsigned* amax = reinterpret_cast<unsigned*>(wsb + L.hamax);
-        e = cudaMemsetAsync(amax, 0, sizeof(unsigned), s);
-        const long long nvec = S * (I / 8);
-        const unsigned g = (unsigned)((nvec + 255) / 256);
-        if (e == cudaSuccess) {
-          hquant_tensor_amax_kernel<<<std::min<unsigned>(g, 4u * grid), 256, 0, s>>>(hbp, I, expert_offsets, E, amax);
-          hquant_tensor_kernel<<<g, 256, 0, s>>>(hbp, I, expert_offsets, E, amax, hq, hs);
-        }
-      }
-      if (e == cudaSuccess) e = cudaGetLastError();
-    }
-    if (e == cudaSuccess) e = launch_gemm<true, kGemm2, 1, 0>(mA2, mA2x2, mB2, p2, grid, s);
-  } else {
-    e = mg1 == 1 ? launch_gemm1<false, 1>(activation, mA1, mA1x2, mB1, p1, grid, s)
-                 : launch_gemm1<false, 2>(activation, mA1, mA1x2, mB1, p1, grid, s);
-    if (e == cudaSuccess)
-      e = mg2 == 1 ? launch_gemm<false, kGemm2, 1, 0>(mA2, mA2x2, mB2, p2, grid, s)
-                   : launch_gemm<false, kGemm2, 2, 0>(mA2, mA2x2, mB2, p2, grid, s);
-  }
-  return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  const moe_experts_problem q = one_problem(a1q, a1q_scale, w13, w13_scale, w2, w2_scale, expert_offsets, sorted_slot,
+                                            tile_map, num_tiles, T, I, E, top_k, fused_expert_output);
+  return experts_run(&q, 1, H, qc, activation, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
 }
 
 extern "C" moe_status_t moe_experts(const void* a1q, const float* a1q_scale, const void* w13, const float* w13_scale,

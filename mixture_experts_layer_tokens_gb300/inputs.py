@@ -49,6 +49,7 @@ class LayerConfig:
     residual: bool = False
     rms: bool = False
     nvfp4: bool = False
+    activation: str = "silu"       # between the expert GEMMs; *_no_mul: w13 holds I rows
     description: str = ""
 
 
@@ -70,6 +71,15 @@ def _cfgs():
     # experts: a small case for detailed profiles of the fp8 kernels
     c["deepseek_e64"] = LayerConfig("deepseek_e64", 1024, 7168, 2048, 64, 8, quant="fp8", shared_I=2048,
                                     description="DeepSeek-V3-shaped experts T1024 H7168 I2048 E64 top8 fp8 + bf16 shared")
+    # the per-token ("A") and per-tensor ("T") activation formats on the same shape
+    for q in ("token", "tensor"):
+        c[f"deepseek_e64_{q}"] = LayerConfig(f"deepseek_e64_{q}", 1024, 7168, 2048, 64, 8, quant=f"fp8_{q}",
+                                             shared_I=2048,
+                                             description=f"DeepSeek-V3-shaped experts T1024 H7168 I2048 E64 top8 fp8 "
+                                                         f"per-{q} activation scales + bf16 shared")
+    c["mixtral_swigluoai"] = LayerConfig("mixtral_swigluoai", 512, 4096, 14336, 8, 2, activation="swigluoai",
+                                         description="Mixtral-8x7B-like layer T512 H4096 I14336 E8 top2 bf16, "
+                                                     "clamped SwiGLU (swigluoai)")
     for T in (128, 512):
         c[f"finalize{T}"] = LayerConfig(f"finalize{T}", T, 7168, 0, 256, 4, finalize_only=True,
                                         residual=True, rms=True, nvfp4=True, shared_I=1,
@@ -159,11 +169,12 @@ def make_inputs(cfg: LayerConfig, seed: int = 0, device="cpu") -> LayerInputs:
     logits = torch.randn((T, E), generator=gen, device=dev, dtype=torch.float32)
     a1 = torch.randn((T, H), generator=gen, device=dev).to(torch.bfloat16)
     inp = LayerInputs(cfg, logits, a1=a1)
+    rows13 = I if cfg.activation.endswith("_no_mul") else 2 * I
     if cfg.quant != "bf16":
-        inp.w13, inp.w13_scale = _fp8_weights(gen, E, 2 * I, H, dev)
+        inp.w13, inp.w13_scale = _fp8_weights(gen, E, rows13, H, dev)
         inp.w2, inp.w2_scale = _fp8_weights(gen, E, H, I, dev)
     else:
-        inp.w13 = _bf16_weights(gen, E, 2 * I, H, dev)
+        inp.w13 = _bf16_weights(gen, E, rows13, H, dev)
         inp.w2 = _bf16_weights(gen, E, H, I, dev)
     if cfg.shared_I:
         inp.shared_w13 = _bf16_weights(gen, 1, 2 * cfg.shared_I, H, dev)

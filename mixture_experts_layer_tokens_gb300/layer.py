@@ -45,6 +45,15 @@ class MoELayer:
             self.al_shared = moe.moe_align(ids0, 1, stream=stream)
             self.ws_shared = torch.empty(max(moe.workspace_size(T, H, cfg.shared_I, 1, 1, "bf16"), 16),
                                          dtype=torch.uint8, device=dev)
+        # a bf16 layer whose shared expert has the routed experts' I and activation runs both
+        # in the same GEMM launches (moe_experts_multi)
+        self.fused_shared = (cfg.shared_I == I and cfg.quant == "bf16" and cfg.activation == "silu")
+        if self.fused_shared:
+            a_dummy = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+            self.ws_multi = torch.empty(max(moe.workspace_size_multi(
+                [moe.experts_problem(a_dummy, None, inp.w13, None, inp.w2, None, self.al, self.y),
+                 moe.experts_problem(a_dummy, None, inp.shared_w13, None, inp.shared_w2, None, self.al_shared,
+                                     self.shared, identity=True)], H, "bf16"), 16), dtype=torch.uint8, device=dev)
 
     def forward(self, logits: torch.Tensor, a1: torch.Tensor, stream=None) -> torch.Tensor:
         cfg, inp = self.cfg, self.inp
@@ -55,15 +64,28 @@ class MoELayer:
         else:
             a1q, a1q_scale = moe.moe_prepare(a1, self.topk_weights, cfg.top_k, cfg.weight_on_input, cfg.quant,
                                              self.a1q, self.a1q_scale, stream=stream)
-        moe.moe_experts(a1q, a1q_scale, inp.w13, inp.w13_scale, inp.w2, inp.w2_scale, self.al, cfg.quant,
-                        out=self.y, ws=self.ws, stream=stream)
-        shared = None
-        if self.shared is not None:
-            shared = moe.moe_experts(a1, None, inp.shared_w13, None, inp.shared_w2, None, self.al_shared, "bf16",
-                                     out=self.shared, ws=self.ws_shared, identity=True, stream=stream)
+        shared = self.experts(a1q, a1q_scale, a1, stream)
         moe.moe_finalize(self.y, self.topk_weights, cfg.top_k, cfg.weight_on_input, shared=shared,
                          residual=inp.residual, rms_weight=inp.rms_weight, output=self.out, stream=stream)
         return self.out
+
+    def experts(self, a1q, a1q_scale, a1, stream=None):
+        """The routed experts into self.y and the shared expert (if any) into
+        self.shared -- one moe_experts_multi call when they can share launches.
+        Returns the shared-expert rows or None."""
+        cfg, inp = self.cfg, self.inp
+        if self.shared is not None and self.fused_shared:
+            moe.moe_experts_multi(
+                [moe.experts_problem(a1q, a1q_scale, inp.w13, inp.w13_scale, inp.w2, inp.w2_scale, self.al, self.y),
+                 moe.experts_problem(a1, None, inp.shared_w13, None, inp.shared_w2, None, self.al_shared, self.shared,
+                                     identity=True)], cfg.H, "bf16", self.ws_multi, stream=stream)
+            return self.shared
+        moe.moe_experts(a1q, a1q_scale, inp.w13, inp.w13_scale, inp.w2, inp.w2_scale, self.al, cfg.quant,
+                        activation=cfg.activation, out=self.y, ws=self.ws, stream=stream)
+        if self.shared is None:
+            return None
+        return moe.moe_experts(a1, None, inp.shared_w13, None, inp.shared_w2, None, self.al_shared, "bf16",
+                               out=self.shared, ws=self.ws_shared, identity=True, stream=stream)
 
 
 class FinalizeStep:

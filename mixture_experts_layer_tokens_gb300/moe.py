@@ -56,6 +56,18 @@ def scale_shape(quant: str, T: int, H: int):
     return {"bf16": None, "fp8": (T, H // 128), "fp8_token": (T,), "fp8_tensor": (1,)}[quant]
 _QCP = ctypes.POINTER(QuantConfig)
 
+
+class ExpertsProblem(ctypes.Structure):
+    """moe_experts_problem: one expert problem of a moe_experts_multi call."""
+    _fields_ = [("a1q", ctypes.c_void_p), ("a1q_scale", ctypes.c_void_p), ("w13", ctypes.c_void_p),
+                ("w13_scale", ctypes.c_void_p), ("w2", ctypes.c_void_p), ("w2_scale", ctypes.c_void_p),
+                ("expert_offsets", ctypes.c_void_p), ("sorted_slot", ctypes.c_void_p), ("tile_map", ctypes.c_void_p),
+                ("num_tiles", ctypes.c_void_p), ("T", ctypes.c_int), ("I", ctypes.c_int), ("E", ctypes.c_int),
+                ("top_k", ctypes.c_int), ("fused_expert_output", ctypes.c_void_p)]
+
+
+_EPP = ctypes.POINTER(ExpertsProblem)
+
 SIGNATURES = {
     "moe_route": ([_P, _I, _I, _I, _I, _P, _P, _P], _I),
     "moe_align": ([_P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _Z, _P], _I),
@@ -65,6 +77,8 @@ SIGNATURES = {
     "moe_prepare": ([_P, _P, _P, _I, _I, _I, _I, _QCP, _P, _P, _P], _I),
     "moe_experts": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _QCP, _P, _P, _Z, _P], _I),
     "moe_experts_act": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _QCP, _I, _P, _P, _Z, _P], _I),
+    "moe_experts_multi": ([_EPP, _I, _I, _QCP, _I, _P, _Z, _P], _I),
+    "moe_workspace_size_multi": ([_EPP, _I, _I, _QCP], _Z),
     "moe_workspace_size": ([_I, _I, _I, _I, _I, _QCP], _Z),
     "moe_finalize": ([_P, _P, _P, _P, _P, _P, _P, _F, _I, _I, _I, _I, _I, _P, _F, _P, _P], _I),
     "moe_device_status": ([_I], _I),
@@ -252,6 +266,37 @@ def moe_experts(a1q: torch.Tensor, a1q_scale: Optional[torch.Tensor], w13: torch
         None if identity else _ptr(al.sorted_slot), _ptr(al.tile_map), _ptr(al.num_tiles), T, H, I, E, k,
         ctypes.byref(qc), ACTIVATIONS[activation], _ptr(out), _ptr(ws), ws.numel(), _stream(stream)))
     return out
+
+
+def experts_problem(a1q: torch.Tensor, a1q_scale: Optional[torch.Tensor], w13: torch.Tensor,
+                    w13_scale: Optional[torch.Tensor], w2: torch.Tensor, w2_scale: Optional[torch.Tensor],
+                    al: Alignment, out: torch.Tensor, identity: bool = False,
+                    activation: str = "silu") -> ExpertsProblem:
+    """One problem of moe_experts_multi (``identity``: NULL sorted_slot, E == 1, top_k == 1)."""
+    T = a1q.shape[0]
+    E, rows13, _ = w13.shape
+    I = rows13 if activation.endswith("_no_mul") else rows13 // 2
+    prob = ExpertsProblem(_ptr(a1q), _ptr(a1q_scale), _ptr(w13), _ptr(w13_scale), _ptr(w2), _ptr(w2_scale),
+                          _ptr(al.expert_offsets), None if identity else _ptr(al.sorted_slot), _ptr(al.tile_map),
+                          _ptr(al.num_tiles), T, I, E, al.top_k, _ptr(out))
+    # the struct holds raw device pointers: keep the tensors alive as long as it is
+    prob._tensors = (a1q, a1q_scale, w13, w13_scale, w2, w2_scale, al, out)
+    return prob
+
+
+def workspace_size_multi(problems, H: int, quant: str) -> int:
+    arr = (ExpertsProblem * len(problems))(*problems)
+    return int(lib().moe_workspace_size_multi(arr, len(problems), H, ctypes.byref(_qc(quant))))
+
+
+def moe_experts_multi(problems, H: int, quant: str, ws: torch.Tensor, activation: str = "silu", stream=None):
+    """Several expert problems (``experts_problem``) in the same GEMM launches."""
+    if activation not in ACTIVATIONS:
+        raise ValueError(f"unknown activation {activation!r}")
+    arr = (ExpertsProblem * len(problems))(*problems)
+    _check("moe_experts_multi", lib().moe_experts_multi(arr, len(problems), H, ctypes.byref(_qc(quant)),
+                                                        ACTIVATIONS[activation], _ptr(ws), ws.numel(),
+                                                        _stream(stream)))
 
 
 def moe_finalize(fused_expert_output: torch.Tensor, topk_weights: Optional[torch.Tensor], top_k: int,

@@ -139,3 +139,22 @@ def test_experts_act_rejects_unknown_activation(moelib):
     assert call(6) == moe.MOE_ERR_UNSUPPORTED
     assert call(moe.ACTIVATIONS["gelu"], T=0) == moe.MOE_OK   # nothing to do, no launch
     assert sorted(moe.ACTIVATIONS.values()) == list(range(6))
+
+
+def test_experts_multi_rejects_what_it_cannot_fuse(moelib):
+    L = moelib
+    P = moe.ExpertsProblem
+
+    def prob(I, T=4):
+        return P(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, T, I, 8, 1, FAKE)
+
+    two = (P * 2)(prob(256), prob(512))
+    assert L.moe_experts_multi(two, 2, 256, ctypes.byref(moe.QC_BF16), 0, FAKE, 1 << 30, None) == \
+        moe.MOE_ERR_UNSUPPORTED                      # the second GEMM's depth differs
+    same = (P * 2)(prob(256), prob(256))
+    assert L.moe_experts_multi(same, 2, 256, ctypes.byref(moe.QC_FP8), 0, FAKE, 1 << 30, None) == \
+        moe.MOE_ERR_UNSUPPORTED                      # fp8 problems run one per call
+    assert L.moe_experts_multi(same, 3, 256, ctypes.byref(moe.QC_BF16), 0, FAKE, 1 << 30, None) == \
+        moe.MOE_ERR_INVALID_ARG
+    empty = (P * 2)(prob(256, T=0), prob(512, T=0))
+    assert L.moe_experts_multi(empty, 2, 256, ctypes.byref(moe.QC_BF16), 0, FAKE, 1 << 30, None) == moe.MOE_OK

@@ -159,3 +159,31 @@ def test_experts_act_silu_is_moe_experts(cuda_dev):
     assert st == moe.MOE_OK
     assert torch.equal(out, y_act)
 
+
+
+@pytest.mark.parametrize("T,H,I,E,k", [
+    (1, 2048, 2048, 16, 1),    # decode: both problems' units split across CTAs (stream-K)
+    (8, 2048, 2048, 16, 1),
+    (200, 512, 384, 6, 2),     # round-robin: routed tiles and the shared expert's tiles side by side
+])
+def test_experts_multi_routed_and_shared(cuda_dev, T, H, I, E, k):
+    # the routed experts and a shared expert (E = 1, identity rows) in the same launches
+    inp = make_inputs(scaled(CONFIGS["llama8"], T=T, H=H, I=I, E=E, top_k=k, shared_I=I, scoring="softmax",
+                             weight_on_input=False))
+    ids = _ids(T, k, E, T + H + 11)
+    d = lambda t: t.to(cuda_dev)
+    al = moe.moe_align(d(ids), E)
+    al_s = moe.moe_align(torch.zeros((T, 1), dtype=torch.int32, device=cuda_dev), 1)
+    a1 = d(inp.a1)
+    y = torch.empty((T * k, H), dtype=torch.bfloat16, device=cuda_dev)
+    ysh = torch.empty((T, H), dtype=torch.bfloat16, device=cuda_dev)
+    probs = [moe.experts_problem(a1, None, d(inp.w13), None, d(inp.w2), None, al, y),
+             moe.experts_problem(a1, None, d(inp.shared_w13), None, d(inp.shared_w2), None, al_s, ysh, identity=True)]
+    ws = torch.empty(moe.workspace_size_multi(probs, H, "bf16"), dtype=torch.uint8, device=cuda_dev)
+    moe.moe_experts_multi(probs, H, "bf16", ws)
+    torch.cuda.synchronize()
+    assert moe.moe_device_status() == moe.MOE_OK
+    yref = moe_ref.experts(inp.a1, None, inp.w13, None, inp.w2, None, moe_ref.align(ids, E, 128), k, "bf16")
+    shref = moe_ref.dense_mlp(inp.a1, inp.shared_w13[0], inp.shared_w2[0])
+    check_bf16(y, yref, "multi: routed", slack=_stored_pair_slack(yref))
+    check_bf16(ysh, shref, "multi: shared", slack=_stored_pair_slack(shref))

@@ -39,14 +39,14 @@ def oracle_tokens(inp, tokens, gpu_ids, gpu_w):
         # one scale over every expert's intermediate: the whole layer at once (all tokens)
         assert n == cfg.T
         y = moe_ref.experts(a1q, sc, inp.w13, inp.w13_scale, inp.w2, inp.w2_scale, moe_ref.align(ids, cfg.E, 128),
-                            k, cfg.quant)
+                            k, cfg.quant, cfg.activation)
     for e in ([] if cfg.quant == "fp8_tensor" else sorted(set(ids.reshape(-1).tolist()))):
         slots = [(i, j) for i in range(n) for j in range(k) if int(ids[i, j]) == e]
         rows = np.array([i for i, _ in slots])
         A = moe_ref._act64(a1q, sc, rows, cfg.quant)
         W13 = moe_ref._weights64(inp.w13, inp.w13_scale, e, cfg.quant)
         W2 = moe_ref._weights64(inp.w2, inp.w2_scale, e, cfg.quant)
-        ye = moe_ref.expert_rows(A, W13, W2, cfg.quant)
+        ye = moe_ref.expert_rows(A, W13, W2, cfg.quant, cfg.activation)
         for r, (i, j) in enumerate(slots):
             y[i * k + j] = ye[r]
     shared = moe_ref.dense_mlp(a1, inp.shared_w13[0], inp.shared_w2[0]) if cfg.shared_I else None
@@ -79,7 +79,13 @@ SMALL = {
     "deepseek_small_tensor": scaled(CONFIGS["deepseek"], T=256, H=512, I=256, E=32, shared_I=256, quant="fp8_tensor"),
     "llama_small": scaled(CONFIGS["llama8"], T=100, H=384, I=512, shared_I=256),
     "llama_small_T1": scaled(CONFIGS["llama1"], H=384, I=512, shared_I=256),
+    # shared expert with the routed experts' I: both in the same launches (moe_experts_multi)
+    "llama_small_fused": scaled(CONFIGS["llama8"], T=100, H=384, I=512, shared_I=512),
+    "llama_small_fused_T1": scaled(CONFIGS["llama1"], H=2048, I=2048, shared_I=2048),
     "residual_rms": scaled(CONFIGS["mixtral"], T=64, H=256, I=256, residual=True, rms=True),
+    "mixtral_small_gelu_tanh": scaled(CONFIGS["mixtral"], T=200, H=512, I=768, activation="gelu_tanh"),
+    "deepseek_small_gelu_no_mul": scaled(CONFIGS["deepseek"], T=256, H=512, I=256, E=32, shared_I=256,
+                                         activation="gelu_no_mul"),
 }
 
 
