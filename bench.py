@@ -93,6 +93,31 @@ def experts_algorithmic(cfg, counts):
 UNIT_SOURCES = {"experts": ["moe_experts.cu", "moe_common.cuh"], "finalize": ["moe_finalize.cu", "moe_common.cuh"]}
 
 
+def graph_kernel_nodes(graph):
+    """Kernel nodes of a captured step (the step calls only this library, so these
+    are its launches), read from the graph through the CUDA runtime; None when
+    the graph cannot be read."""
+    try:
+        import ctypes
+        raw = graph.raw_cuda_graph()
+        rt = ctypes.CDLL("libcudart.so.13")
+        n = ctypes.c_size_t(0)
+        if rt.cudaGraphGetNodes(ctypes.c_void_p(int(raw)), None, ctypes.byref(n)) != 0 or n.value == 0:
+            return None
+        nodes = (ctypes.c_void_p * n.value)()
+        if rt.cudaGraphGetNodes(ctypes.c_void_p(int(raw)), nodes, ctypes.byref(n)) != 0:
+            return None
+        kernels = 0
+        for node in nodes:
+            t = ctypes.c_int(-1)
+            if rt.cudaGraphNodeGetType(ctypes.c_void_p(node), ctypes.byref(t)) != 0:
+                return None
+            kernels += t.value == 0  # cudaGraphNodeTypeKernel
+        return kernels
+    except Exception:
+        return None
+
+
 def sources_digest(files) -> str:
     """sha256 over the given csrc/ files and the public header."""
     import hashlib
@@ -312,15 +337,15 @@ def run_gpu(args, ws, rank, local):
             def step():
                 step_obj.weights()
                 step_obj.finalize(True)
-            launches_per_step = 2
+            launches_per_step = 2  # estimate; replaced by the captured graph's kernel count
         else:
             layer = MoELayer(inp, stream=stream)
 
             def step():
                 layer.forward(inp.logits, inp.a1)
-            # route 1, align 3, prepare 0/1, experts 3 (gather, GEMM1, GEMM2), finalize 1,
-            # shared expert 2 (identity permutation: no gather)
-            launches_per_step = 1 + 3 + (0 if layer.passthrough else 1) + 3 + 1 + (2 if cfg.shared_I else 0)
+            # estimate (route, align, prepare, plan + gather + 2 GEMMs, finalize); replaced by
+            # the captured graph's kernel count when the graph can be read
+            launches_per_step = 1 + 1 + (0 if layer.passthrough else 1) + 4 + 1
         for _ in range(args.warmup):
             step()
         torch.cuda.synchronize(dev)
@@ -365,11 +390,21 @@ def run_gpu(args, ws, rank, local):
                                   "kernel": dom_name}), flush=True)
             return
         graph = None
+        launches_counted = False
         if not args.no_graph:
             # the step's library calls captured once and replayed: same kernels, no per-call host work
-            graph = torch.cuda.CUDAGraph()
+            try:
+                graph = torch.cuda.CUDAGraph(keep_graph=True)
+            except TypeError:
+                graph = torch.cuda.CUDAGraph()
             with torch.cuda.graph(graph, stream=stream):
                 step()
+            counted = graph_kernel_nodes(graph)
+            if counted:
+                launches_per_step = counted
+                launches_counted = True
+            if hasattr(graph, "instantiate"):
+                graph.instantiate()
             for _ in range(3):
                 graph.replay()
             torch.cuda.synchronize(dev)
@@ -502,6 +537,8 @@ def run_gpu(args, ws, rank, local):
             "config": {"workload": cfg.description, "T": cfg.T, "H": cfg.H, "I": cfg.I, "E": cfg.E,
                        "top_k": cfg.top_k, "parallelism": f"replicas{ws}",
                        "launch": "cuda_graph" if not args.no_graph else "eager",
+                       "gpu_launches_per_step": launches_per_step,
+                       "gpu_launches_from": "captured graph's kernel nodes" if launches_counted else "estimate",
                        "l2": "no flush: each step streams the expert weights (larger than the 129 MB L2)"
                        if not cfg.finalize_only else "inputs smaller than L2 (finalize-only workload)"},
             "roofline": roofline, "cpu_baseline": cpu, "clocks": clk, "e2e": e2e,
