@@ -89,7 +89,7 @@ def experts_algorithmic(cfg, counts):
     return w + act, flops
 
 
-# kernel sources of each dominant unit (csrc/ files; the public header always counts)
+# kernel sources of each dominant unit (csrc/ files)
 UNIT_SOURCES = {"experts": ["moe_experts.cu", "moe_common.cuh"], "finalize": ["moe_finalize.cu", "moe_common.cuh"]}
 
 
@@ -119,11 +119,11 @@ def graph_kernel_nodes(graph):
 
 
 def sources_digest(files) -> str:
-    """sha256 over the given csrc/ files and the public header."""
+    """sha256 over the given csrc/ files (the unit's kernels and their helpers)."""
     import hashlib
     csrc = os.path.join(os.path.dirname(os.path.abspath(__file__)), "mixture_experts_layer_tokens_gb300", "csrc")
     h = hashlib.sha256()
-    for f in sorted(files) + ["../../include/moe.h"]:
+    for f in sorted(files):
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(f.encode() + b"\0" + fh.read())
     return h.hexdigest()
