@@ -38,6 +38,9 @@
 //          every 128-deep K block the MMA writes each K block into one of two
 //          partial accumulators that the epilogue scales and adds into fp32
 //          registers (software promotion; the scales are fp32).
+//   problems  one launch may carry two expert problems (moe_experts_multi: a
+//          layer's routed experts and its shared expert): their units are
+//          numbered one after the other and share the schedule below.
 //   schedule  with at least 4 units per CTA, units are dealt round-robin and
 //          units that share a weight tile run side by side on neighbouring
 //          SMs; with fewer (decode, deep-K GEMM2 tails) the (unit, K block)
@@ -200,7 +203,6 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity) {
   return __all_sync(0xffffffffu, mbar_wait(bar, parity));
 }
 
-__device__ __forceinline__ float4 ldcg4(const float* p) { return __ldcg(reinterpret_cast<const float4*>(p)); }
 
 // Epilogue threads of the CTA that finishes a split unit: one thread polls the
 // unit's arrival count (the other threads polling the same L2 line would
@@ -523,7 +525,7 @@ __global__ void __launch_bounds__(Warps<kFP8>::THREADS, 1)
     const int sub = q / 4;               // fp8: column half (bf16: always 0)
     const int r = quarter * 32 + lane;   // row within an M tile == TMEM lane
     const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
-    float* my_partial = p0.partials + (size_t)blockIdx.x * C::PARTIAL_FLOATS;  // [MG][BM][BN] (bf16) / [BM][2][128] (fp8)
+    float* my_partial = p0.partials + (size_t)blockIdx.x * C::PARTIAL_FLOATS;  // [MG][BM][BN] (bf16 splits)
     int acc = 0;
     uint32_t acc_phase = 0;
     int xbuf = 0;
@@ -544,9 +546,9 @@ __global__ void __launch_bounds__(Warps<kFP8>::THREADS, 1)
         c_first = blockIdx.x + 1;
         c_last = sched.cta_of((long long)u * KB + KB - 1);
       }
-      // thread-private slot of a split-unit partial: bf16 256 columns of (M tile m, row r) at
-      // poff + m * BM * 256; fp8 128 values of (r, half)
-      const size_t poff = kFP8 ? ((size_t)r * 2 + sub) * 128 : (size_t)r * 256;
+      // thread-private slot of a split-unit partial (bf16): 256 columns of (M tile m, row r)
+      // at poff + m * BM * 256
+      const size_t poff = (size_t)r * 256;
 
       if (!kFP8) {
         // one warp per TMEM lane quarter: rows r of each M tile of the group, 8 chunks of
@@ -781,30 +783,7 @@ __global__ void __launch_bounds__(Warps<kFP8>::THREADS, 1)
           if (acc == 0) acc_phase ^= 1;
         }
         if (!ok) break;
-        if (role == 2) {
-          if (valid) {
-            float4* dst = reinterpret_cast<float4*>(my_partial + poff);
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-              __stcg(dst + j, make_float4(accv[4 * j], accv[4 * j + 1], accv[4 * j + 2], accv[4 * j + 3]));
-          }
-          signal_split_partial(p.flags + lu);
-          continue;
-        }
-        if (role == 1) {
-          ok = wait_split_partials(p.flags + lu, (c_last - c_first + 1) * EPI_THREADS, fixbar);
-          if (!ok) break;
-          if (valid) {
-            for (int cc = c_first; cc <= c_last; ++cc) {
-              const float* src = p.partials + (size_t)cc * C::PARTIAL_FLOATS + poff;
-#pragma unroll
-              for (int j = 0; j < 32; ++j) {
-                const float4 a = ldcg4(src + 4 * j);
-                accv[4 * j] += a.x; accv[4 * j + 1] += a.y; accv[4 * j + 2] += a.z; accv[4 * j + 3] += a.w;
-              }
-            }
-          }
-        }
+        // (fp8 units are never split: no partials to park or to add)
         if (kHB16) {
           // the "A"/"T" formats: h goes out in bf16 ([rows][I]); a later pass quantises it
           const int hc0 = kNoMul ? (2 * it.n + half) * 128 : it.n * 128 + 64 * half;
@@ -995,7 +974,10 @@ __global__ void __launch_bounds__(1024)
 __global__ void __launch_bounds__(256)
     gather_kernel(const uint8_t* __restrict__ a1q, const float* __restrict__ a1q_scale,
                   const int32_t* __restrict__ sorted_slot, int S, int top_k, int row_bytes, int ngroups,
-                  uint8_t* __restrict__ A, float* __restrict__ a_scale_t, int s_pad, int scale_stride) {
+                  uint8_t* __restrict__ A, float* __restrict__ a_scale_t, int s_pad, int scale_stride,
+                  int* __restrict__ flags, int nflags) {
+  // (when no plan launch runs, the gather also clears the split-unit flags)
+  for (int i = blockIdx.x * 256 + threadIdx.x; i < nflags; i += gridDim.x * 256) flags[i] = 0;
   const int p = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (p >= S) return;
@@ -1286,7 +1268,13 @@ moe_status_t experts_run(const moe_experts_problem* probs, int nprob, int H, con
   GemmProblems g1 = {}, g2 = {};
   g1.nprob = g2.nprob = n;
   int* flags_all = reinterpret_cast<int*>(wsb + L.flags);
-  if (mg1 == 2 || mg2 == 2 || split1 || split2) {
+  // The split flags are cleared by the plan launch when there is one (two-tile group
+  // maps), else by the first gather launch, else by a plan launch of their own.
+  bool gathers = fp8;
+  for (int i = 0; i < n; ++i) gathers = gathers || pr[i].sorted_slot != nullptr;
+  const bool split = split1 || split2;
+  bool flags_pending = split && !(mg1 == 2 || mg2 == 2) && gathers;
+  if (mg1 == 2 || mg2 == 2 || (split && !gathers)) {
     // clears every problem's flags; builds problem 0's two-tile group maps (n == 1 when mg > 1)
     const ProbLayout& P = L.p[0];
     plan_kernel<<<1, 1024, 0, s>>>(pr[0].tile_map, pr[0].num_tiles, pr[0].expert_offsets, mg1, mg2,
@@ -1309,7 +1297,9 @@ moe_status_t experts_run(const moe_experts_problem* probs, int nprob, int H, con
       const unsigned gb = (unsigned)((S + 7) / 8);
       gather_kernel<<<gb, 256, 0, s>>>(static_cast<const uint8_t*>(q.a1q), q.a1q_scale, q.sorted_slot, (int)S,
                                        q.top_k, H * esz, hb16 ? 1 : H / 128, gather_rows ? wsb + P.A : nullptr, As,
-                                       P.s_pad, group == 128 ? H / 128 : (group == MOE_GROUP_TOKEN ? 1 : 0));
+                                       P.s_pad, group == 128 ? H / 128 : (group == MOE_GROUP_TOKEN ? 1 : 0),
+                                       flags_pending ? flags_all : nullptr, flags_pending ? L.nflags : 0);
+      flags_pending = false;
       if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
     }
     // A maps with one-tile and two-tile boxes; weight maps with 256-row boxes (gemm2:
