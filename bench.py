@@ -129,12 +129,12 @@ def sources_digest(files) -> str:
     return h.hexdigest()
 
 
-def measured_traffic(workload: str):
+def measured_traffic(workload: str, path: str = None):
     """DRAM bytes (read + write) of one dominant-unit call from the committed ncu
     capture (profiles/dram_traffic.json; for a workload too large to capture, the
     recorded scaling of a smaller case); None when there is none or the unit's
     kernel sources changed since."""
-    path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "profiles", "dram_traffic.json")
+    path = path or os.path.join(os.path.dirname(os.path.abspath(__file__)), "profiles", "dram_traffic.json")
     try:
         with open(path) as f:
             e = json.load(f)["workloads"][workload]

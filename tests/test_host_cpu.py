@@ -1,0 +1,71 @@
+"""Host-side logic that needs no GPU: the binding's argument handling and the
+bench's traffic records (only while the recorded kernel sources match)."""
+import importlib.util
+import json
+import os
+
+import pytest
+import torch
+
+from mixture_experts_layer_tokens_gb300 import moe
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _bench():
+    spec = importlib.util.spec_from_file_location("bench_under_test", os.path.join(ROOT, "bench.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod
+
+
+def test_quant_and_activation_names():
+    assert set(moe.QUANT_CONFIGS) == {"bf16", "fp8", "fp8_token", "fp8_tensor"}
+    assert moe.QUANT_CONFIGS["fp8_token"].act_group == moe.MOE_GROUP_TOKEN == -1
+    assert moe.QUANT_CONFIGS["fp8_tensor"].act_group == moe.MOE_GROUP_TENSOR == -2
+    assert moe.scale_shape("fp8", 5, 256) == (5, 2)
+    assert moe.scale_shape("fp8_token", 5, 256) == (5,)
+    assert moe.scale_shape("fp8_tensor", 5, 256) == (1,)
+    with pytest.raises(ValueError):
+        moe._qc("int8")
+
+
+def test_experts_problem_keeps_its_tensors_alive():
+    a = torch.zeros(4, 256, dtype=torch.bfloat16)
+    w13 = torch.zeros(2, 512, 256, dtype=torch.bfloat16)
+    w2 = torch.zeros(2, 256, 256, dtype=torch.bfloat16)
+    out = torch.zeros(4, 256, dtype=torch.bfloat16)
+
+    class Al:  # the fields experts_problem reads
+        expert_offsets = sorted_slot = tile_map = num_tiles = torch.zeros(4, dtype=torch.int32)
+        top_k = 1
+    p = moe.experts_problem(a, None, w13, None, w2, None, Al(), out)
+    assert (p.T, p.I, p.E, p.top_k) == (4, 256, 2, 1)
+    assert p.w13 == w13.data_ptr() and any(t is w13 for t in p._tensors)
+    q = moe.experts_problem(a, None, w13[:, :256], None, w2, None, Al(), out, activation="gelu_no_mul")
+    assert q.I == 256
+
+
+def test_traffic_record_only_while_sources_match(tmp_path):
+    b = _bench()
+    rec = json.load(open(os.path.join(ROOT, "profiles", "dram_traffic.json")))
+    for name, e in rec["workloads"].items():
+        assert e["unit"] in b.UNIT_SOURCES and e["bytes_per_call"] > 0
+    # a record whose hash matches the unit's current sources is reported, a stale one is not
+    digest = b.sources_digest(b.UNIT_SOURCES["finalize"])
+    fake = {"workloads": {"w_ok": {"unit": "finalize", "bytes_per_call": 123, "sources_sha256": digest},
+                          "w_stale": {"unit": "finalize", "bytes_per_call": 456, "sources_sha256": "0" * 64}}}
+    path = tmp_path / "traffic.json"
+    path.write_text(json.dumps(fake))
+    assert b.measured_traffic("w_ok", str(path)) == 123
+    assert b.measured_traffic("w_stale", str(path)) is None
+    assert b.measured_traffic("absent", str(path)) is None
+
+
+def test_graph_kernel_count_without_a_graph_is_none():
+    b = _bench()
+
+    class NoGraph:
+        def raw_cuda_graph(self):
+            raise RuntimeError("no graph")
+    assert b.graph_kernel_nodes(NoGraph()) is None
