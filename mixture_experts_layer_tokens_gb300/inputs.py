@@ -13,6 +13,14 @@ residual, RMSNorm weight):
 * fp8 expert weights: E4M3 codes of N(0, 64^2) draws (torch's cast) with one
   fp32 scale per 128x128 block, scale = U(0.75, 1.25) / (64 sqrt(fan_in)), so the
   dequantised weights have the N(0, 1/fan_in) scale of the bf16 ones;
+* NVFP4 expert weights: uniform random bytes (two E2M1 codes each, so every
+  code is equally likely), E4M3 scale codes uniform in [0x40, 0x50) (values
+  2 .. 7.5) per 16 elements, and one fp32 global scale per expert and matrix,
+  U(0.75, 1.25) / (13.2 sqrt(fan_in)), so the dequantised weights have about the
+  N(0, 1/fan_in) scale of the bf16 ones (E2M1 codes have rms 2.93, the scales
+  about 4.5); the activations' global scale is 2^-8 and the intermediate's
+  2^-7 (a1 ~ N(0, 1) and h = silu(g) u with g, u of unit scale keep every
+  group's scale code below the E4M3 maximum);
 * shared expert (when present): bf16 weights drawn like the routed ones;
 * finalize-only workloads: expert rows y ~ N(0, 1) bf16 [T*k, H], logits over k
   experts ~ N(0, 1) (softmax of them gives the top-k weights), distinct random
@@ -41,7 +49,8 @@ class LayerConfig:
     E: int
     top_k: int
     quant: str = "bf16"            # "bf16"; "fp8" (E4M3 G(128) activations, 128x128 block weights);
-                                   # "fp8_token" / "fp8_tensor" (per-token / per-tensor activation scales)
+                                   # "fp8_token" / "fp8_tensor" (per-token / per-tensor activation scales);
+                                   # "nvfp4" (E2M1 + E4M3 per 16 + fp32 global scales, every operand)
     scoring: str = "softmax"       # "softmax" (renormalised top-k) or "sigmoid" (top-1)
     weight_on_input: bool = False  # apply the top-k weight to a1 in prepare (top_k == 1)
     shared_I: int = 0              # intermediate size of the bf16 shared expert, 0 = none
@@ -144,6 +153,22 @@ def _fp8_weights(gen, E, N, K, device):
     return codes, scale
 
 
+def _nvfp4_weights(gen, E, N, K, device):
+    assert K % 16 == 0
+    packed = torch.empty((E, N, K // 2), dtype=torch.uint8, device=device)
+    sf = torch.empty((E, N, K // 16), dtype=torch.uint8, device=device)
+    for e in range(E):
+        packed[e] = torch.randint(0, 256, (N, K // 2), generator=gen, device=device, dtype=torch.int32).to(torch.uint8)
+        sf[e] = torch.randint(0x40, 0x50, (N, K // 16), generator=gen, device=device, dtype=torch.int32).to(torch.uint8)
+    u = torch.rand((E,), generator=gen, device=device) * 0.5 + 0.75
+    gscale = (u / (13.2 * math.sqrt(K))).to(torch.float32)
+    return packed, sf, gscale
+
+
+NVFP4_A1_GSCALE = 2.0 ** -8
+NVFP4_H_GSCALE = 2.0 ** -7
+
+
 def make_logits(cfg: LayerConfig, seed: int = 0, device="cpu") -> torch.Tensor:
     """The router logits of `make_inputs(cfg, seed, device)` (its first draw) alone."""
     gen = torch.Generator(device=torch.device(device))
@@ -170,7 +195,11 @@ def make_inputs(cfg: LayerConfig, seed: int = 0, device="cpu") -> LayerInputs:
     a1 = torch.randn((T, H), generator=gen, device=dev).to(torch.bfloat16)
     inp = LayerInputs(cfg, logits, a1=a1)
     rows13 = I if cfg.activation.endswith("_no_mul") else 2 * I
-    if cfg.quant != "bf16":
+    if cfg.quant == "nvfp4":
+        inp.w13, inp.w13_scale, g13 = _nvfp4_weights(gen, E, rows13, H, dev)
+        inp.w2, inp.w2_scale, g2 = _nvfp4_weights(gen, E, H, I, dev)
+        inp.extra.update(w13_gscale=g13, w2_gscale=g2, a1_gscale=NVFP4_A1_GSCALE, h_gscale=NVFP4_H_GSCALE)
+    elif cfg.quant != "bf16":
         inp.w13, inp.w13_scale = _fp8_weights(gen, E, rows13, H, dev)
         inp.w2, inp.w2_scale = _fp8_weights(gen, E, H, I, dev)
     else:

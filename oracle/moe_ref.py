@@ -483,3 +483,89 @@ def finalize(fused_expert_output, topk_weights, top_k: int, apply_router_weight_
     if nvfp4_global_scale is not None:
         fo.nvfp4 = nvfp4_quantize(o, nvfp4_global_scale)
     return fo
+
+
+# =========================================================================== NVFP4 experts
+# Reading: the "Fused MoE Kernel Features" experts table lists nvfp4 as the
+# quantisation type of the cutlass_fp4 experts (formats A, T; SiLU) and of the
+# trtllm experts (G(16)).  NVFP4 is the encoding the flashinfer finalize page's
+# packed output uses: E2M1 pairs, one E4M3 scale per 16 elements, and one fp32
+# global scale per tensor ("T").  Every tensor of the experts here is in that
+# encoding: the activations (one global scale), each expert's weight matrices
+# (one global scale per expert and matrix) and the intermediate h between the
+# GEMMs (one global scale), which is stored in the activation type (bf16) and
+# then quantised, as the "A"/"T" fp8 formats do.
+
+def nvfp4_quantize_fp32(x: np.ndarray, global_scale: float):
+    """NVFP4 packing with each decision step in fp32, the precision the kernels
+    quantise in: s6 = fp32(6 g); sf = e4m3_rn_satfinite(fp32(amax / s6));
+    d = fp32(sf g); q_i = e2m1_rn_satfinite(fp32(x_i / d)) (q = 0 when d = 0).
+    x must hold fp32 values (bf16 inputs do); g an fp32 number > 0.  Returns
+    (packed uint8 [R, C/2], element 2i in the low nibble; scale codes [R, C/16])."""
+    R, C = x.shape
+    g32 = float(np.float32(global_scale))
+    grp = np.asarray(x, dtype=np.float64).reshape(R, C // 16, 16)
+    amax = np.abs(grp).max(axis=2)
+    s6 = float(np.float32(6.0 * g32))
+    sf_code = codecs.e4m3_encode(codecs.round_fp32(amax / s6))
+    d = codecs.round_fp32(codecs.e4m3_decode(sf_code) * g32)[:, :, None]
+    with np.errstate(divide="ignore", invalid="ignore"):
+        ratio = np.where(d > 0, codecs.round_fp32(grp / np.where(d > 0, d, 1.0)), 0.0)
+    codes = codecs.e2m1_encode(ratio).reshape(R, C)
+    packed = (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)
+    return packed, sf_code.astype(np.uint8)
+
+
+def prepare_nvfp4(a1: torch.Tensor, topk_weights, apply_router_weight_on_input: bool, global_scale: float):
+    """Prepare into NVFP4: the optional weight on the input exactly as
+    ``prepare``, then ``nvfp4_quantize_fp32`` of the bf16 rows with the
+    activations' global scale.  Returns (packed [T, H/2], scale codes [T, H/16])
+    as uint8 tensors."""
+    x = _np(a1)
+    if apply_router_weight_on_input:
+        w = _np(topk_weights)
+        assert w.shape[1] == 1, "apply_router_weight_on_input needs top_k == 1"
+        x = codecs.round_bf16(x * codecs.round_bf16(w[:, 0])[:, None])
+    packed, sf = nvfp4_quantize_fp32(x, global_scale)
+    return torch.from_numpy(packed), torch.from_numpy(sf)
+
+
+def experts_nvfp4(a1q, a1q_sf, a1_gscale: float, w13, w13_sf, w13_gscale, w2, w2_sf, w2_gscale,
+                  h_gscale: float, al: Alignment, top_k: int, act: str = "silu", return_h: bool = False):
+    """Grouped experts with every operand in NVFP4 (see the reading above).
+
+    For expert e and its rows (token t of slot f as in ``experts``):
+    A = dequant(a1q[t]; g_a), W13 = dequant(w13[e]; g13[e]) in fp64;
+    h = act(A W13^T) (fp64), stored bf16, then h_q = nvfp4_quantize_fp32(h; g_h);
+    y[f] = bf16(dequant(h_q; g_h) . dequant(w2[e]; g2[e])^T).
+    w13 [E, 2I, H/2] (*_no_mul: [E, I, H/2]) with w13_sf [E, rows, H/16];
+    w2 [E, H, I/2] with w2_sf [E, H, I/16]; w13_gscale, w2_gscale [E].
+    Returns y [T*k, H] (fp64 holding bf16 values); with ``return_h`` also the
+    unrounded fp64 h of every sorted row [S, I] (S = offsets[E])."""
+    offs = _np(al.expert_offsets)
+    order = _np(al.sorted_slot)
+    S = int(offs[-1])
+    aq, asf = _np(a1q).astype(np.uint8), _np(a1q_sf).astype(np.uint8)
+    H = aq.shape[1] * 2
+    g13 = _np(w13_gscale).astype(np.float64).reshape(-1)
+    g2 = _np(w2_gscale).astype(np.float64).reshape(-1)
+    y = torch.zeros((S, H), dtype=F64)
+    h_all = None
+    for e in range(len(offs) - 1):
+        p0, p1 = int(offs[e]), int(offs[e + 1])
+        if p0 == p1:
+            continue
+        slots = order[p0:p1]
+        t = slots // top_k
+        A = nvfp4_dequantize(aq[t], asf[t], a1_gscale)
+        W13 = nvfp4_dequantize(_np(w13[e]).astype(np.uint8), _np(w13_sf[e]).astype(np.uint8), g13[e])
+        h = activation(torch.from_numpy(A @ W13.T), act).numpy()
+        if return_h:
+            if h_all is None:
+                h_all = np.zeros((S, h.shape[1]))
+            h_all[p0:p1] = h
+        hq, hsf = nvfp4_quantize_fp32(codecs.round_bf16(h), h_gscale)
+        W2 = nvfp4_dequantize(_np(w2[e]).astype(np.uint8), _np(w2_sf[e]).astype(np.uint8), g2[e])
+        y[torch.from_numpy(slots.astype(np.int64))] = _expert_out(nvfp4_dequantize(hq, hsf, h_gscale),
+                                                                  torch.from_numpy(W2))
+    return (y, h_all) if return_h else y
