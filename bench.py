@@ -71,11 +71,20 @@ def experts_algorithmic(cfg, counts):
     """Bytes and FLOPs one expert pass must move/do: the weights of the experts
     that received tokens (+ fp8 block scales), the activations read once, the
     intermediate h written and read once, the output rows written once; FLOPs
-    2 H I per weight matrix (3 gated, 2 for *_no_mul) per token slot (no padded rows)."""
+    2 H I per weight matrix (3 gated, 2 for *_no_mul) per token slot (no padded rows).
+    NVFP4: half a byte per code plus one scale byte per 16; h is stored in bf16,
+    then as NVFP4 codes and scales, each written and read once."""
+    mats = 2 if cfg.activation.endswith("_no_mul") else 3  # gate (+ up) and down projections
+    S = cfg.T * cfg.top_k
+    flops = 2.0 * mats * S * cfg.H * cfg.I
+    if cfg.quant == "nvfp4":
+        touched = int((counts > 0).sum())
+        w = touched * mats * cfg.H * cfg.I * 9 // 16
+        act = cfg.T * cfg.H * 9 // 16 + 2 * S * cfg.I * 2 + 2 * S * cfg.I * 9 // 16 + S * cfg.H * 2
+        return w + act, flops
     fp8 = cfg.quant != "bf16"
     esz = 1 if fp8 else 2
     touched = int((counts > 0).sum())
-    mats = 2 if cfg.activation.endswith("_no_mul") else 3  # gate (+ up) and down projections
     w = touched * mats * cfg.H * cfg.I * esz
     if fp8:
         w += touched * mats * (cfg.H // 128) * (cfg.I // 128) * 4
@@ -85,8 +94,15 @@ def experts_algorithmic(cfg, counts):
         act += cfg.T * (cfg.H // 128) * 4 + 2 * S * (cfg.I // 128) * 4
     elif fp8:  # per-token / per-tensor: per-row scales, and h also stored in bf16 and read back
         act += cfg.T * 4 + 2 * S * 4 + 2 * S * cfg.I * 2
-    flops = 2.0 * mats * S * cfg.H * cfg.I
     return w + act, flops
+
+
+# nominal dense tensor rates relative to bf16 (2.25 / 4.5 / 13.5 PFLOP/s on a GB300)
+TENSOR_RATIO = {"bf16": 1.0, "nvfp4": 6.0}
+
+
+def tensor_ratio(quant):
+    return TENSOR_RATIO.get(quant, 2.0)  # the fp8 formats: 2x
 
 
 # kernel sources of each dominant unit (csrc/ files)
@@ -222,11 +238,18 @@ def oracle_tokens_seconds(inp, tokens):
     else:
         ids, w = moe_ref.route_softmax_renorm(logits, cfg.top_k)
     a1 = inp.a1[tokens].cpu()
-    a1q, sc = moe_ref.prepare(a1, w, cfg.weight_on_input, cfg.quant)
-    if cfg.quant == "fp8_tensor":  # one intermediate scale over every expert's rows of the sample
+    if cfg.quant == "nvfp4":
+        x = inp.extra
+        a1q, sc = moe_ref.prepare_nvfp4(a1, w, cfg.weight_on_input, x["a1_gscale"])
+        y = moe_ref.experts_nvfp4(a1q, sc, x["a1_gscale"], inp.w13.cpu(), inp.w13_scale.cpu(), x["w13_gscale"].cpu(),
+                                  inp.w2.cpu(), inp.w2_scale.cpu(), x["w2_gscale"].cpu(), x["h_gscale"],
+                                  moe_ref.align(ids, cfg.E, 128), cfg.top_k, cfg.activation)
+    elif cfg.quant == "fp8_tensor":  # one intermediate scale over every expert's rows of the sample
+        a1q, sc = moe_ref.prepare(a1, w, cfg.weight_on_input, cfg.quant)
         y = moe_ref.experts(a1q, sc, inp.w13, inp.w13_scale, inp.w2, inp.w2_scale, moe_ref.align(ids, cfg.E, 128),
                             cfg.top_k, cfg.quant, cfg.activation)
     else:
+        a1q, sc = moe_ref.prepare(a1, w, cfg.weight_on_input, cfg.quant)
         y = torch.cat([moe_ref.token_expert_rows(a1q, sc, inp.w13, inp.w13_scale, inp.w2, inp.w2_scale, ids, i,
                                                  cfg.quant, cfg.activation) for i in range(len(tokens))], 0)
     shared = moe_ref.dense_mlp(a1, inp.shared_w13[0], inp.shared_w2[0]) if cfg.shared_I else None
@@ -454,8 +477,9 @@ def run_gpu(args, ws, rank, local):
             b.record(stream)
         torch.cuda.synchronize(dev)
         dom_ms = a.elapsed_time(b) / (reps * R)
-        # the binding roof: HBM bytes or tensor FLOPs (fp8 peak = measured bf16 x the nominal 2x)
-        tensor_peak = bf16_peak * (2.0 if cfg.quant != "bf16" else 1.0)
+        # the binding roof: HBM bytes or tensor FLOPs (fp8 / NVFP4 peak = measured bf16 x the
+        # nominal 2x / 6x)
+        tensor_peak = bf16_peak * tensor_ratio(cfg.quant)
         t_hbm = nbytes / (hbm_peak * 1e9)
         t_tensor = flops / (tensor_peak * 1e12) if flops else 0.0
         if t_tensor > t_hbm:
@@ -464,7 +488,8 @@ def run_gpu(args, ws, rank, local):
                         "unit": "TFLOP/s", "frac": round(achieved / tensor_peak, 4),
                         "traffic": measured_traffic(cfg.name),
                         "kernel": dom_name, "algorithmic_flops": flops, "ms": round(dom_ms, 4),
-                        "peak_kind": peak_kind + (" bf16 x2 (nominal fp8:bf16)" if cfg.quant != "bf16" else "")}
+                        "peak_kind": peak_kind + ("" if cfg.quant == "bf16" else
+                                                  f" bf16 x{tensor_ratio(cfg.quant):g} (nominal {cfg.quant}:bf16)")}
             roofline["hbm_gbs"] = round(nbytes / (dom_ms * 1e-3) / 1e9, 1)
         else:
             achieved = nbytes / (dom_ms * 1e-3) / 1e9
@@ -533,7 +558,8 @@ def run_gpu(args, ws, rank, local):
                          f"({dt:.1f} s), CPU {cpu_model()}"}
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "fp8" if cfg.quant != "bf16" else "bf16", "data": "synthetic",
+            "vs_baseline": None, "dtype": {"bf16": "bf16", "nvfp4": "nvfp4"}.get(cfg.quant, "fp8"),
+            "data": "synthetic",
             "config": {"workload": cfg.description, "T": cfg.T, "H": cfg.H, "I": cfg.I, "E": cfg.E,
                        "top_k": cfg.top_k, "parallelism": f"replicas{ws}",
                        "launch": "cuda_graph" if not args.no_graph else "eager",

@@ -266,6 +266,50 @@ moe_status_t moe_experts_multi(const moe_experts_problem *problems, int num_prob
 size_t moe_workspace_size_multi(const moe_experts_problem *problems, int num_problems, int H,
                                 const moe_quant_config *qc);
 
+/* ------------------------------------------------------------------ NVFP4 experts
+ * The experts with every operand in NVFP4 ("Fused MoE Kernel Features", experts
+ * table: nvfp4 is a quantisation type of the cutlass_fp4 and trtllm experts),
+ * in the encoding of the finalize page's packed output: E2M1 codes in pairs
+ * (element 2i in the low nibble), one E4M3 scale code per 16 consecutive
+ * elements of a row, and one fp32 global scale g per tensor, value =
+ * e2m1(q) * e4m3(sf) * g.  Quantising a row (prepare, the intermediate):
+ *   sf = e4m3_rn_satfinite(fp32(amax16 / fp32(6 g))),
+ *   q  = e2m1_rn_satfinite(fp32(x / fp32(e4m3(sf) * g)))   (q = 0 when that is 0).
+ *
+ * moe_prepare_nvfp4: a1 [T, H] bf16 (optionally first a1 <- bf16(a1 *
+ *   bf16(w)) with the top-1 weight, as moe_prepare) -> a1q [T, H/2] codes,
+ *   a1q_sf [T, H/16] scale codes, with the global scale *a1_gscale (device
+ *   pointer, fp32, > 0).  H % 16 == 0; a1 and a1q 16-byte aligned.
+ *
+ * moe_experts_nvfp4: for every expert e and its sorted rows (as moe_experts):
+ *   [g | u] = dequant(a1q[t]) . dequant(w13[e])^T    fp32 accumulation; the
+ *            tensor core applies the E4M3 block scales, the product of the two
+ *            global scales *a1_gscale * w13_gscale[e] multiplies the sums
+ *   h      = act(g, u) stored bf16, then quantised to NVFP4 with *h_gscale
+ *   fused_expert_output[f] = dequant(h) . dequant(w2[e])^T   (bf16 [T*top_k, H],
+ *            token-major, unweighted)
+ * w13 [E, 2I, H/2] codes with w13_sf [E, 2I, H/16] (rows 0..I-1 gate, I..2I-1
+ * up; the *_NO_MUL activations: [E, I, H/2] and [E, I, H/16]); w2 [E, H, I/2]
+ * with w2_sf [E, H, I/16]; w13_gscale, w2_gscale [E] fp32; a1_gscale, h_gscale
+ * [1] fp32 (all device pointers).  expert_offsets / sorted_slot / tile_map /
+ * num_tiles as for moe_experts (sorted_slot NULL only when E == 1 and top_k ==
+ * 1).  H % 256 == 0, I % 256 == 0; every code, scale and output pointer 16-byte
+ * aligned.  ws: moe_workspace_size_nvfp4(...) bytes (MOE_ERR_WORKSPACE when
+ * smaller); an unknown activation returns MOE_ERR_UNSUPPORTED.  The caller owns
+ * every buffer; nothing is allocated. */
+moe_status_t moe_prepare_nvfp4(const void *a1, const float *topk_weights, int T, int H, int top_k,
+                               int apply_router_weight_on_input, const float *a1_gscale, void *a1q,
+                               void *a1q_sf, moe_stream_t stream);
+moe_status_t moe_experts_nvfp4(const void *a1q, const void *a1q_sf, const float *a1_gscale,
+                               const void *w13, const void *w13_sf, const float *w13_gscale,
+                               const void *w2, const void *w2_sf, const float *w2_gscale,
+                               const float *h_gscale, const int32_t *expert_offsets,
+                               const int32_t *sorted_slot, const int32_t *tile_map,
+                               const int32_t *num_tiles, int T, int H, int I, int E, int top_k,
+                               int activation, void *fused_expert_output, void *ws, size_t ws_bytes,
+                               moe_stream_t stream);
+size_t moe_workspace_size_nvfp4(int T, int H, int I, int E, int top_k);
+
 /* ------------------------------------------------------------------ finalize
  * Finalize: the top-k weight-and-reduce of the "No DP/EP" listing followed by
  * the single-GPU part of the flashinfer finalize fusion (introduction of its

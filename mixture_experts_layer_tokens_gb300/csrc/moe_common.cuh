@@ -3,6 +3,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp4.h>
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -236,6 +237,53 @@ __device__ __forceinline__ void mma_fp8(uint32_t d_tmem, uint64_t adesc, uint64_
       : "memory");
 }
 
+// Same with NVFP4 inputs and block scaling (kind::mxf4nvf4, scale_vec::4X): packed
+// E2M1 operands, one E4M3 scale per 16 K elements of every row of A and of B, read
+// by the tensor core from tensor memory at sfa / sfb, fp32 accumulate.  The scales
+// of one K = 64 step occupy 4 consecutive columns per 128 rows: the scale word
+// (4 E4M3 codes, K groups 0-3 in bytes 0-3) of row l + 32 c sits in lane l of each
+// 32-lane quarter, column c.
+__device__ __forceinline__ void mma_nvf4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+// Instruction descriptor of the block-scaled NVFP4 MMA: E2M1 A and B (format 1 of
+// kind::mxf4nvf4), K-major, E4M3 scales (bit 23 clear), shape M x N, K = 64.
+__host__ __device__ constexpr uint32_t make_idesc_nvf4(int M, int N) {
+  return (1u << 7)                       // A format: E2M1
+         | (1u << 10)                    // B format: E2M1
+         | ((uint32_t)(N >> 3) << 17)    // N / 8
+         | ((uint32_t)(M >> 4) << 24);   // M / 16
+}
+
+// 32 lanes x 16 / 32 consecutive 32-bit columns from registers into tensor memory.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]),
+      "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
+      "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
 // Shared-memory matrix descriptor for a K-major operand stored in 128-byte
 // swizzled rows (the layout a TMA load with SWIZZLE_128B writes): 8-row atoms
 // of 1024 bytes, consecutive atoms 1024 bytes apart along M/N.
@@ -320,6 +368,28 @@ __device__ __forceinline__ uint2 e4m3x8(const float (&x)[8], float s) {
       packed[i >> 1] = two;
   }
   return make_uint2(packed[0], packed[1]);
+}
+
+// One NVFP4 group of 16 values with global scale g, every step in fp32:
+// sf = e4m3_rn_satfinite(amax / (6 g)), q_i = e2m1_rn_satfinite(x_i / (sf g))
+// (0 when sf g = 0).  Returns the 16 codes packed (element 2i in the low nibble
+// of byte i) and writes the scale code.
+__device__ __forceinline__ uint64_t nvfp4_group16(const float (&x)[16], float g, uint8_t& sf_code) {
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(x[i]));
+  const __nv_fp8_storage_t sf8 = __nv_cvt_float_to_fp8(__fdiv_rn(amax, 6.0f * g), __NV_SATFINITE, __NV_E4M3);
+  const float d = __half2float(__half(__nv_cvt_fp8_to_halfraw(sf8, __NV_E4M3))) * g;
+  sf_code = (uint8_t)sf8;
+  uint64_t q = 0;
+  if (d > 0.f) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float2 r = make_float2(__fdiv_rn(x[2 * i], d), __fdiv_rn(x[2 * i + 1], d));
+      q |= (uint64_t)__nv_cvt_float2_to_fp4x2(r, __NV_E2M1, cudaRoundNearest) << (8 * i);
+    }
+  }
+  return q;
 }
 
 // Block-wide max of non-negative values over kThreads threads; every thread gets it.

@@ -87,15 +87,26 @@ constexpr int L2_PREFETCH_AHEAD = 8;     // weight tiles prefetched into L2 ahea
 
 enum Kind { kGemm1 = 0, kGemm2 = 1 };
 
-template <bool kFP8, int kMG>
+// kFP4: NVFP4 operands (packed E2M1 pairs, 256 K elements per 128-byte row) with
+// their E4M3 block scales staged beside each stage's tiles: 128 A rows and 256
+// weight rows of 16 scale bytes (one per 16 K elements) per stage.
+constexpr int SFA_BYTES = BM * 16;
+constexpr int SFB_BYTES = 2 * 128 * 16;
+// tensor memory of the NVFP4 GEMMs: one accumulator (columns 0-255) and, per
+// stage, the block scales of its 4 MMAs: 4 A columns and 8 weight columns each
+// (the layout of mma_nvf4), from column 256 on
+constexpr int SF_TMEM_BASE = 256;
+constexpr int SF_TMEM_STAGE = 4 * 4 + 4 * 8;
+
+template <bool kFP8, int kMG, bool kFP4 = false>
 struct Cfg {
   static constexpr int MG = kMG;  // M tiles per unit
   static constexpr int STAGES = kMG == 2 ? 3 : 4;
-  static constexpr int STAGE_BYTES = MG * A_BYTES + 2 * B_HALF_BYTES;
-  static constexpr int kElemBytes = kFP8 ? 1 : 2;
-  static constexpr int kBK = BKB / kElemBytes;  // K elements per stage
-  static constexpr int kMmaK = kFP8 ? 32 : 16;  // K per tcgen05.mma
-  static constexpr uint32_t kIdesc = make_idesc(kFP8 ? 0u : 1u, BM, BN);
+  static constexpr int STAGE_BYTES = MG * A_BYTES + 2 * B_HALF_BYTES + (kFP4 ? SFA_BYTES + SFB_BYTES : 0);
+  static constexpr int kBK = kFP4 ? 2 * BKB : (kFP8 ? BKB : BKB / 2);  // K elements per stage
+  static constexpr int kMapK = kFP4 ? BKB : kBK;  // the same in units of the tensor maps' elements
+  static constexpr int kMmaBytes = 32;            // bytes of K per tcgen05.mma (K = 16 bf16, 32 fp8, 64 fp4)
+  static constexpr uint32_t kIdesc = kFP4 ? make_idesc_nvf4(BM, BN) : make_idesc(kFP8 ? 0u : 1u, BM, BN);
   static constexpr int PARTIAL_FLOATS = MG * BM * BN;  // one split-unit partial
   // fp8: ring of per-K-block scales (128 activation-row scales + 2 weight-block scales)
   static constexpr int SCALE_SLOTS = 8;
@@ -103,6 +114,8 @@ struct Cfg {
   static constexpr int SCALE_RING_BYTES = kFP8 ? SCALE_SLOTS * SCALE_SLOT_FLOATS * 4 : 0;
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 4096 /*barriers, exchange*/ + SCALE_RING_BYTES +
                                     1024 /*align*/;
+  static_assert(!kFP4 || (!kFP8 && kMG == 1), "NVFP4 units hold one M tile");
+  static_assert(!kFP4 || SF_TMEM_BASE + STAGES * SF_TMEM_STAGE <= TMEM_COLS, "NVFP4 scales must fit the TMEM");
 };
 
 struct GemmParams {
@@ -119,6 +132,8 @@ struct GemmParams {
   int a_kstride;               // fp8: stride of a_scale_t between K blocks (0: one scale per row)
   const float* a_scale_t;      // fp8: [K/128][a_kstride] scales of the A rows
   const float* w_scale;        // fp8: [E][b_rows/128][K/128]
+  const float* a_gscale;       // NVFP4: [1] global scale of the A rows
+  const float* w_gscale;       // NVFP4: [E] global scale of each expert's weights
   void* out;                   // gemm1: h [rows][I]; gemm2: y [T*k][H] bf16
   float* out_scale_t;          // gemm1 fp8: [I/128][s_pad]
   int allow_split;             // decode-sized problem: few units may be split across CTAs (bf16 only)
@@ -273,13 +288,14 @@ __device__ __forceinline__ void fma2(float& a0, float& a1, float v0, float v1, f
       : "f"(v0), "f"(v1), "f"(s));
 }
 
-template <bool kFP8, int kKind, int kMG, int kAct, bool kHB16>
+template <bool kFP8, int kKind, int kMG, int kAct, bool kHB16, bool kFP4>
 __global__ void __launch_bounds__(Warps<kFP8>::THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
                 const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmA_1,
                 const __grid_constant__ CUtensorMap tmA2_1, const __grid_constant__ CUtensorMap tmB_1,
+                const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
                 const __grid_constant__ GemmProblems pp) {
-  using C = Cfg<kFP8, kMG>;
+  using C = Cfg<kFP8, kMG, kFP4>;
   // gemm1 forms: a gated activation reads 128 gate + 128 up rows per unit (one 3-D
   // box); a *_NO_MUL one reads 256 consecutive gate rows, like gemm2
   constexpr bool kNoMul = kKind == kGemm1 && (kAct == MOE_ACT_SILU_NO_MUL || kAct == MOE_ACT_GELU_NO_MUL);
@@ -303,6 +319,7 @@ __global__ void __launch_bounds__(Warps<kFP8>::THREADS, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sempty + C::SCALE_SLOTS);
   float* scale_ring = reinterpret_cast<float*>(ctrl + 4096);  // fp8: [SCALE_SLOTS][SCALE_SLOT_FLOATS]
   float* amax_x = reinterpret_cast<float*>(ctrl + 256);  // [2 items][2 halves][BM]
+  uint64_t* sfready = reinterpret_cast<uint64_t*>(ctrl + 3072);  // NVFP4: [STAGES] stage's scales in TMEM
   // bf16 split units: the finished rows (own accumulator + later segments' partials),
   // [BM][FIX_STRIDE] fp32 over the stage buffers
   constexpr int FIX_STRIDE = 257;  // odd stride: row-per-thread writes hit distinct banks
@@ -320,6 +337,8 @@ __global__ void __launch_bounds__(Warps<kFP8>::THREADS, 1)
       mbar_init(&tempty[a], EPI_WARPS);  // one arrival per epilogue warp
     }
     mbar_init(xbar, EPI_WARPS);
+    if (kFP4)
+      for (int st = 0; st < STAGES; ++st) mbar_init(&sfready[st], EPI_WARPS);
     mbar_init(drain, 1);
     mbar_init(fixbar, 1);
     for (int i = 0; i < C::SCALE_SLOTS; ++i) {
@@ -330,6 +349,10 @@ __global__ void __launch_bounds__(Warps<kFP8>::THREADS, 1)
     prefetch_tensormap(&tmA);
     if (MG == 2) prefetch_tensormap(&tmA2);
     prefetch_tensormap(&tmB);
+    if (kFP4) {
+      prefetch_tensormap(&tmSA);
+      prefetch_tensormap(&tmSB);
+    }
     if (pp.nprob > 1) {
       prefetch_tensormap(&tmA_1);
       if (MG == 2) prefetch_tensormap(&tmA2_1);
@@ -376,9 +399,9 @@ __global__ void __launch_bounds__(Warps<kFP8>::THREADS, 1)
       if (issue) {
         const CUtensorMap* mB = pf_prob ? &tmB_1 : &tmB;
         if (kPair)
-          tma_prefetch_3d(mB, pf_kb * C::kBK, pit.n * 128, 2 * pit.e);
+          tma_prefetch_3d(mB, pf_kb * C::kMapK, pit.n * 128, 2 * pit.e);
         else
-          tma_prefetch_2d(mB, pf_kb * C::kBK, pit.e * pp.p[pf_prob].b_rows + pit.n * 256);
+          tma_prefetch_2d(mB, pf_kb * C::kMapK, pit.e * pp.p[pf_prob].b_rows + pit.n * 256);
       }
       ++pf_kb;
     };
@@ -426,8 +449,18 @@ __global__ void __launch_bounds__(Warps<kFP8>::THREADS, 1)
         if (lane == 0) {
           uint8_t* sA = smem + stage * C::STAGE_BYTES;
           uint8_t* sB = sA + MG * A_BYTES;
-          mbar_arrive_expect_tx(&full[stage], mcnt * A_BYTES + 2 * B_HALF_BYTES);
-          const int kx = kb * C::kBK;
+          mbar_arrive_expect_tx(&full[stage],
+                                mcnt * A_BYTES + 2 * B_HALF_BYTES + (kFP4 ? SFA_BYTES + SFB_BYTES : 0));
+          const int kx = kb * C::kMapK;
+          if (kFP4) {
+            // the block scales of the stage: 16 bytes of each A row and of each weight row
+            uint8_t* sSF = sB + 2 * B_HALF_BYTES;
+            tma_load_2d(sSF, &tmSA, kb * 16, it.row0, &full[stage], pol_a);
+            if (kPair)
+              tma_load_3d(sSF + SFA_BYTES, &tmSB, kb * 16, brow, 2 * it.e, &full[stage], pol_b);
+            else
+              tma_load_2d(sSF + SFA_BYTES, &tmSB, kb * 16, brow, &full[stage], pol_b);
+          }
           if (MG == 2 && mcnt == 2)
             tma_load_2d(sA, mA2, kx, it.row0, &full[stage], pol_a);  // both M tiles, one 256-row box
           else
@@ -482,6 +515,7 @@ __global__ void __launch_bounds__(Warps<kFP8>::THREADS, 1)
           tc_fence_after();
         }
         if (!(ok = warp_wait(&full[stage], phase))) break;
+        if (kFP4 && !(ok = warp_wait(&sfready[stage], phase))) break;  // the stage's scales are in TMEM
         tc_fence_after();
         if (lane == 0) {
           const uint32_t a0 = smem_u32(smem + stage * C::STAGE_BYTES);
@@ -489,10 +523,14 @@ __global__ void __launch_bounds__(Warps<kFP8>::THREADS, 1)
           for (int m = 0; m < mcnt; ++m) {
             const uint32_t d = tmem + ((kFP8 || MG == 1) ? acc * BN : m * BN);
 #pragma unroll
-            for (int kk = 0; kk < BKB / (C::kMmaK * C::kElemBytes); ++kk) {
-              const uint32_t koff = kk * C::kMmaK * C::kElemBytes;
+            for (int kk = 0; kk < BKB / C::kMmaBytes; ++kk) {
+              const uint32_t koff = kk * C::kMmaBytes;
               const uint32_t accum = kFP8 ? (kk > 0) : (kb > kb0 || kk > 0);
-              if (kFP8)
+              if (kFP4) {
+                const uint32_t sf = tmem + SF_TMEM_BASE + stage * SF_TMEM_STAGE;
+                mma_nvf4(d, sw128_desc(a0 + koff), sw128_desc(b0 + koff), C::kIdesc, sf + 4 * kk, sf + 16 + 8 * kk,
+                         accum);
+              } else if (kFP8)
                 mma_fp8(d, sw128_desc(a0 + m * A_BYTES + koff), sw128_desc(b0 + koff), C::kIdesc, accum);
               else
                 mma_bf16(d, sw128_desc(a0 + m * A_BYTES + koff), sw128_desc(b0 + koff), C::kIdesc, accum);
@@ -514,7 +552,7 @@ __global__ void __launch_bounds__(Warps<kFP8>::THREADS, 1)
       if (!kFP8 && ok) {
         if (lane == 0) tc_commit(&tfull[acc]);
         __syncwarp();
-        if (MG == 1) acc ^= 1;
+        if (MG == 1 && !kFP4) acc ^= 1;  // (NVFP4: one accumulator, the scales take the other half)
         if (acc == 0) acc_phase ^= 1;
       }
     }
@@ -531,6 +569,8 @@ __global__ void __launch_bounds__(Warps<kFP8>::THREADS, 1)
     int xbuf = 0;
     uint32_t xphase = 0;
     long long sfill = 0;  // fp8: K blocks consumed from the scale ring
+    int fstage = 0;       // NVFP4: stages whose scales this warp has put in TMEM
+    uint32_t fphase = 0;
     bool ok = true;
     while (ok && sched.next(u, kb0, kb1)) {
       const int prob = u >= units0;
@@ -549,6 +589,54 @@ __global__ void __launch_bounds__(Warps<kFP8>::THREADS, 1)
       // thread-private slot of a split-unit partial (bf16): 256 columns of (M tile m, row r)
       // at poff + m * BM * 256
       const size_t poff = (size_t)r * 256;
+      // NVFP4: the accumulators hold sums of (E2M1 x block scale) products; the two
+      // operands' global scales multiply the finished sums
+      const float alpha = kFP4 ? __ldg(p.a_gscale) * __ldg(p.w_gscale + it.e) : 1.0f;
+      if (kFP4) {
+        // Before the unit's epilogue, every K block's block scales go from the stage
+        // into tensor memory in the layout mma_nvf4 reads; each warp writes the same
+        // copy into its own lane quarter: lane l holds the scale words of A rows
+        // l + 32 c (columns 4 kk + c of the stage's slot, kk the MMA) and of weight
+        // rows 128 hh + l + 32 c (columns 16 + 8 kk + 4 hh + c).
+        bool fed = true;
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!(fed = warp_wait(&full[fstage], fphase))) break;
+          const uint8_t* sSF = smem + fstage * C::STAGE_BYTES + MG * A_BYTES + 2 * B_HALF_BYTES;
+          uint4 ra[4], rb[8];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) ra[c] = *reinterpret_cast<const uint4*>(sSF + (lane + 32 * c) * 16);
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            rb[c] = *reinterpret_cast<const uint4*>(sSF + SFA_BYTES + (128 * (c >> 2) + lane + 32 * (c & 3)) * 16);
+          uint32_t va[16], vb[32];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            va[c] = ra[c].x;
+            va[4 + c] = ra[c].y;
+            va[8 + c] = ra[c].z;
+            va[12 + c] = ra[c].w;
+          }
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            vb[c] = rb[c].x;
+            vb[8 + c] = rb[c].y;
+            vb[16 + c] = rb[c].z;
+            vb[24 + c] = rb[c].w;
+          }
+          const uint32_t col = tmem + lane_addr + SF_TMEM_BASE + fstage * SF_TMEM_STAGE;
+          tmem_st16(col, va);
+          tmem_st32(col + 16, vb);
+          tmem_st_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sfready[fstage]);
+          if (++fstage == STAGES) {
+            fstage = 0;
+            fphase ^= 1;
+          }
+        }
+        if (!(ok = fed)) break;
+      }
 
       if (!kFP8) {
         // one warp per TMEM lane quarter: rows r of each M tile of the group, 8 chunks of
@@ -600,7 +688,7 @@ __global__ void __launch_bounds__(Warps<kFP8>::THREADS, 1)
 #pragma unroll
               for (int k = 0; k < 4; ++k) {
                 const int i = i0 + k * EPI_THREADS;
-                if (i < n) fix[(i >> 8) * FIX_STRIDE + (i & 255)] = a[k];
+                if (i < n) fix[(i >> 8) * FIX_STRIDE + (i & 255)] = a[k] * alpha;
               }
             }
           }
@@ -645,7 +733,7 @@ __global__ void __launch_bounds__(Warps<kFP8>::THREADS, 1)
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&tempty[acc]);
-          if (MG == 1) acc ^= 1;
+          if (MG == 1 && !kFP4) acc ^= 1;
           if (acc == 0) acc_phase ^= 1;
           continue;
         }
@@ -676,6 +764,13 @@ __global__ void __launch_bounds__(Warps<kFP8>::THREADS, 1)
               tmem_ld32(tb + c * 32, g);
               tmem_ld32(tb + 128 + c * 32, uu);
               tmem_ld_wait();
+              if (kFP4) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                  g[j] *= alpha;
+                  uu[j] *= alpha;
+                }
+              }
               if (mvalid) {
                 uint4* dst = reinterpret_cast<uint4*>(hrow + c * 32);
 #pragma unroll
@@ -697,6 +792,10 @@ __global__ void __launch_bounds__(Warps<kFP8>::THREADS, 1)
               float v[32];
               tmem_ld32(tb + c * 32, v);
               tmem_ld_wait();
+              if (kFP4) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] *= alpha;
+              }
               if (mvalid && c * 32 < ncols) {
                 uint4* dst = reinterpret_cast<uint4*>(hrow + c * 32);
 #pragma unroll
@@ -719,6 +818,10 @@ __global__ void __launch_bounds__(Warps<kFP8>::THREADS, 1)
               float v[32];
               tmem_ld32(tb + c * 32, v);
               tmem_ld_wait();
+              if (kFP4) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] *= alpha;
+              }
               if (mvalid && c * 32 < ncols) {
                 uint4* dst = reinterpret_cast<uint4*>(yrow + c * 32);
 #pragma unroll
@@ -738,7 +841,7 @@ __global__ void __launch_bounds__(Warps<kFP8>::THREADS, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&tempty[acc]);
-        if (MG == 1) acc ^= 1;
+        if (MG == 1 && !kFP4) acc ^= 1;
         if (acc == 0) acc_phase ^= 1;
       } else {
         // fp8: promote every K block's partial into registers.
@@ -970,12 +1073,14 @@ __global__ void __launch_bounds__(1024)
 }
 
 // gather: one warp per sorted row p.  Copies the row of token sorted_slot[p]/k
-// (unless codes are not wanted) and, for fp8, writes its scales transposed.
+// (unless codes are not wanted) and, for fp8, writes its scales transposed; for
+// NVFP4 it also copies the row's block-scale bytes (sf_bytes of a1q_sf) to ASF.
 __global__ void __launch_bounds__(256)
     gather_kernel(const uint8_t* __restrict__ a1q, const float* __restrict__ a1q_scale,
                   const int32_t* __restrict__ sorted_slot, int S, int top_k, int row_bytes, int ngroups,
                   uint8_t* __restrict__ A, float* __restrict__ a_scale_t, int s_pad, int scale_stride,
-                  int* __restrict__ flags, int nflags) {
+                  int* __restrict__ flags, int nflags, const uint8_t* __restrict__ a1q_sf, int sf_bytes,
+                  uint8_t* __restrict__ ASF) {
   // (when no plan launch runs, the gather also clears the split-unit flags)
   for (int i = blockIdx.x * 256 + threadIdx.x; i < nflags; i += gridDim.x * 256) flags[i] = 0;
   const int p = blockIdx.x * 8 + (threadIdx.x >> 5);
@@ -991,6 +1096,45 @@ __global__ void __launch_bounds__(256)
   if (a_scale_t)
     for (int g = lane; g < ngroups; g += 32)
       a_scale_t[(size_t)g * s_pad + p] = __ldg(a1q_scale + (size_t)t * scale_stride + g);
+  if (ASF) {
+    const uint4* src = reinterpret_cast<const uint4*>(a1q_sf + (size_t)t * sf_bytes);
+    uint4* dst = reinterpret_cast<uint4*>(ASF + (size_t)p * sf_bytes);
+    for (int i = lane; i < sf_bytes / 16; i += 32) dst[i] = __ldg(src + i);
+  }
+}
+
+// NVFP4 quantiser of bf16 rows [rows][C] (one thread per 16-element group, see
+// nvfp4_group16), with the global scale at g: packed codes q [rows][C/2] and
+// scale codes sf [rows][C/16].  rows = *nrows when nrows is given (the experts'
+// intermediate: expert_offsets[E]), else max_rows.  weights (the prepare step's
+// weight on the input, top-k 1): each row is first multiplied by bf16(weights[row])
+// and rounded to bf16.
+__global__ void __launch_bounds__(256)
+    nvfp4_quant_kernel(const __nv_bfloat16* __restrict__ x, int C, long long max_rows,
+                       const int32_t* __restrict__ nrows, const float* __restrict__ weights,
+                       const float* __restrict__ g, uint8_t* __restrict__ q, uint8_t* __restrict__ sf) {
+  const long long i = (long long)blockIdx.x * 256 + threadIdx.x;  // group index
+  const int gpr = C / 16;
+  const long long rows = nrows ? (long long)__ldg(nrows) : max_rows;
+  if (i >= rows * gpr) return;
+  const long long row = i / gpr;
+  float v[16];
+  float a[8];
+  load_bf16x8(x + i * 16, a);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) v[j] = a[j];
+  load_bf16x8(x + i * 16 + 8, a);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) v[8 + j] = a[j];
+  if (weights) {
+    const float w = __bfloat162float(__float2bfloat16_rn(__ldg(weights + row)));
+#pragma unroll
+    for (int j = 0; j < 16; ++j) v[j] = __bfloat162float(__float2bfloat16_rn(v[j] * w));
+  }
+  uint8_t code;
+  const uint64_t packed = nvfp4_group16(v, __ldg(g), code);
+  reinterpret_cast<uint2*>(q)[i] = make_uint2((uint32_t)packed, (uint32_t)(packed >> 32));
+  sf[i] = code;
 }
 
 // The "A" and "T" formats' intermediate: h rows [rows][I] in bf16 (rows =
@@ -1090,38 +1234,70 @@ bool make_map_gate_up(CUtensorMap* m, const void* base, bool fp8, long long k, l
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Tensor maps of one problem for one GEMM: A with one-tile and two-tile boxes, weights.
+// Block-scale rows of an NVFP4 operand: 2-D map over [rows][row_bytes] bytes with a
+// box of 16 bytes (one stage's 256 K elements) x box_rows rows, no swizzle.
+bool make_map_sf(CUtensorMap* m, const void* base, long long row_bytes, long long rows, int box_rows) {
+  auto enc = get_encode();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)row_bytes, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
+  cuuint32_t box[2] = {16, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The gate/up block-scale rows of w13 viewed as [2E][I][row_bytes] (the scale
+// counterpart of make_map_gate_up): a box of 16 bytes x 128 rows x 2.
+bool make_map_sf_gate_up(CUtensorMap* m, const void* base, long long row_bytes, long long I, long long E) {
+  auto enc = get_encode();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)row_bytes, (cuuint64_t)I, (cuuint64_t)(2 * E)};
+  cuuint64_t strides[2] = {(cuuint64_t)row_bytes, (cuuint64_t)(I * row_bytes)};
+  cuuint32_t box[3] = {16, 128, 2};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Tensor maps of one problem for one GEMM: A with one-tile and two-tile boxes,
+// weights; NVFP4: the block-scale rows of A and of the weights.
 struct GemmMaps {
-  CUtensorMap a, a2, b;
+  CUtensorMap a, a2, b, sa, sb;
 };
 
-template <bool kFP8, int kKind, int kMG, int kAct, bool kHB16 = false>
+template <bool kFP8, int kKind, int kMG, int kAct, bool kHB16 = false, bool kFP4 = false>
 cudaError_t launch_gemm(const GemmMaps* m, const GemmProblems& pp, int grid, cudaStream_t s) {
+  using C = Cfg<kFP8, kMG, kFP4>;
   static int configured[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_kernel<kFP8, kKind, kMG, kAct, kHB16>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<kFP8, kMG>::SMEM_BYTES);
+    cudaError_t e = cudaFuncSetAttribute(gemm_kernel<kFP8, kKind, kMG, kAct, kHB16, kFP4>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     configured[dev] = 1;
   }
   const GemmMaps& m1 = pp.nprob > 1 ? m[1] : m[0];
-  gemm_kernel<kFP8, kKind, kMG, kAct, kHB16><<<grid, Warps<kFP8>::THREADS, Cfg<kFP8, kMG>::SMEM_BYTES, s>>>(
-      m[0].a, m[0].a2, m[0].b, m1.a, m1.a2, m1.b, pp);
+  gemm_kernel<kFP8, kKind, kMG, kAct, kHB16, kFP4><<<grid, Warps<kFP8>::THREADS, C::SMEM_BYTES, s>>>(
+      m[0].a, m[0].a2, m[0].b, m1.a, m1.a2, m1.b, m[0].sa, m[0].sb, pp);
   return cudaGetLastError();
 }
 
 // gemm1 with the activation chosen at run time (kHB16: fp8 mainloop, bf16 h out)
-template <bool kFP8, int kMG, bool kHB16 = false>
+template <bool kFP8, int kMG, bool kHB16 = false, bool kFP4 = false>
 cudaError_t launch_gemm1(int act, const GemmMaps* m, const GemmProblems& pp, int grid, cudaStream_t s) {
   switch (act) {
-    case MOE_ACT_SILU: return launch_gemm<kFP8, kGemm1, kMG, MOE_ACT_SILU, kHB16>(m, pp, grid, s);
-    case MOE_ACT_GELU: return launch_gemm<kFP8, kGemm1, kMG, MOE_ACT_GELU, kHB16>(m, pp, grid, s);
-    case MOE_ACT_GELU_TANH: return launch_gemm<kFP8, kGemm1, kMG, MOE_ACT_GELU_TANH, kHB16>(m, pp, grid, s);
-    case MOE_ACT_SWIGLUOAI: return launch_gemm<kFP8, kGemm1, kMG, MOE_ACT_SWIGLUOAI, kHB16>(m, pp, grid, s);
-    case MOE_ACT_SILU_NO_MUL: return launch_gemm<kFP8, kGemm1, kMG, MOE_ACT_SILU_NO_MUL, kHB16>(m, pp, grid, s);
-    case MOE_ACT_GELU_NO_MUL: return launch_gemm<kFP8, kGemm1, kMG, MOE_ACT_GELU_NO_MUL, kHB16>(m, pp, grid, s);
+    case MOE_ACT_SILU: return launch_gemm<kFP8, kGemm1, kMG, MOE_ACT_SILU, kHB16, kFP4>(m, pp, grid, s);
+    case MOE_ACT_GELU: return launch_gemm<kFP8, kGemm1, kMG, MOE_ACT_GELU, kHB16, kFP4>(m, pp, grid, s);
+    case MOE_ACT_GELU_TANH: return launch_gemm<kFP8, kGemm1, kMG, MOE_ACT_GELU_TANH, kHB16, kFP4>(m, pp, grid, s);
+    case MOE_ACT_SWIGLUOAI: return launch_gemm<kFP8, kGemm1, kMG, MOE_ACT_SWIGLUOAI, kHB16, kFP4>(m, pp, grid, s);
+    case MOE_ACT_SILU_NO_MUL:
+      return launch_gemm<kFP8, kGemm1, kMG, MOE_ACT_SILU_NO_MUL, kHB16, kFP4>(m, pp, grid, s);
+    case MOE_ACT_GELU_NO_MUL:
+      return launch_gemm<kFP8, kGemm1, kMG, MOE_ACT_GELU_NO_MUL, kHB16, kFP4>(m, pp, grid, s);
   }
   return cudaErrorInvalidValue;
 }
@@ -1264,7 +1440,7 @@ moe_status_t experts_run(const moe_experts_problem* probs, int nprob, int H, con
   }
   const bool split1 = allow_split && H / 64 >= 32, split2 = allow_split && pr[0].I / 64 >= 32;
 
-  GemmMaps maps1[kMaxProblems], maps2[kMaxProblems];
+  GemmMaps maps1[kMaxProblems] = {}, maps2[kMaxProblems] = {};
   GemmProblems g1 = {}, g2 = {};
   g1.nprob = g2.nprob = n;
   int* flags_all = reinterpret_cast<int*>(wsb + L.flags);
@@ -1298,7 +1474,8 @@ moe_status_t experts_run(const moe_experts_problem* probs, int nprob, int H, con
       gather_kernel<<<gb, 256, 0, s>>>(static_cast<const uint8_t*>(q.a1q), q.a1q_scale, q.sorted_slot, (int)S,
                                        q.top_k, H * esz, hb16 ? 1 : H / 128, gather_rows ? wsb + P.A : nullptr, As,
                                        P.s_pad, group == 128 ? H / 128 : (group == MOE_GROUP_TOKEN ? 1 : 0),
-                                       flags_pending ? flags_all : nullptr, flags_pending ? L.nflags : 0);
+                                       flags_pending ? flags_all : nullptr, flags_pending ? L.nflags : 0, nullptr,
+                                       0, nullptr);
       flags_pending = false;
       if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
     }
@@ -1407,6 +1584,138 @@ moe_experts_problem one_problem(const void* a1q, const float* a1q_scale, const v
   return q;
 }
 
+// ------------------------------------------------------------------ NVFP4 experts
+// Workspace of an NVFP4 call: gathered A rows and their scale rows, the bf16
+// intermediate, its NVFP4 codes and scales, the split flags of both GEMMs and one
+// split partial per CTA.
+struct Fp4Layout {
+  size_t A, ASF, hb, hq, hsf, flags, partials, total;
+  int nflags1, nflags2;
+};
+
+Fp4Layout ws_layout_nvfp4(long long S, int H, int I, int E, int grid) {
+  Fp4Layout L{};
+  const int cap_groups = std::max(1, moe_tile_map_capacity((int)S, E, BM));
+  L.nflags1 = cap_groups * (I / 128);
+  L.nflags2 = cap_groups * (H / 256);
+  size_t off = 0;
+  L.A = off;
+  off = al256(off + (size_t)S * H / 2);
+  L.ASF = off;
+  off = al256(off + (size_t)S * H / 16);
+  L.hb = off;
+  off = al256(off + (size_t)S * I * 2);
+  L.hq = off;
+  off = al256(off + (size_t)S * I / 2);
+  L.hsf = off;
+  off = al256(off + (size_t)S * I / 16);
+  L.flags = off;
+  off = al256(off + (size_t)(L.nflags1 + L.nflags2) * 4);
+  L.partials = off;
+  off = al256(off + (size_t)grid * BM * BN * 4);
+  L.total = off;
+  return L;
+}
+
+// gather (+ scale rows) -> gemm1 (bf16 h) -> NVFP4 quantisation of h -> gemm2
+moe_status_t experts_nvfp4_run(const void* a1q, const void* a1q_sf, const float* a1_gscale, const void* w13,
+                               const void* w13_sf, const float* w13_gscale, const void* w2, const void* w2_sf,
+                               const float* w2_gscale, const float* h_gscale, const int32_t* expert_offsets,
+                               const int32_t* sorted_slot, const int32_t* tile_map, const int32_t* num_tiles, int T,
+                               int H, int I, int E, int top_k, int activation, void* out, void* ws, size_t ws_bytes,
+                               cudaStream_t s) {
+  if (activation < MOE_ACT_SILU || activation > MOE_ACT_GELU_NO_MUL) return MOE_ERR_UNSUPPORTED;
+  MOE_CHECK_ARG(T >= 0 && H > 0 && H % 256 == 0 && I > 0 && I % 256 == 0 && E >= 1 && top_k >= 1 && top_k <= E);
+  const long long S = (long long)T * top_k;
+  MOE_CHECK_ARG(fits_int32(S + 4 * BM) && fits_int32((long long)E * 2 * I) && fits_int32((long long)E * H) &&
+                fits_int32((long long)H * 8));
+  if (S == 0) return MOE_OK;
+  MOE_CHECK_ARG(a1q && a1q_sf && a1_gscale && w13 && w13_sf && w13_gscale && w2 && w2_sf && w2_gscale && h_gscale &&
+                expert_offsets && tile_map && num_tiles && out);
+  MOE_CHECK_ARG(sorted_slot || (E == 1 && top_k == 1));
+  MOE_CHECK_ARG(aligned16(a1q) && aligned16(a1q_sf) && aligned16(w13) && aligned16(w13_sf) && aligned16(w2) &&
+                aligned16(w2_sf) && aligned16(out));
+  const bool no_mul = activation == MOE_ACT_SILU_NO_MUL || activation == MOE_ACT_GELU_NO_MUL;
+  const int grid = gemm_grid();
+  const Fp4Layout L = ws_layout_nvfp4(S, H, I, E, grid);
+  if (!ws || ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+  MOE_CHECK_ARG(aligned16(ws));
+  uint8_t* wsb = static_cast<uint8_t*>(ws);
+  // decode-sized problems split units across CTAs, as in the bf16 path
+  const bool allow_split = S <= 16LL * E;
+  const bool split1 = allow_split && H / 64 >= 32, split2 = allow_split && I / 64 >= 32;
+  int* flags = reinterpret_cast<int*>(wsb + L.flags);
+  const int nflags = L.nflags1 + L.nflags2;
+  const bool split = split1 || split2;
+  const bool gather_rows = sorted_slot != nullptr;
+  if (gather_rows) {
+    gather_kernel<<<(unsigned)((S + 7) / 8), 256, 0, s>>>(
+        static_cast<const uint8_t*>(a1q), nullptr, sorted_slot, (int)S, top_k, H / 2, 0, wsb + L.A, nullptr, 0, 0,
+        split ? flags : nullptr, split ? nflags : 0, static_cast<const uint8_t*>(a1q_sf), H / 16, wsb + L.ASF);
+  } else if (split) {
+    plan_kernel<<<1, 1024, 0, s>>>(tile_map, num_tiles, expert_offsets, 1, 1, nullptr, nullptr, nullptr, nullptr,
+                                   flags, nflags);
+  }
+  if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+  const void* A = gather_rows ? (const void*)(wsb + L.A) : a1q;
+  const void* ASF = gather_rows ? (const void*)(wsb + L.ASF) : a1q_sf;
+  void* hb = wsb + L.hb;
+  uint8_t* hq = wsb + L.hq;
+  uint8_t* hsf = wsb + L.hsf;
+  // packed operands are uint8 maps over rows of K/2 bytes; scale rows are K/16 bytes
+  GemmMaps m1 = {}, m2 = {};
+  const bool b1 = no_mul ? make_map(&m1.b, w13, true, H / 2, (long long)E * I, 256)
+                         : make_map_gate_up(&m1.b, w13, true, H / 2, I, E);
+  const bool sb1 = no_mul ? make_map_sf(&m1.sb, w13_sf, H / 16, (long long)E * I, 256)
+                          : make_map_sf_gate_up(&m1.sb, w13_sf, H / 16, I, E);
+  if (!b1 || !sb1 || !make_map(&m1.a, A, true, H / 2, S, 128) || !make_map(&m1.a2, A, true, H / 2, S, 128) ||
+      !make_map_sf(&m1.sa, ASF, H / 16, S, 128) || !make_map(&m2.a, hq, true, I / 2, S, 128) ||
+      !make_map(&m2.a2, hq, true, I / 2, S, 128) || !make_map_sf(&m2.sa, hsf, I / 16, S, 128) ||
+      !make_map(&m2.b, w2, true, I / 2, (long long)E * H, 256) ||
+      !make_map_sf(&m2.sb, w2_sf, I / 16, (long long)E * H, 256))
+    return MOE_ERR_CUDA;
+
+  GemmProblems g1 = {}, g2 = {};
+  g1.nprob = g2.nprob = 1;
+  GemmParams& p1 = g1.p[0];
+  p1.offsets = expert_offsets;
+  p1.group_map = tile_map;
+  p1.num_groups = num_tiles;
+  p1.sorted_slot = sorted_slot;
+  p1.K = H;
+  p1.NT = no_mul ? (I + 255) / 256 : I / 128;
+  p1.I = I;
+  p1.H = H;
+  p1.b_rows = no_mul ? I : 2 * I;
+  p1.a_gscale = a1_gscale;
+  p1.w_gscale = w13_gscale;
+  p1.out = hb;
+  p1.flags = flags;
+  p1.partials = reinterpret_cast<float*>(wsb + L.partials);
+  p1.allow_split = split1;
+  GemmParams& p2 = g2.p[0];
+  p2 = p1;
+  p2.K = I;
+  p2.NT = H / 256;
+  p2.b_rows = H;
+  p2.a_gscale = h_gscale;
+  p2.w_gscale = w2_gscale;
+  p2.out = out;
+  p2.flags = flags + L.nflags1;
+  p2.allow_split = split2;
+
+  cudaError_t e = launch_gemm1<false, 1, false, true>(activation, &m1, g1, grid, s);
+  if (e == cudaSuccess) {
+    const long long groups = S * (I / 16);
+    nvfp4_quant_kernel<<<(unsigned)((groups + 255) / 256), 256, 0, s>>>(static_cast<const __nv_bfloat16*>(hb), I, S,
+                                                                        expert_offsets + E, nullptr, h_gscale, hq,
+                                                                        hsf);
+    e = cudaGetLastError();
+  }
+  if (e == cudaSuccess) e = launch_gemm<false, kGemm2, 1, 0, false, true>(&m2, g2, grid, s);
+  return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
 }  // namespace
 
 MOE_DEFINE_STATUS_READER(experts_status)
@@ -1454,4 +1763,37 @@ extern "C" moe_status_t moe_experts(const void* a1q, const float* a1q_scale, con
                                     void* fused_expert_output, void* ws, size_t ws_bytes, moe_stream_t stream) {
   return moe_experts_act(a1q, a1q_scale, w13, w13_scale, w2, w2_scale, expert_offsets, sorted_slot, tile_map,
                          num_tiles, T, H, I, E, top_k, qc, MOE_ACT_SILU, fused_expert_output, ws, ws_bytes, stream);
+}
+
+extern "C" size_t moe_workspace_size_nvfp4(int T, int H, int I, int E, int top_k) {
+  if (T < 0 || H <= 0 || H % 256 || I <= 0 || I % 256 || E < 1 || top_k < 1) return 0;
+  return ws_layout_nvfp4((long long)T * top_k, H, I, E, gemm_grid()).total;
+}
+
+extern "C" moe_status_t moe_experts_nvfp4(const void* a1q, const void* a1q_sf, const float* a1_gscale,
+                                          const void* w13, const void* w13_sf, const float* w13_gscale,
+                                          const void* w2, const void* w2_sf, const float* w2_gscale,
+                                          const float* h_gscale, const int32_t* expert_offsets,
+                                          const int32_t* sorted_slot, const int32_t* tile_map,
+                                          const int32_t* num_tiles, int T, int H, int I, int E, int top_k,
+                                          int activation, void* fused_expert_output, void* ws, size_t ws_bytes,
+                                          moe_stream_t stream) {
+  return experts_nvfp4_run(a1q, a1q_sf, a1_gscale, w13, w13_sf, w13_gscale, w2, w2_sf, w2_gscale, h_gscale,
+                           expert_offsets, sorted_slot, tile_map, num_tiles, T, H, I, E, top_k, activation,
+                           fused_expert_output, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" moe_status_t moe_prepare_nvfp4(const void* a1, const float* topk_weights, int T, int H, int top_k,
+                                          int apply_router_weight_on_input, const float* a1_gscale, void* a1q,
+                                          void* a1q_sf, moe_stream_t stream) {
+  MOE_CHECK_ARG(T >= 0 && H > 0 && H % 16 == 0 && top_k >= 1);
+  MOE_CHECK_ARG(!apply_router_weight_on_input || (top_k == 1 && topk_weights));
+  MOE_CHECK_ARG(fits_int32((long long)H * 8));
+  if (T == 0) return MOE_OK;
+  MOE_CHECK_ARG(a1 && a1_gscale && a1q && a1q_sf && aligned16(a1) && aligned16(a1q));
+  const long long groups = (long long)T * (H / 16);
+  nvfp4_quant_kernel<<<(unsigned)((groups + 255) / 256), 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+      static_cast<const __nv_bfloat16*>(a1), H, T, nullptr, apply_router_weight_on_input ? topk_weights : nullptr,
+      a1_gscale, static_cast<uint8_t*>(a1q), static_cast<uint8_t*>(a1q_sf));
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

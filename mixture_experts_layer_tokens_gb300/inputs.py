@@ -93,6 +93,13 @@ def _cfgs():
         c[f"finalize{T}"] = LayerConfig(f"finalize{T}", T, 7168, 0, 256, 4, finalize_only=True,
                                         residual=True, rms=True, nvfp4=True, shared_I=1,
                                         description=f"finalize kernel T{T} H7168 top4 + shared + residual + RMSNorm")
+    # every expert operand in NVFP4 (E2M1 + E4M3 per 16 + fp32 global scales)
+    c["mixtral_nvfp4"] = LayerConfig("mixtral_nvfp4", 512, 4096, 14336, 8, 2, quant="nvfp4",
+                                     description="Mixtral-8x7B-like layer T512 H4096 I14336 E8 top2 NVFP4 experts")
+    c["llama1_nvfp4"] = LayerConfig("llama1_nvfp4", 1, 5120, 8192, 16, 1, scoring="sigmoid", weight_on_input=True,
+                                    shared_I=8192, quant="nvfp4",
+                                    description="Llama-4-Scout-like layer T1 H5120 I8192 E16 top1 sigmoid-on-input, "
+                                                "NVFP4 experts + bf16 shared I8192")
     for T in (1, 8, 64, 512):
         c[f"llama{T}"] = LayerConfig(f"llama{T}", T, 5120, 8192, 16, 1, scoring="sigmoid",
                                      weight_on_input=True, shared_I=8192,

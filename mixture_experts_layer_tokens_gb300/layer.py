@@ -4,6 +4,8 @@ allocated once up front (PyTorch allocates, the library computes).
 Step (all on one stream):
   moe_route -> moe_align -> moe_prepare -> moe_experts [-> shared expert via
   moe_experts with one expert and the identity permutation] -> moe_finalize.
+NVFP4 layers use moe_prepare_nvfp4 and moe_experts_nvfp4 (the shared expert
+stays bf16).
 
 The shared expert sees the unweighted bf16 input, as the shared-expert row of
 the flashinfer finalize fusion is added unscaled.
@@ -29,14 +31,25 @@ class MoELayer:
         self.topk_ids = torch.empty((T, k), dtype=torch.int32, device=dev)
         self.topk_weights = torch.empty((T, k), dtype=torch.float32, device=dev)
         self.al = moe.Alignment(T, k, E, dev)
-        fp8 = cfg.quant != "bf16"
+        self.nvfp4 = cfg.quant == "nvfp4"
+        fp8 = cfg.quant != "bf16" and not self.nvfp4
         # bf16 without weight-on-input: prepare is the passthrough (a1q is a1)
-        self.passthrough = not fp8 and not cfg.weight_on_input
-        self.a1q = None if self.passthrough else torch.empty((T, H), dtype=torch.uint8 if fp8 else torch.bfloat16,
-                                                             device=dev)
-        self.a1q_scale = torch.empty(moe.scale_shape(cfg.quant, T, H), dtype=torch.float32, device=dev) if fp8 else None
+        self.passthrough = cfg.quant == "bf16" and not cfg.weight_on_input
         self.y = torch.empty((T * k, H), dtype=torch.bfloat16, device=dev)
-        self.ws = torch.empty(max(moe.workspace_size(T, H, I, E, k, cfg.quant), 16), dtype=torch.uint8, device=dev)
+        if self.nvfp4:
+            # packed codes and one E4M3 scale code per 16 elements; fp32 global scales on the device
+            self.a1q = torch.empty((T, H // 2), dtype=torch.uint8, device=dev)
+            self.a1q_scale = torch.empty((T, H // 16), dtype=torch.uint8, device=dev)
+            self.g_a = torch.tensor([inp.extra["a1_gscale"]], dtype=torch.float32, device=dev)
+            self.g_h = torch.tensor([inp.extra["h_gscale"]], dtype=torch.float32, device=dev)
+            self.ws = torch.empty(max(moe.workspace_size_nvfp4(T, H, I, E, k), 16), dtype=torch.uint8, device=dev)
+        else:
+            self.a1q = None if self.passthrough else torch.empty(
+                (T, H), dtype=torch.uint8 if fp8 else torch.bfloat16, device=dev)
+            self.a1q_scale = (torch.empty(moe.scale_shape(cfg.quant, T, H), dtype=torch.float32, device=dev)
+                              if fp8 else None)
+            self.ws = torch.empty(max(moe.workspace_size(T, H, I, E, k, cfg.quant), 16), dtype=torch.uint8,
+                                  device=dev)
         self.out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
         self.shared = None
         if cfg.shared_I:
@@ -61,6 +74,9 @@ class MoELayer:
         moe.moe_align(self.topk_ids, cfg.E, out=self.al, stream=stream)
         if self.passthrough:
             a1q, a1q_scale = a1, None
+        elif self.nvfp4:
+            a1q, a1q_scale = moe.moe_prepare_nvfp4(a1, self.topk_weights, cfg.top_k, cfg.weight_on_input, self.g_a,
+                                                   self.a1q, self.a1q_scale, stream=stream)
         else:
             a1q, a1q_scale = moe.moe_prepare(a1, self.topk_weights, cfg.top_k, cfg.weight_on_input, cfg.quant,
                                              self.a1q, self.a1q_scale, stream=stream)
@@ -80,8 +96,13 @@ class MoELayer:
                  moe.experts_problem(a1, None, inp.shared_w13, None, inp.shared_w2, None, self.al_shared, self.shared,
                                      identity=True)], cfg.H, "bf16", self.ws_multi, stream=stream)
             return self.shared
-        moe.moe_experts(a1q, a1q_scale, inp.w13, inp.w13_scale, inp.w2, inp.w2_scale, self.al, cfg.quant,
-                        activation=cfg.activation, out=self.y, ws=self.ws, stream=stream)
+        if self.nvfp4:
+            moe.moe_experts_nvfp4(a1q, a1q_scale, self.g_a, inp.w13, inp.w13_scale, inp.extra["w13_gscale"], inp.w2,
+                                  inp.w2_scale, inp.extra["w2_gscale"], self.g_h, self.al, out=self.y, ws=self.ws,
+                                  stream=stream, activation=cfg.activation)
+        else:
+            moe.moe_experts(a1q, a1q_scale, inp.w13, inp.w13_scale, inp.w2, inp.w2_scale, self.al, cfg.quant,
+                            activation=cfg.activation, out=self.y, ws=self.ws, stream=stream)
         if self.shared is None:
             return None
         return moe.moe_experts(a1, None, inp.shared_w13, None, inp.shared_w2, None, self.al_shared, "bf16",

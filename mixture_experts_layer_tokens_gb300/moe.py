@@ -80,6 +80,10 @@ SIGNATURES = {
     "moe_experts_multi": ([_EPP, _I, _I, _QCP, _I, _P, _Z, _P], _I),
     "moe_workspace_size_multi": ([_EPP, _I, _I, _QCP], _Z),
     "moe_workspace_size": ([_I, _I, _I, _I, _I, _QCP], _Z),
+    "moe_prepare_nvfp4": ([_P, _P, _I, _I, _I, _I, _P, _P, _P, _P], _I),
+    "moe_experts_nvfp4": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P,
+                           _Z, _P], _I),
+    "moe_workspace_size_nvfp4": ([_I, _I, _I, _I, _I], _Z),
     "moe_finalize": ([_P, _P, _P, _P, _P, _P, _P, _F, _I, _I, _I, _I, _I, _P, _F, _P, _P], _I),
     "moe_device_status": ([_I], _I),
     "moe_status_string": ([_I], ctypes.c_char_p),
@@ -297,6 +301,72 @@ def moe_experts_multi(problems, H: int, quant: str, ws: torch.Tensor, activation
     _check("moe_experts_multi", lib().moe_experts_multi(arr, len(problems), H, ctypes.byref(_qc(quant)),
                                                         ACTIVATIONS[activation], _ptr(ws), ws.numel(),
                                                         _stream(stream)))
+
+
+def _gscale(g, device, name):
+    """A global scale as the device fp32 tensor the C ABI takes (a Python number is copied)."""
+    if isinstance(g, torch.Tensor):
+        _need(g, torch.float32, name)
+        return g
+    return torch.tensor([float(g)], dtype=torch.float32, device=device)
+
+
+def moe_prepare_nvfp4(a1: torch.Tensor, topk_weights: Optional[torch.Tensor], top_k: int,
+                      apply_router_weight_on_input: bool, a1_gscale, a1q: Optional[torch.Tensor] = None,
+                      a1q_sf: Optional[torch.Tensor] = None, stream=None):
+    """NVFP4 prepare: a1 [T, H] bf16 -> (a1q [T, H/2] codes, a1q_sf [T, H/16] scale
+    codes) with global scale ``a1_gscale`` (number or [1] fp32 device tensor)."""
+    _need(a1, torch.bfloat16, "a1")
+    _need(topk_weights, torch.float32, "topk_weights")
+    T, H = a1.shape
+    g = _gscale(a1_gscale, a1.device, "a1_gscale")
+    if a1q is None:
+        a1q = torch.empty((T, H // 2), dtype=torch.uint8, device=a1.device)
+    if a1q_sf is None:
+        a1q_sf = torch.empty((T, H // 16), dtype=torch.uint8, device=a1.device)
+    _need(a1q, torch.uint8, "a1q")
+    _need(a1q_sf, torch.uint8, "a1q_sf")
+    _check("moe_prepare_nvfp4", lib().moe_prepare_nvfp4(
+        _ptr(a1), _ptr(topk_weights), T, H, top_k, int(bool(apply_router_weight_on_input)), _ptr(g), _ptr(a1q),
+        _ptr(a1q_sf), _stream(stream)))
+    return a1q, a1q_sf
+
+
+def workspace_size_nvfp4(T: int, H: int, I: int, E: int, top_k: int) -> int:
+    return int(lib().moe_workspace_size_nvfp4(T, H, I, E, top_k))
+
+
+def moe_experts_nvfp4(a1q: torch.Tensor, a1q_sf: torch.Tensor, a1_gscale, w13: torch.Tensor,
+                      w13_sf: torch.Tensor, w13_gscale: torch.Tensor, w2: torch.Tensor, w2_sf: torch.Tensor,
+                      w2_gscale: torch.Tensor, h_gscale, al: Alignment, out: Optional[torch.Tensor] = None,
+                      ws: Optional[torch.Tensor] = None, identity: bool = False, stream=None,
+                      activation: str = "silu") -> torch.Tensor:
+    """Grouped expert MLPs with NVFP4 operands (``moe_experts_nvfp4``): packed codes
+    a1q [T, H/2], w13 [E, 2I, H/2] (*_no_mul: [E, I, H/2]), w2 [E, H, I/2] with
+    their scale codes (one per 16 elements) and fp32 global scales."""
+    if activation not in ACTIVATIONS:
+        raise ValueError(f"unknown activation {activation!r}")
+    for t, n in ((a1q, "a1q"), (a1q_sf, "a1q_sf"), (w13, "w13"), (w13_sf, "w13_sf"), (w2, "w2"), (w2_sf, "w2_sf")):
+        _need(t, torch.uint8, n)
+    _need(w13_gscale, torch.float32, "w13_gscale")
+    _need(w2_gscale, torch.float32, "w2_gscale")
+    T, H = a1q.shape[0], a1q.shape[1] * 2
+    E, rows13, _ = w13.shape
+    I = rows13 if activation.endswith("_no_mul") else rows13 // 2
+    k = al.top_k
+    ga = _gscale(a1_gscale, a1q.device, "a1_gscale")
+    gh = _gscale(h_gscale, a1q.device, "h_gscale")
+    if out is None:
+        out = torch.empty((T * k, H), dtype=torch.bfloat16, device=a1q.device)
+    _need(out, torch.bfloat16, "fused_expert_output")
+    if ws is None:
+        ws = torch.empty(max(workspace_size_nvfp4(T, H, I, E, k), 16), dtype=torch.uint8, device=a1q.device)
+    _check("moe_experts_nvfp4", lib().moe_experts_nvfp4(
+        _ptr(a1q), _ptr(a1q_sf), _ptr(ga), _ptr(w13), _ptr(w13_sf), _ptr(w13_gscale), _ptr(w2), _ptr(w2_sf),
+        _ptr(w2_gscale), _ptr(gh), _ptr(al.expert_offsets), None if identity else _ptr(al.sorted_slot),
+        _ptr(al.tile_map), _ptr(al.num_tiles), T, H, I, E, k, ACTIVATIONS[activation], _ptr(out), _ptr(ws),
+        ws.numel(), _stream(stream)))
+    return out
 
 
 def moe_finalize(fused_expert_output: torch.Tensor, topk_weights: Optional[torch.Tensor], top_k: int,

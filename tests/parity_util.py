@@ -55,3 +55,21 @@ def check_fp8(gpu, ref, what="", tol=3e-2):
     g, r, rms, rel, maxabs = stats(gpu, ref)
     assert rel <= tol, f"{what}: relative Frobenius {rel:.3e} > {tol}"
     return rel, maxabs / max(rms, 1e-30)
+
+
+def check_nvfp4(gpu, ref, what="", rel_tol=5e-3, frac_tol=1e-3):
+    """NVFP4 experts: both sides apply the same quantisation steps, so the output
+    matches like a bf16 path (relative Frobenius <= 5e-3; elements within
+    1e-2*RMS + a bf16 ulp) except where the GPU's fp32 accumulation moved a stored
+    bf16 h element to its neighbour and that neighbour rounds to another E2M1 code
+    (or group scale) than the oracle's: such a flip moves whole output rows by one
+    code step of one h element.  Those rows may exceed the element bound; they
+    must be a rare fraction (<= 1e-3 of the elements)."""
+    g, r, rms, rel, maxabs = stats(gpu, ref)
+    bound = 1e-2 * rms + 2.0 * half_ulp_bf16(r)
+    bad = np.abs(g - r) > bound
+    frac = float(bad.mean()) if bad.size else 0.0
+    assert rel <= rel_tol, f"{what}: relative Frobenius {rel:.3e} > {rel_tol}"
+    assert frac <= frac_tol, (f"{what}: {int(bad.sum())} elements ({frac:.2e}) beyond 1e-2*RMS + rounding slack "
+                              f"(max |err|/RMS {maxabs / max(rms, 1e-30):.3e})")
+    return rel, maxabs / max(rms, 1e-30)

@@ -12,7 +12,7 @@ from mixture_experts_layer_tokens_gb300 import moe
 from mixture_experts_layer_tokens_gb300.inputs import CONFIGS, make_inputs, scaled
 from mixture_experts_layer_tokens_gb300.layer import MoELayer
 from oracle import moe_ref
-from parity_util import check_bf16, check_fp8, ulp_bf16
+from parity_util import check_bf16, check_fp8, check_nvfp4, ulp_bf16
 
 pytestmark = pytest.mark.gpu
 
@@ -32,15 +32,23 @@ def oracle_tokens(inp, tokens, gpu_ids, gpu_w):
     assert torch.equal(ids, gpu_ids[tokens].cpu())
     w = gpu_w[tokens].cpu()
     a1 = inp.a1[tokens].cpu()
-    a1q, sc = moe_ref.prepare(a1, w, cfg.weight_on_input, cfg.quant)
     n, H = len(tokens), cfg.H
     y = torch.zeros((n * k, H), dtype=torch.float64)
+    if cfg.quant == "nvfp4":
+        # every row quantises on its own: the sampled tokens' rows are exact
+        a1q, sc = moe_ref.prepare_nvfp4(a1, w, cfg.weight_on_input, inp.extra["a1_gscale"])
+        x = inp.extra
+        y = moe_ref.experts_nvfp4(a1q, sc, x["a1_gscale"], inp.w13.cpu(), inp.w13_scale.cpu(),
+                                  x["w13_gscale"].cpu(), inp.w2.cpu(), inp.w2_scale.cpu(), x["w2_gscale"].cpu(),
+                                  x["h_gscale"], moe_ref.align(ids, cfg.E, 128), k, cfg.activation)
+    else:
+        a1q, sc = moe_ref.prepare(a1, w, cfg.weight_on_input, cfg.quant)
     if cfg.quant == "fp8_tensor":
         # one scale over every expert's intermediate: the whole layer at once (all tokens)
         assert n == cfg.T
         y = moe_ref.experts(a1q, sc, inp.w13, inp.w13_scale, inp.w2, inp.w2_scale, moe_ref.align(ids, cfg.E, 128),
                             k, cfg.quant, cfg.activation)
-    for e in ([] if cfg.quant == "fp8_tensor" else sorted(set(ids.reshape(-1).tolist()))):
+    for e in ([] if cfg.quant in ("fp8_tensor", "nvfp4") else sorted(set(ids.reshape(-1).tolist()))):
         slots = [(i, j) for i in range(n) for j in range(k) if int(ids[i, j]) == e]
         rows = np.array([i for i, _ in slots])
         A = moe_ref._act64(a1q, sc, rows, cfg.quant)
@@ -66,6 +74,8 @@ def oracle_tokens(inp, tokens, gpu_ids, gpu_w):
 
 def _check(cfg, out, ref, what):
     ref, slack = ref
+    if cfg.quant == "nvfp4":
+        return check_nvfp4(out, ref, what)
     if cfg.quant != "bf16":
         return check_fp8(out, ref, what)
     return check_bf16(out, ref, what, slack=slack)
@@ -86,6 +96,9 @@ SMALL = {
     "mixtral_small_gelu_tanh": scaled(CONFIGS["mixtral"], T=200, H=512, I=768, activation="gelu_tanh"),
     "deepseek_small_gelu_no_mul": scaled(CONFIGS["deepseek"], T=256, H=512, I=256, E=32, shared_I=256,
                                          activation="gelu_no_mul"),
+    "mixtral_small_nvfp4": scaled(CONFIGS["mixtral"], T=200, H=512, I=768, quant="nvfp4"),
+    # weight on the input before the NVFP4 quantisation, bf16 shared expert beside the NVFP4 experts
+    "llama_small_nvfp4": scaled(CONFIGS["llama8"], T=100, H=512, I=512, shared_I=256, quant="nvfp4"),
 }
 
 
@@ -102,7 +115,8 @@ def test_layer_small_all_tokens(cuda_dev, name):
 
 
 @pytest.mark.parametrize("name,sample", [("mixtral", 12), ("deepseek", 3), ("llama1", 1), ("llama8", 8),
-                                         ("llama64", 6), ("llama512", 6)])
+                                         ("llama64", 6), ("llama512", 6), ("mixtral_nvfp4", 12),
+                                         ("llama1_nvfp4", 1)])
 def test_layer_full_size_sampled_tokens(cuda_dev, name, sample):
     cfg = CONFIGS[name]
     inp = make_inputs(cfg, device=cuda_dev)   # full-size weights drawn on the device
