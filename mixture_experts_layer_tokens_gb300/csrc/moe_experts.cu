@@ -257,8 +257,12 @@ __device__ __forceinline__ void signal_split_partial(int* flag) {
 }
 
 // Activations between the two GEMMs (moe_activation_t): act_gate is the gate's
-// function alone (the *_NO_MUL forms), act_mul the gated form h(g, u).
-__device__ __forceinline__ float act_silu(float g) { return g / (1.0f + __expf(-g)); }
+// function alone (the *_NO_MUL forms), act_mul the gated form h(g, u).  The
+// sigmoids divide with the fast fp32 division intrinsic (a couple of fp32 ulps,
+// far below the bf16 rounding of h; for a denominator past 2^126, i.e. g below
+// about -87, it returns 0, the value h has in bf16 there): the IEEE division took
+// most of an NVFP4 GEMM1 epilogue, which the next unit's MMAs wait for.
+__device__ __forceinline__ float act_silu(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
 __device__ __forceinline__ float act_gelu(float g) { return 0.5f * g * (1.0f + erff(g * 0.70710678118654752f)); }
 __device__ __forceinline__ float act_gelu_tanh(float g) {
   return 0.5f * g * (1.0f + tanhf(0.79788456080286536f * (g + 0.044715f * g * g * g)));
@@ -274,7 +278,7 @@ __device__ __forceinline__ float act_mul(float g, float u) {
   if (kAct == MOE_ACT_SWIGLUOAI) {
     // gpt-oss SwiGLU: gate clamped above at 7, up clamped to [-7, 7], sigmoid(1.702 g)
     const float gc = fminf(g, 7.0f), uc = fminf(fmaxf(u, -7.0f), 7.0f);
-    return (uc + 1.0f) * (gc / (1.0f + __expf(-1.702f * gc)));
+    return (uc + 1.0f) * __fdividef(gc, 1.0f + __expf(-1.702f * gc));
   }
   return act_gate<kAct>(g) * u;
 }
