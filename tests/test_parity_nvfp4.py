@@ -79,6 +79,8 @@ def _run(T, H, I, E, k, ids, dev, act="silu", identity=False, seed=0):
     (4, 2048, 2048, 16, 1, False),    # stream-K in both GEMMs, single-row tiles
     (1, 4096, 1024, 8, 1, False),     # stream-K GEMM1: few units cut into many segments
     (12, 2048, 2048, 8, 2, True),     # stream-K with skewed routing
+    (512, 4096, 2048, 8, 2, False),   # the Mixtral-like shape at a smaller I: ~190 gemm2 units, 1.3 waves
+    (600, 4096, 2048, 8, 2, True),    # the same with skewed routing (a many-tile expert, an empty one)
 ])
 def test_experts_nvfp4(cuda_dev, T, H, I, E, k, skew):
     y, yref = _run(T, H, I, E, k, _ids(T, k, E, T + H, skew), cuda_dev)
