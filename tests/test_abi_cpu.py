@@ -158,3 +158,43 @@ def test_experts_multi_rejects_what_it_cannot_fuse(moelib):
         moe.MOE_ERR_INVALID_ARG
     empty = (P * 2)(prob(256, T=0), prob(512, T=0))
     assert L.moe_experts_multi(empty, 2, 256, ctypes.byref(moe.QC_BF16), 0, FAKE, 1 << 30, None) == moe.MOE_OK
+
+
+def test_nvfp4_entry_points_reject_bad_arguments(moelib):
+    L = moelib
+    G = FAKE  # a global-scale pointer
+
+    def experts(T=16, H=256, I=512, E=8, k=2, act=0, ws=FAKE, wsb=1 << 30, slot=FAKE, a=FAKE, asf=FAKE, out=FAKE):
+        return L.moe_experts_nvfp4(a, asf, G, FAKE, FAKE, G, FAKE, FAKE, G, G, FAKE, slot, FAKE, FAKE, T, H, I, E,
+                                   k, act, out, ws, wsb, None)
+
+    assert experts(H=384) == moe.MOE_ERR_INVALID_ARG            # H % 256
+    assert experts(I=128) == moe.MOE_ERR_INVALID_ARG            # I % 256
+    assert experts(k=9) == moe.MOE_ERR_INVALID_ARG              # top_k > E
+    assert experts(act=6) == moe.MOE_ERR_UNSUPPORTED            # unknown activation
+    assert experts(a=None) == moe.MOE_ERR_INVALID_ARG
+    assert experts(asf=P(264)) == moe.MOE_ERR_INVALID_ARG       # scale rows not 16-byte aligned
+    assert experts(slot=None) == moe.MOE_ERR_INVALID_ARG        # identity needs E == 1 and k == 1
+    assert experts(ws=None) == moe.MOE_ERR_WORKSPACE
+    assert experts(wsb=1000) == moe.MOE_ERR_WORKSPACE
+    assert experts(T=0, a=None, asf=None, out=None) == moe.MOE_OK
+
+    def prepare(T=4, H=256, k=1, weight=0, w=FAKE, g=G, a1=FAKE):
+        return L.moe_prepare_nvfp4(a1, w, T, H, k, weight, g, FAKE, FAKE, None)
+
+    assert prepare(H=24) == moe.MOE_ERR_INVALID_ARG             # H % 16
+    assert prepare(weight=1, k=2) == moe.MOE_ERR_INVALID_ARG    # weight on the input needs top_k == 1
+    assert prepare(weight=1, w=None) == moe.MOE_ERR_INVALID_ARG
+    assert prepare(g=None) == moe.MOE_ERR_INVALID_ARG
+    assert prepare(a1=P(264)) == moe.MOE_ERR_INVALID_ARG        # bf16 rows not 16-byte aligned
+    assert prepare(T=0, a1=None) == moe.MOE_OK
+
+
+def test_nvfp4_workspace_size(moelib):
+    assert moe.workspace_size_nvfp4(512, 384, 14336, 8, 2) == 0        # H % 256
+    assert moe.workspace_size_nvfp4(512, 4096, 14000, 8, 2) == 0       # I % 256
+    S, H, I = 1024, 4096, 14336
+    # gathered codes and scale rows, bf16 h, h codes and scales
+    need = S * H // 2 + S * H // 16 + S * I * 2 + S * I // 2 + S * I // 16
+    assert moe.workspace_size_nvfp4(512, H, I, 8, 2) >= need
+    assert moe.workspace_size_nvfp4(0, H, I, 8, 2) > 0                 # flags and partials only
