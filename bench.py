@@ -505,35 +505,62 @@ def run_gpu(args, ws, rank, local):
         if cfg.finalize_only:
             e2e = None
         else:
+            # Every step copies its inputs from pinned host memory and reads its output
+            # back, as a serving loop does; the loop is pipelined like one: inputs and
+            # outputs are double-buffered and the copies run on their own streams, so step
+            # i's upload and step i-1's download overlap the neighbouring steps' compute.
             h_logits = inp.logits.cpu().pin_memory()
             h_a1 = inp.a1.cpu().pin_memory()
-            h_out = torch.empty((cfg.T, cfg.H), dtype=torch.bfloat16).pin_memory()
-            d_logits = torch.empty_like(inp.logits)
-            d_a1 = torch.empty_like(inp.a1)
-
-            e2e_graph = None
+            h_out = [torch.empty((cfg.T, cfg.H), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+            d_logits = [torch.empty_like(inp.logits) for _ in range(2)]
+            d_a1 = [torch.empty_like(inp.a1) for _ in range(2)]
+            d_out = [torch.empty_like(layer.out) for _ in range(2)]
+            up, down = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+            ev_in = [torch.cuda.Event() for _ in range(2)]    # inputs of buffer b uploaded
+            ev_done = [torch.cuda.Event() for _ in range(2)]  # the step on buffer b computed
+            ev_out = [torch.cuda.Event() for _ in range(2)]   # output of buffer b downloaded
+            layer_out = layer.out
+            e2e_graphs = [None, None]
             if not args.no_graph:
-                e2e_graph = torch.cuda.CUDAGraph()
-                with torch.cuda.graph(e2e_graph, stream=stream):
-                    layer.forward(d_logits, d_a1)
+                for bb in range(2):
+                    layer.out = d_out[bb]
+                    e2e_graphs[bb] = torch.cuda.CUDAGraph()
+                    with torch.cuda.graph(e2e_graphs[bb], stream=stream):
+                        layer.forward(d_logits[bb], d_a1[bb])
+                layer.out = layer_out
 
-            def e2e_step():
-                d_logits.copy_(h_logits, non_blocking=True)
-                d_a1.copy_(h_a1, non_blocking=True)
-                if e2e_graph is not None:
-                    e2e_graph.replay()
+            def e2e_step(i):
+                bb = i % 2
+                up.wait_event(ev_done[bb])                # step i-2 has read this buffer's inputs
+                with torch.cuda.stream(up):
+                    d_logits[bb].copy_(h_logits, non_blocking=True)
+                    d_a1[bb].copy_(h_a1, non_blocking=True)
+                ev_in[bb].record(up)
+                stream.wait_event(ev_in[bb])
+                stream.wait_event(ev_out[bb])             # step i-2's output has been read back
+                if e2e_graphs[bb] is not None:
+                    e2e_graphs[bb].replay()
                 else:
-                    layer.forward(d_logits, d_a1)
-                h_out.copy_(layer.out, non_blocking=True)
-            for _ in range(args.warmup):
-                e2e_step()
+                    layer.out = d_out[bb]
+                    layer.forward(d_logits[bb], d_a1[bb])
+                    layer.out = layer_out
+                ev_done[bb].record(stream)
+                down.wait_event(ev_done[bb])
+                with torch.cuda.stream(down):
+                    h_out[bb].copy_(d_out[bb], non_blocking=True)
+                ev_out[bb].record(down)
+
+            for i in range(args.warmup):
+                e2e_step(i)
             torch.cuda.synchronize(dev)
             barrier(ws)
             t0 = time.perf_counter()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
-            for _ in range(args.steps):
-                e2e_step()
+            up.wait_event(a)
+            for i in range(args.steps):
+                e2e_step(i)
+            stream.wait_event(ev_out[(args.steps - 1) % 2])  # the last output is on the host
             b.record(stream)
             torch.cuda.synchronize(dev)
             wall = (time.perf_counter() - t0) / args.steps
@@ -541,7 +568,7 @@ def run_gpu(args, ws, rank, local):
             ems = max_over_ranks(ems, ws, dev)
             e2e = {"value": ws * cfg.T / (ems * 1e-3), "unit": "tokens/s",
                    "h2d_bytes_per_step": h_logits.numel() * 4 + h_a1.numel() * 2,
-                   "d2h_bytes_per_step": h_out.numel() * 2}
+                   "d2h_bytes_per_step": h_out[0].numel() * 2, "copies": "pipelined (double-buffered, own streams)"}
 
     if rank != 0:
         return
