@@ -106,7 +106,9 @@ def tensor_ratio(quant):
 
 
 # kernel sources of each dominant unit (csrc/ files)
-UNIT_SOURCES = {"experts": ["moe_experts.cu", "moe_common.cuh"], "finalize": ["moe_finalize.cu", "moe_common.cuh"]}
+UNIT_SOURCES = {"experts": ["moe_experts.cu", "moe_common.cuh", "moe_route.cuh"],
+                "fused": ["moe_experts.cu", "moe_common.cuh", "moe_route.cuh"],
+                "finalize": ["moe_finalize.cu", "moe_common.cuh"]}
 
 
 def graph_kernel_nodes(graph):
@@ -390,7 +392,10 @@ def run_gpu(args, ws, rank, local):
                         + ("" if not cfg.shared_I else
                            " + shared expert" + (" in the same launches" if layer.fused_shared else "")))
             layer.forward(inp.logits, inp.a1)  # route/align/prepare state for the experts call
-            counts = torch.diff(layer.al.expert_offsets).cpu().numpy()
+            if layer.single:
+                counts = torch.bincount(layer.topk_ids.reshape(-1).long(), minlength=cfg.E).cpu().numpy()
+            else:
+                counts = torch.diff(layer.al.expert_offsets).cpu().numpy()
             nbytes, flops = experts_algorithmic(cfg, counts)
             if cfg.shared_I:
                 nbytes += 3 * cfg.H * cfg.shared_I * 2 + 2 * cfg.T * cfg.H * 2 + 2 * cfg.T * cfg.shared_I * 2
@@ -399,6 +404,17 @@ def run_gpu(args, ws, rank, local):
 
             def dom_call():
                 layer.experts(a1q_dom, layer.a1q_scale, inp.a1)
+            if layer.single:
+                # one launch is the whole step: the experts' bytes plus the router logits and the
+                # finalize's reads (expert rows, shared row, residual) and its output
+                dom_name = ("moe_layer_fused (route, align, prepare, experts"
+                            + (" + shared expert" if cfg.shared_I else "") + ", finalize: one launch)")
+                S = cfg.T * cfg.top_k
+                nbytes += cfg.T * cfg.E * 4 + S * cfg.H * 2 + cfg.T * cfg.H * 2 * (
+                    1 + (cfg.shared_I > 0) + (inp.residual is not None))
+
+                def dom_call():
+                    layer.forward(inp.logits, inp.a1)
         if args.profile_unit or args.profile_step:
             # one call between profiler start and stop (ncu --profile-from-start off), then exit
             (dom_call if args.profile_unit else step)()

@@ -310,6 +310,30 @@ moe_status_t moe_experts_nvfp4(const void *a1q, const void *a1q_sf, const float 
                                moe_stream_t stream);
 size_t moe_workspace_size_nvfp4(int T, int H, int I, int E, int top_k);
 
+/* ------------------------------------------------------------------ single-launch layer
+ * The whole bf16 layer step in one cooperative kernel launch -- the monolithic form of
+ * the experts ("[vLLM] MoE Oracle & Prepare/Finalize", section "Modular vs
+ * Monolithic": one kernel from the router logits to the layer output) -- for
+ * decode-sized problems.  Its phases, separated by grid-wide barriers, compute what the
+ * separate calls do: moe_route (scoring as there), moe_align (the same order),
+ * prepare (bf16; a1 <- bf16(a1 * bf16(w)) with apply_router_weight_on_input, top_k 1),
+ * the experts with SiLU-and-mul (the shared expert, when given, in the same GEMM units
+ * on the unweighted a1), and moe_finalize's sum (weights skipped with the weight on the
+ * input) + shared row + residual, RMSNorm when rms_weight is given, bf16 output.
+ * logits [T, E] fp32; a1 [T, H] bf16; w13 [E, 2I, H], w2 [E, H, I] bf16; shared_w13
+ * [2I, H] and shared_w2 [H, I] bf16, both or neither; residual [T, H] and rms_weight
+ * [H] bf16 or NULL; topk_ids / topk_weights [T, top_k] are written as by moe_route;
+ * output [T, H] bf16.  Limits: T * top_k <= 2048, E <= 256, H and I multiples of 128,
+ * H <= 12288; beyond them, or on a device without cooperative launch,
+ * MOE_ERR_UNSUPPORTED.  ws: moe_layer_fused_workspace_size(...) bytes, caller-owned;
+ * every wait (the grid barriers included) gives up as described under "status". */
+moe_status_t moe_layer_fused(const float *logits, const void *a1, int T, int H, int I, int E, int top_k,
+                             int scoring, int apply_router_weight_on_input, const void *w13, const void *w2,
+                             const void *shared_w13, const void *shared_w2, const void *residual,
+                             const void *rms_weight, float eps, int32_t *topk_ids, float *topk_weights,
+                             void *output, void *ws, size_t ws_bytes, moe_stream_t stream);
+size_t moe_layer_fused_workspace_size(int T, int H, int I, int E, int top_k, int has_shared);
+
 /* ------------------------------------------------------------------ finalize
  * Finalize: the top-k weight-and-reduce of the "No DP/EP" listing followed by
  * the single-GPU part of the flashinfer finalize fusion (introduction of its

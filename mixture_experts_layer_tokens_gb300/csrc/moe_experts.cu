@@ -60,6 +60,7 @@
 #include <algorithm>
 
 #include "moe_common.cuh"
+#include "moe_route.cuh"
 
 namespace moe {
 namespace {
@@ -292,13 +293,17 @@ __device__ __forceinline__ void fma2(float& a0, float& a1, float v0, float v1, f
       : "f"(v0), "f"(v1), "f"(s));
 }
 
+// The persistent GEMM (see the top of the file), run by every CTA of the grid over the
+// dynamic shared memory `smem_raw`.  `standalone`: the CTA's only work (it gives up its
+// TMEM allocation permit after allocating); otherwise one phase of a longer kernel,
+// which may allocate again and re-initialise the barriers, so they are invalidated at
+// the end.
 template <bool kFP8, int kKind, int kMG, int kAct, bool kHB16, bool kFP4>
-__global__ void __launch_bounds__(Warps<kFP8>::THREADS, 1)
-    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
-                const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmA_1,
-                const __grid_constant__ CUtensorMap tmA2_1, const __grid_constant__ CUtensorMap tmB_1,
-                const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
-                const __grid_constant__ GemmProblems pp) {
+__device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensorMap& tmA2, const CUtensorMap& tmB,
+                                          const CUtensorMap& tmA_1, const CUtensorMap& tmA2_1,
+                                          const CUtensorMap& tmB_1, const CUtensorMap& tmSA,
+                                          const CUtensorMap& tmSB, const GemmProblems& pp, uint8_t* smem_raw,
+                                          bool standalone) {
   using C = Cfg<kFP8, kMG, kFP4>;
   // gemm1 forms: a gated activation reads 128 gate + 128 up rows per unit (one 3-D
   // box); a *_NO_MUL one reads 256 consecutive gate rows, like gemm2
@@ -308,7 +313,6 @@ __global__ void __launch_bounds__(Warps<kFP8>::THREADS, 1)
   constexpr int EPI_THREADS = Warps<kFP8>::EPI_THREADS;
   constexpr int MG = C::MG;
   constexpr int STAGES = C::STAGES;
-  extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* ctrl = smem + STAGES * C::STAGE_BYTES;
   uint64_t* full = reinterpret_cast<uint64_t*>(ctrl);
@@ -365,7 +369,7 @@ __global__ void __launch_bounds__(Warps<kFP8>::THREADS, 1)
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, TMEM_COLS);
-    tmem_relinquish();
+    if (standalone) tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
@@ -997,8 +1001,9 @@ __global__ void __launch_bounds__(Warps<kFP8>::THREADS, 1)
 
   // ------------------------------------------------------------ teardown
   // After a failed wait some MMAs may still be in flight: wait (bounded) for
-  // the MMA pipe to drain before the TMEM is released.
-  if (warp == 1 && status_failed()) {
+  // the MMA pipe to drain before the TMEM is released.  (A phase of a longer kernel
+  // always drains: every commit must have arrived before its barriers are reused.)
+  if (warp == 1 && (status_failed() || !standalone)) {
     if (lane == 0) {
       tc_commit(drain);
       mbar_wait(drain, 0, false, 100000000ull);
@@ -1011,6 +1016,37 @@ __global__ void __launch_bounds__(Warps<kFP8>::THREADS, 1)
     tc_fence_after();
     tmem_dealloc(tmem, TMEM_COLS);
   }
+  if (!standalone && threadIdx.x == 0) {
+    // every barrier of this phase is idle: free them for the next phase's initialisation
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_inval(&full[s]);
+      mbar_inval(&empty[s]);
+      if (kFP4) mbar_inval(&sfready[s]);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_inval(&tfull[a]);
+      mbar_inval(&tempty[a]);
+    }
+    mbar_inval(xbar);
+    mbar_inval(drain);
+    mbar_inval(fixbar);
+    for (int i = 0; i < C::SCALE_SLOTS; ++i) {
+      mbar_inval(&sfull[i]);
+      mbar_inval(&sempty[i]);
+    }
+  }
+}
+
+template <bool kFP8, int kKind, int kMG, int kAct, bool kHB16, bool kFP4>
+__global__ void __launch_bounds__(Warps<kFP8>::THREADS, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
+                const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmA_1,
+                const __grid_constant__ CUtensorMap tmA2_1, const __grid_constant__ CUtensorMap tmB_1,
+                const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
+                const __grid_constant__ GemmProblems pp) {
+  extern __shared__ uint8_t smem_raw[];
+  gemm_body<kFP8, kKind, kMG, kAct, kHB16, kFP4>(tmA, tmA2, tmB, tmA_1, tmA2_1, tmB_1, tmSA, tmSB, pp, smem_raw,
+                                                 true);
 }
 
 // Groups of MG tiles of one expert (expert, first row) and their count, from
@@ -1588,6 +1624,333 @@ moe_experts_problem one_problem(const void* a1q, const float* a1q_scale, const v
   return q;
 }
 
+// ------------------------------------------------------------------ single-launch layer
+// One cooperative launch runs the whole bf16 layer step for decode-sized problems:
+// route -> align -> prepare -> gather -> GEMM1 -> GEMM2 -> finalize, each phase over
+// the whole grid (one CTA per SM), separated by grid-wide barriers.  The GEMM phases
+// are the persistent GEMM of the separate calls (gemm_body), carrying the routed
+// experts and, when the layer has one, the shared expert in the same units.
+constexpr int kFusedMaxSlots = 2048;  // T * top_k handled by the one-CTA align
+constexpr int kFusedMaxE = 256;       // the router keeps E / 32 <= 8 logits per lane
+constexpr int kFusedMaxVec = 8;       // finalize: H / 8 <= 8 vectors per thread
+constexpr int kFusedThreads = Warps<false>::THREADS;
+
+struct FusedParams {
+  const float* logits;
+  const __nv_bfloat16* a1;
+  const __nv_bfloat16* residual;    // [T, H] or null
+  const __nv_bfloat16* rms_weight;  // [H] or null
+  int T, H, I, E, top_k, scoring, weight_on_input, has_shared;
+  float eps;
+  int32_t* topk_ids;
+  float* topk_weights;
+  __nv_bfloat16* out;        // [T, H]
+  unsigned* grid_ctr;        // barrier arrivals (zeroed before the launch)
+  int32_t* offsets;          // routed alignment: [E + 1]
+  int32_t* sorted_slot;      // [S]
+  int32_t* tile_map;         // [cap][2]
+  int32_t* num_tiles;        // [1]
+  int32_t* sh_offsets;       // shared expert: [2]
+  int32_t* sh_tile_map;      // [ceil(T/128)][2]
+  int32_t* sh_num_tiles;     // [1]
+  __nv_bfloat16* a1q;        // weight-on-input rows [T, H] (null: the experts read a1)
+  __nv_bfloat16* A;          // gathered rows [S, H]
+  __nv_bfloat16* y;          // routed expert rows [S, H], token-major
+  __nv_bfloat16* ys;         // shared expert rows [T, H]
+};
+
+// Grid-wide barrier number `n` (1, 2, ...): every CTA arrives once per barrier on a
+// counter zeroed before the launch.  Generic-proxy writes before it are made visible
+// to the async proxy (the TMA loads of the next phase) on both sides.  Bounded: gives
+// up (recording MOE_ERR_TIMEOUT) after the wait limit or when a failure is recorded.
+__device__ bool grid_barrier(unsigned* ctr, unsigned n) {
+  asm volatile("fence.proxy.async;" ::: "memory");
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    atomicAdd(ctr, 1u);
+    const unsigned target = n * gridDim.x;
+    const uint64_t t0 = global_ns();
+    while (true) {
+      unsigned v;
+      asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
+      if (v >= target || status_failed()) break;
+      if (global_ns() - t0 > kWaitLimitNs) {
+        record_timeout();
+        break;
+      }
+      __nanosleep(64);
+    }
+    __threadfence();
+  }
+  __syncthreads();
+  asm volatile("fence.proxy.async;" ::: "memory");
+  return !status_failed();
+}
+
+// The alignment of moe_align for S <= kFusedMaxSlots slots, by one CTA: counts,
+// offsets and tile bases (warp 0 scans), a stable scatter in slot order (warp 0, 32
+// slots per step, ranks among equal experts from __match_any_sync), then the tile map.
+__device__ void fused_align(const int32_t* __restrict__ ids, int S, int E, int32_t* offsets, int32_t* sorted_slot,
+                            int32_t* tile_map, int32_t* num_tiles, int* cnt, int* cur, int* tb) {
+  const int tid = threadIdx.x, lane = tid & 31;
+  for (int e = tid; e < E; e += blockDim.x) cnt[e] = 0;
+  __syncthreads();
+  for (int f = tid; f < S; f += blockDim.x) atomicAdd(&cnt[ids[f]], 1);
+  __syncthreads();
+  if (tid < 32) {
+    const int per = (E + 31) / 32, e0 = lane * per, e1 = min(E, e0 + per);
+    int rows = 0, tiles = 0;
+    for (int e = e0; e < e1; ++e) {
+      rows += cnt[e];
+      tiles += (cnt[e] + BM - 1) / BM;
+    }
+    int xr = rows, xt = tiles;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int yr = __shfl_up_sync(0xffffffffu, xr, off), yt = __shfl_up_sync(0xffffffffu, xt, off);
+      if (lane >= off) {
+        xr += yr;
+        xt += yt;
+      }
+    }
+    int r0 = xr - rows, t0 = xt - tiles;
+    for (int e = e0; e < e1; ++e) {
+      offsets[e] = r0;
+      cur[e] = r0;
+      tb[e] = t0;
+      r0 += cnt[e];
+      t0 += (cnt[e] + BM - 1) / BM;
+    }
+    if (lane == 31) {
+      offsets[E] = xr;
+      *num_tiles = xt;
+    }
+  }
+  __syncthreads();
+  if (tid < 32) {
+    for (int base = 0; base < S; base += 32) {
+      const int f = base + lane;
+      const int e = f < S ? ids[f] : -1;
+      const unsigned peers = __match_any_sync(0xffffffffu, e);
+      const int rank = __popc(peers & ((1u << lane) - 1u));
+      const int pos = f < S ? cur[e] + rank : 0;
+      __syncwarp();
+      if (f < S) {
+        sorted_slot[pos] = f;
+        if (rank == 0) cur[e] += __popc(peers);
+      }
+      __syncwarp();
+    }
+  }
+  __syncthreads();
+  for (int e = tid; e < E; e += blockDim.x) {
+    const int n = (cnt[e] + BM - 1) / BM;
+    for (int i = 0; i < n; ++i) {
+      tile_map[2 * (tb[e] + i)] = e;
+      tile_map[2 * (tb[e] + i) + 1] = offsets[e] + BM * i;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kFusedThreads, 1)
+    fused_layer_kernel(const __grid_constant__ CUtensorMap g1a, const __grid_constant__ CUtensorMap g1b,
+                       const __grid_constant__ CUtensorMap g1a_s, const __grid_constant__ CUtensorMap g1b_s,
+                       const __grid_constant__ CUtensorMap g2a, const __grid_constant__ CUtensorMap g2b,
+                       const __grid_constant__ CUtensorMap g2a_s, const __grid_constant__ CUtensorMap g2b_s,
+                       const __grid_constant__ GemmProblems pp1, const __grid_constant__ GemmProblems pp2,
+                       const __grid_constant__ FusedParams fp) {
+  extern __shared__ uint8_t smem_raw[];
+  const int T = fp.T, H = fp.H, k = fp.top_k, S = T * k;
+  const int lane = threadIdx.x & 31, nwarp = blockDim.x / 32;
+  const int gwarp = blockIdx.x * nwarp + (threadIdx.x >> 5), gwarps = gridDim.x * nwarp;
+  unsigned bar = 0;
+
+  // route (one warp per token); the shared expert's identity tiles
+  for (int t = gwarp; t < T; t += gwarps) route_token<kFusedMaxE / 32>(fp.logits, t, fp.E, k, fp.scoring, fp.topk_ids,
+                                                                         fp.topk_weights);
+  if (fp.has_shared && blockIdx.x == 0) {
+    const int nt = (T + BM - 1) / BM;
+    for (int i = threadIdx.x; i < nt; i += blockDim.x) {
+      fp.sh_tile_map[2 * i] = 0;
+      fp.sh_tile_map[2 * i + 1] = BM * i;
+    }
+    if (threadIdx.x == 0) {
+      fp.sh_offsets[0] = 0;
+      fp.sh_offsets[1] = T;
+      *fp.sh_num_tiles = nt;
+    }
+  }
+  grid_barrier(fp.grid_ctr, ++bar);
+
+  // align (CTA 0) beside the weight on the input (the other CTAs)
+  if (!status_failed()) {
+    if (blockIdx.x == 0) {
+      int* sm = reinterpret_cast<int*>(smem_raw);
+      fused_align(fp.topk_ids, S, fp.E, fp.offsets, fp.sorted_slot, fp.tile_map, fp.num_tiles, sm, sm + kFusedMaxE,
+                  sm + 2 * kFusedMaxE);
+    }
+    if (fp.weight_on_input && (blockIdx.x > 0 || gridDim.x == 1)) {
+      const int c0 = gridDim.x == 1 ? 0 : 1, nc = gridDim.x == 1 ? 1 : gridDim.x - 1;
+      const long long nvec = (long long)T * H / 8;
+      for (long long v = (long long)(blockIdx.x - c0) * blockDim.x + threadIdx.x; v < nvec;
+           v += (long long)nc * blockDim.x) {
+        const int t = (int)(v * 8 / H);
+        const float w = __bfloat162float(__float2bfloat16_rn(__ldg(fp.topk_weights + t)));  // top_k == 1
+        float x[8];
+        load_bf16x8(fp.a1 + v * 8, x);
+        reinterpret_cast<uint4*>(fp.a1q)[v] =
+            make_uint4(pack_bf16x2(x[0] * w, x[1] * w), pack_bf16x2(x[2] * w, x[3] * w), pack_bf16x2(x[4] * w, x[5] * w),
+                       pack_bf16x2(x[6] * w, x[7] * w));
+      }
+    }
+  }
+  grid_barrier(fp.grid_ctr, ++bar);
+
+  // gather: one warp per sorted row
+  if (!status_failed()) {
+    const __nv_bfloat16* src = fp.weight_on_input ? fp.a1q : fp.a1;
+    const int nv = H / 8;
+    for (int p = gwarp; p < S; p += gwarps) {
+      const int t = __ldg(fp.sorted_slot + p) / k;
+      const uint4* s4 = reinterpret_cast<const uint4*>(src + (size_t)t * H);
+      uint4* d4 = reinterpret_cast<uint4*>(fp.A + (size_t)p * H);
+      for (int i = lane; i < nv; i += 32) d4[i] = s4[i];
+    }
+  }
+  grid_barrier(fp.grid_ctr, ++bar);
+
+  // the expert GEMMs (the routed experts and the shared expert in the same units)
+  // (after a failed phase the tile maps may be unset: the GEMMs are skipped)
+  if (!status_failed())
+    gemm_body<false, kGemm1, 1, MOE_ACT_SILU, false, false>(g1a, g1a, g1b, g1a_s, g1a_s, g1b_s, g1a, g1a, pp1,
+                                                            smem_raw, false);
+  grid_barrier(fp.grid_ctr, ++bar);
+  if (!status_failed())
+    gemm_body<false, kGemm2, 1, MOE_ACT_SILU, false, false>(g2a, g2a, g2b, g2a_s, g2a_s, g2b_s, g2a, g2a, pp2,
+                                                            smem_raw, false);
+  grid_barrier(fp.grid_ctr, ++bar);
+
+  // finalize: one CTA per token; sums in fp32 (the weighted expert rows, the shared row,
+  // the residual), then RMSNorm when a weight is given
+  if (status_failed()) return;
+  __shared__ float red[kFusedThreads / 32];
+  const int nv = H / 8;
+  for (int t = blockIdx.x; t < T; t += gridDim.x) {
+    float o[kFusedMaxVec][8];
+    float ss = 0.f;
+#pragma unroll
+    for (int j = 0; j < kFusedMaxVec; ++j) {
+      const int v = threadIdx.x + j * blockDim.x;
+      if (v >= nv) break;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) o[j][i] = 0.f;
+      for (int kk = 0; kk < k; ++kk) {
+        const float w = fp.weight_on_input ? 1.0f : __ldg(fp.topk_weights + (size_t)t * k + kk);
+        float x[8];
+        load_bf16x8(fp.y + ((size_t)t * k + kk) * H + v * 8, x);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) o[j][i] = fmaf(w, x[i], o[j][i]);
+      }
+      if (fp.has_shared) {
+        float x[8];
+        load_bf16x8(fp.ys + (size_t)t * H + v * 8, x);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) o[j][i] += x[i];
+      }
+      if (fp.residual) {
+        float x[8];
+        load_bf16x8(fp.residual + (size_t)t * H + v * 8, x);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) o[j][i] += x[i];
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) ss = fmaf(o[j][i], o[j][i], ss);
+    }
+    float scale = 1.0f;
+    if (fp.rms_weight) {
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+      if (lane == 0) red[threadIdx.x >> 5] = ss;
+      __syncthreads();
+      float tot = 0.f;
+      for (int w = 0; w < nwarp; ++w) tot += red[w];
+      __syncthreads();
+      scale = rsqrtf(tot / (float)H + fp.eps);
+    }
+#pragma unroll
+    for (int j = 0; j < kFusedMaxVec; ++j) {
+      const int v = threadIdx.x + j * blockDim.x;
+      if (v >= nv) break;
+      float g[8];
+      if (fp.rms_weight) {
+        load_bf16x8(fp.rms_weight + v * 8, g);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) o[j][i] *= scale * g[i];
+      }
+      reinterpret_cast<uint4*>(fp.out + (size_t)t * H)[v] =
+          make_uint4(pack_bf16x2(o[j][0], o[j][1]), pack_bf16x2(o[j][2], o[j][3]), pack_bf16x2(o[j][4], o[j][5]),
+                     pack_bf16x2(o[j][6], o[j][7]));
+    }
+  }
+}
+
+// Workspace of the single-launch layer (the counter and the split flags first: one
+// memset clears them).
+struct FusedLayout {
+  size_t ctr, flags1, flags2, ctl_end, offsets, sorted, tiles, ntiles, sh_offsets, sh_tiles, sh_ntiles, a1q, A, h, hs, y,
+      ys, partials, total;
+  int nflags1, nflags2;
+};
+
+FusedLayout fused_layout(int T, int H, int I, int E, int top_k, bool shared, int grid) {
+  FusedLayout L{};
+  const long long S = (long long)T * top_k;
+  const int cap = std::max(1, moe_tile_map_capacity((int)S, E, BM));
+  const int sh_tiles = std::max(1, (T + BM - 1) / BM);
+  L.nflags1 = (cap + (shared ? sh_tiles : 0)) * (I / 128);
+  L.nflags2 = (cap + (shared ? sh_tiles : 0)) * ((H + 255) / 256);
+  size_t off = 0;
+  L.ctr = off;
+  off += 16;
+  L.flags1 = off;
+  off += (size_t)L.nflags1 * 4;
+  L.flags2 = off;
+  off += (size_t)L.nflags2 * 4;
+  L.ctl_end = off;
+  off = al256(off);
+  L.offsets = off;
+  off = al256(off + (size_t)(E + 1) * 4);
+  L.sorted = off;
+  off = al256(off + (size_t)S * 4);
+  L.tiles = off;
+  off = al256(off + (size_t)cap * 8);
+  L.ntiles = off;
+  off = al256(off + 4);
+  L.sh_offsets = off;
+  off = al256(off + 8);
+  L.sh_tiles = off;
+  off = al256(off + (size_t)sh_tiles * 8);
+  L.sh_ntiles = off;
+  off = al256(off + 4);
+  L.a1q = off;
+  off = al256(off + (size_t)T * H * 2);
+  L.A = off;
+  off = al256(off + (size_t)S * H * 2);
+  L.h = off;
+  off = al256(off + (size_t)S * I * 2);
+  L.hs = off;
+  off = al256(off + (shared ? (size_t)T * I * 2 : 0));
+  L.y = off;
+  off = al256(off + (size_t)S * H * 2);
+  L.ys = off;
+  off = al256(off + (shared ? (size_t)T * H * 2 : 0));
+  L.partials = off;
+  off = al256(off + (size_t)grid * BM * BN * 4);
+  L.total = off;
+  return L;
+}
+
 // ------------------------------------------------------------------ NVFP4 experts
 // Workspace of an NVFP4 call: gathered A rows and their scale rows, the bf16
 // intermediate, its NVFP4 codes and scales, the split flags of both GEMMs and one
@@ -1800,4 +2163,144 @@ extern "C" moe_status_t moe_prepare_nvfp4(const void* a1, const float* topk_weig
       static_cast<const __nv_bfloat16*>(a1), H, T, nullptr, apply_router_weight_on_input ? topk_weights : nullptr,
       a1_gscale, static_cast<uint8_t*>(a1q), static_cast<uint8_t*>(a1q_sf));
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+extern "C" size_t moe_layer_fused_workspace_size(int T, int H, int I, int E, int top_k, int has_shared) {
+  if (T < 0 || H <= 0 || I <= 0 || E < 1 || top_k < 1) return 0;
+  return fused_layout(T, H, I, E, top_k, has_shared != 0, gemm_grid()).total;
+}
+
+extern "C" moe_status_t moe_layer_fused(const float* logits, const void* a1, int T, int H, int I, int E, int top_k,
+                                        int scoring, int apply_router_weight_on_input, const void* w13, const void* w2,
+                                        const void* shared_w13, const void* shared_w2, const void* residual,
+                                        const void* rms_weight, float eps, int32_t* topk_ids, float* topk_weights,
+                                        void* output, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  MOE_CHECK_ARG(T >= 0 && E >= 1 && top_k >= 1 && top_k <= E && top_k <= 32 && H > 0 && I > 0);
+  MOE_CHECK_ARG(scoring == MOE_SCORING_SOFTMAX_RENORM || scoring == MOE_SCORING_SIGMOID);
+  MOE_CHECK_ARG(scoring != MOE_SCORING_SIGMOID || top_k == 1);
+  MOE_CHECK_ARG(!apply_router_weight_on_input || top_k == 1);
+  MOE_CHECK_ARG(H % 128 == 0 && I % 128 == 0 && fits_int32((long long)H * 8) && fits_int32((long long)E * 2 * I));
+  MOE_CHECK_ARG((shared_w13 == nullptr) == (shared_w2 == nullptr));
+  if ((long long)T * top_k > kFusedMaxSlots || E > kFusedMaxE || H / 8 > kFusedMaxVec * kFusedThreads)
+    return MOE_ERR_UNSUPPORTED;
+  if (T == 0) return MOE_OK;
+  MOE_CHECK_ARG(logits && a1 && w13 && w2 && topk_ids && topk_weights && output);
+  MOE_CHECK_ARG(aligned16(a1) && aligned16(w13) && aligned16(w2) && aligned16(output) &&
+                (!shared_w13 || (aligned16(shared_w13) && aligned16(shared_w2))) && (!residual || aligned16(residual)) &&
+                (!rms_weight || aligned16(rms_weight)));
+  const bool shared = shared_w13 != nullptr;
+  const int grid = gemm_grid();
+  const FusedLayout L = fused_layout(T, H, I, E, top_k, shared, grid);
+  if (!ws || ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+  MOE_CHECK_ARG(aligned16(ws));
+  int dev = 0, coop = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (!coop) return MOE_ERR_UNSUPPORTED;
+  uint8_t* wsb = static_cast<uint8_t*>(ws);
+  const long long S = (long long)T * top_k;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+  FusedParams fp{};
+  fp.logits = logits;
+  fp.a1 = static_cast<const __nv_bfloat16*>(a1);
+  fp.residual = static_cast<const __nv_bfloat16*>(residual);
+  fp.rms_weight = static_cast<const __nv_bfloat16*>(rms_weight);
+  fp.T = T;
+  fp.H = H;
+  fp.I = I;
+  fp.E = E;
+  fp.top_k = top_k;
+  fp.scoring = scoring;
+  fp.weight_on_input = apply_router_weight_on_input != 0;
+  fp.has_shared = shared;
+  fp.eps = eps;
+  fp.topk_ids = topk_ids;
+  fp.topk_weights = topk_weights;
+  fp.out = static_cast<__nv_bfloat16*>(output);
+  fp.grid_ctr = reinterpret_cast<unsigned*>(wsb + L.ctr);
+  fp.offsets = reinterpret_cast<int32_t*>(wsb + L.offsets);
+  fp.sorted_slot = reinterpret_cast<int32_t*>(wsb + L.sorted);
+  fp.tile_map = reinterpret_cast<int32_t*>(wsb + L.tiles);
+  fp.num_tiles = reinterpret_cast<int32_t*>(wsb + L.ntiles);
+  fp.sh_offsets = reinterpret_cast<int32_t*>(wsb + L.sh_offsets);
+  fp.sh_tile_map = reinterpret_cast<int32_t*>(wsb + L.sh_tiles);
+  fp.sh_num_tiles = reinterpret_cast<int32_t*>(wsb + L.sh_ntiles);
+  fp.a1q = reinterpret_cast<__nv_bfloat16*>(wsb + L.a1q);
+  fp.A = reinterpret_cast<__nv_bfloat16*>(wsb + L.A);
+  fp.y = reinterpret_cast<__nv_bfloat16*>(wsb + L.y);
+  fp.ys = shared ? reinterpret_cast<__nv_bfloat16*>(wsb + L.ys) : nullptr;
+  void* h = wsb + L.h;
+  void* hs = wsb + L.hs;
+
+  // tensor maps: gemm1 reads the gathered rows and w13 (the shared expert: a1 and its
+  // w13), gemm2 the intermediates and w2
+  GemmMaps m1[2] = {}, m2[2] = {};
+  if (!make_map(&m1[0].a, fp.A, false, H, S, 128) || !make_map_gate_up(&m1[0].b, w13, false, H, I, E) ||
+      !make_map(&m2[0].a, h, false, I, S, 128) || !make_map(&m2[0].b, w2, false, I, (long long)E * H, 256))
+    return MOE_ERR_CUDA;
+  if (shared && (!make_map(&m1[1].a, a1, false, H, T, 128) || !make_map_gate_up(&m1[1].b, shared_w13, false, H, I, 1) ||
+                 !make_map(&m2[1].a, hs, false, I, T, 128) || !make_map(&m2[1].b, shared_w2, false, I, H, 256)))
+    return MOE_ERR_CUDA;
+  if (!shared) {
+    m1[1] = m1[0];
+    m2[1] = m2[0];
+  }
+  // the split rule of the separate calls: decode-sized problems with deep K
+  const bool allow_split = S <= 16LL * E && (!shared || T <= 16);
+  const bool split1 = allow_split && H / 64 >= 32, split2 = allow_split && I / 64 >= 32;
+  const int cap = std::max(1, moe_tile_map_capacity((int)S, E, BM));
+  GemmProblems g1 = {}, g2 = {};
+  g1.nprob = g2.nprob = shared ? 2 : 1;
+  for (int i = 0; i < g1.nprob; ++i) {
+    GemmParams& q1 = g1.p[i];
+    q1.offsets = i ? fp.sh_offsets : fp.offsets;
+    q1.group_map = i ? fp.sh_tile_map : fp.tile_map;
+    q1.num_groups = i ? fp.sh_num_tiles : fp.num_tiles;
+    q1.sorted_slot = i ? nullptr : fp.sorted_slot;
+    q1.K = H;
+    q1.NT = I / 128;
+    q1.I = I;
+    q1.H = H;
+    q1.b_rows = 2 * I;
+    q1.out = i ? hs : h;
+    q1.flags = reinterpret_cast<int*>(wsb + L.flags1) + (i ? cap * (I / 128) : 0);
+    q1.partials = reinterpret_cast<float*>(wsb + L.partials);
+    q1.allow_split = split1;
+    GemmParams& q2 = g2.p[i];
+    q2 = q1;
+    q2.K = I;
+    q2.NT = (H + 255) / 256;
+    q2.b_rows = H;
+    q2.out = i ? (void*)fp.ys : (void*)fp.y;
+    q2.flags = reinterpret_cast<int*>(wsb + L.flags2) + (i ? cap * ((H + 255) / 256) : 0);
+    q2.allow_split = split2;
+  }
+  static int configured[64] = {0};
+  void (*kern)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap,
+               CUtensorMap, GemmProblems, GemmProblems, FusedParams) = fused_layer_kernel;
+  const int smem = Cfg<false, 1>::SMEM_BYTES;
+  if (dev < 64 && !configured[dev]) {
+    if (cudaFuncSetAttribute(reinterpret_cast<const void*>(kern), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smem) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    configured[dev] = 1;
+  }
+  // the barrier counter and the split flags start at zero
+  if (cudaMemsetAsync(wsb + L.ctr, 0, L.ctl_end - L.ctr, s) != cudaSuccess) return MOE_ERR_CUDA;
+  // a cooperative launch: every CTA resident at once (the grid barriers need it), or an error
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3(grid);
+  lc.blockDim = dim3(kFusedThreads);
+  lc.dynamicSmemBytes = (size_t)smem;
+  lc.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  lc.attrs = attr;
+  lc.numAttrs = 1;
+  if (cudaLaunchKernelEx(&lc, kern, m1[0].a, m1[0].b, m1[1].a, m1[1].b, m2[0].a, m2[0].b, m2[1].a, m2[1].b, g1, g2,
+                         fp) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
 }

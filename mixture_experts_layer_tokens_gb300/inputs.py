@@ -59,6 +59,7 @@ class LayerConfig:
     rms: bool = False
     nvfp4: bool = False
     activation: str = "silu"       # between the expert GEMMs; *_no_mul: w13 holds I rows
+    single_launch: bool = False    # the whole step as one launch (moe_layer_fused)
     description: str = ""
 
 
@@ -104,6 +105,14 @@ def _cfgs():
         c[f"llama{T}"] = LayerConfig(f"llama{T}", T, 5120, 8192, 16, 1, scoring="sigmoid",
                                      weight_on_input=True, shared_I=8192,
                                      description=f"Llama-4-Scout-like layer T{T} H5120 I8192 E16 top1 sigmoid-on-input + shared I8192")
+    # the same layers as one launch (route, align, prepare, experts, finalize in one kernel)
+    for T in (1, 8, 64):
+        c[f"llama{T}_fused"] = LayerConfig(f"llama{T}_fused", T, 5120, 8192, 16, 1, scoring="sigmoid",
+                                           weight_on_input=True, shared_I=8192, single_launch=True,
+                                           description=f"Llama-4-Scout-like layer T{T} H5120 I8192 E16 top1 "
+                                                       f"sigmoid-on-input + shared I8192, one launch")
+    c["mixtral_fused"] = LayerConfig("mixtral_fused", 512, 4096, 14336, 8, 2, single_launch=True,
+                                     description="Mixtral-8x7B-like layer T512 H4096 I14336 E8 top2 bf16, one launch")
     return c
 
 

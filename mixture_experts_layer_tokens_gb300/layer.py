@@ -5,7 +5,7 @@ Step (all on one stream):
   moe_route -> moe_align -> moe_prepare -> moe_experts [-> shared expert via
   moe_experts with one expert and the identity permutation] -> moe_finalize.
 NVFP4 layers use moe_prepare_nvfp4 and moe_experts_nvfp4 (the shared expert
-stays bf16).
+stays bf16).  Single-launch layers run the whole step as one moe_layer_fused launch.
 
 The shared expert sees the unweighted bf16 input, as the shared-expert row of
 the flashinfer finalize fusion is added unscaled.
@@ -58,6 +58,13 @@ class MoELayer:
             self.al_shared = moe.moe_align(ids0, 1, stream=stream)
             self.ws_shared = torch.empty(max(moe.workspace_size(T, H, cfg.shared_I, 1, 1, "bf16"), 16),
                                          dtype=torch.uint8, device=dev)
+        # the whole step as one launch: a bf16 SiLU layer whose shared expert (if any) has the
+        # routed experts' I
+        self.single = cfg.single_launch
+        if self.single:
+            assert cfg.quant == "bf16" and cfg.activation == "silu" and cfg.shared_I in (0, I)
+            self.ws_fused = torch.empty(max(moe.layer_fused_workspace_size(T, H, I, E, k, cfg.shared_I > 0), 16),
+                                        dtype=torch.uint8, device=dev)
         # a bf16 layer whose shared expert has the routed experts' I and activation runs both
         # in the same GEMM launches (moe_experts_multi)
         self.fused_shared = (cfg.shared_I == I and cfg.quant == "bf16" and cfg.activation == "silu")
@@ -70,6 +77,13 @@ class MoELayer:
 
     def forward(self, logits: torch.Tensor, a1: torch.Tensor, stream=None) -> torch.Tensor:
         cfg, inp = self.cfg, self.inp
+        if self.single:
+            return moe.moe_layer_fused(
+                logits, a1, inp.w13, inp.w2, cfg.top_k, self.scoring, cfg.weight_on_input,
+                shared_w13=inp.shared_w13[0] if cfg.shared_I else None,
+                shared_w2=inp.shared_w2[0] if cfg.shared_I else None, residual=inp.residual,
+                rms_weight=inp.rms_weight, eps=1e-6, topk_ids=self.topk_ids, topk_weights=self.topk_weights,
+                output=self.out, ws=self.ws_fused, stream=stream)
         moe.moe_route(logits, cfg.top_k, self.scoring, self.topk_ids, self.topk_weights, stream=stream)
         moe.moe_align(self.topk_ids, cfg.E, out=self.al, stream=stream)
         if self.passthrough:

@@ -84,6 +84,8 @@ SIGNATURES = {
     "moe_experts_nvfp4": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P,
                            _Z, _P], _I),
     "moe_workspace_size_nvfp4": ([_I, _I, _I, _I, _I], _Z),
+    "moe_layer_fused": ([_P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _F, _P, _P, _P, _P, _Z, _P], _I),
+    "moe_layer_fused_workspace_size": ([_I, _I, _I, _I, _I, _I], _Z),
     "moe_finalize": ([_P, _P, _P, _P, _P, _P, _P, _F, _I, _I, _I, _I, _I, _P, _F, _P, _P], _I),
     "moe_device_status": ([_I], _I),
     "moe_status_string": ([_I], ctypes.c_char_p),
@@ -367,6 +369,43 @@ def moe_experts_nvfp4(a1q: torch.Tensor, a1q_sf: torch.Tensor, a1_gscale, w13: t
         _ptr(al.tile_map), _ptr(al.num_tiles), T, H, I, E, k, ACTIVATIONS[activation], _ptr(out), _ptr(ws),
         ws.numel(), _stream(stream)))
     return out
+
+
+def layer_fused_workspace_size(T: int, H: int, I: int, E: int, top_k: int, has_shared: bool) -> int:
+    return int(lib().moe_layer_fused_workspace_size(T, H, I, E, top_k, int(bool(has_shared))))
+
+
+def moe_layer_fused(logits: torch.Tensor, a1: torch.Tensor, w13: torch.Tensor, w2: torch.Tensor, top_k: int,
+                    scoring: int = MOE_SCORING_SOFTMAX_RENORM, apply_router_weight_on_input: bool = False,
+                    shared_w13: Optional[torch.Tensor] = None, shared_w2: Optional[torch.Tensor] = None,
+                    residual: Optional[torch.Tensor] = None, rms_weight: Optional[torch.Tensor] = None,
+                    eps: float = 1e-6, topk_ids: Optional[torch.Tensor] = None,
+                    topk_weights: Optional[torch.Tensor] = None, output: Optional[torch.Tensor] = None,
+                    ws: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """The whole bf16 layer step in one launch (``moe_layer_fused``): w13 [E, 2I, H],
+    w2 [E, H, I]; shared_w13 [2I, H] / shared_w2 [H, I] (or [1, ...]) for a shared expert."""
+    _need(logits, torch.float32, "logits")
+    for t, n in ((a1, "a1"), (w13, "w13"), (w2, "w2"), (shared_w13, "shared_w13"), (shared_w2, "shared_w2"),
+                 (residual, "residual"), (rms_weight, "rms_weight")):
+        _need(t, torch.bfloat16, n)
+    T, H = a1.shape
+    E, rows13, _ = w13.shape
+    I = rows13 // 2
+    dev = a1.device
+    if topk_ids is None:
+        topk_ids = torch.empty((T, top_k), dtype=torch.int32, device=dev)
+    if topk_weights is None:
+        topk_weights = torch.empty((T, top_k), dtype=torch.float32, device=dev)
+    if output is None:
+        output = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    if ws is None:
+        ws = torch.empty(max(layer_fused_workspace_size(T, H, I, E, top_k, shared_w13 is not None), 16),
+                         dtype=torch.uint8, device=dev)
+    _check("moe_layer_fused", lib().moe_layer_fused(
+        _ptr(logits), _ptr(a1), T, H, I, E, top_k, scoring, int(bool(apply_router_weight_on_input)), _ptr(w13),
+        _ptr(w2), _ptr(shared_w13), _ptr(shared_w2), _ptr(residual), _ptr(rms_weight), eps, _ptr(topk_ids),
+        _ptr(topk_weights), _ptr(output), _ptr(ws), ws.numel(), _stream(stream)))
+    return output
 
 
 def moe_finalize(fused_expert_output: torch.Tensor, topk_weights: Optional[torch.Tensor], top_k: int,

@@ -198,3 +198,23 @@ def test_nvfp4_workspace_size(moelib):
     need = S * H // 2 + S * H // 16 + S * I * 2 + S * I // 2 + S * I // 16
     assert moe.workspace_size_nvfp4(512, H, I, 8, 2) >= need
     assert moe.workspace_size_nvfp4(0, H, I, 8, 2) > 0                 # flags and partials only
+
+
+def test_layer_fused_rejects_what_it_cannot_run(moelib):
+    L = moelib
+
+    def call(T=4, H=256, I=256, E=8, k=2, scoring=0, woi=0, sh13=FAKE, sh2=FAKE, ws=FAKE, wsb=1 << 30, a1=FAKE):
+        return L.moe_layer_fused(FAKE, a1, T, H, I, E, k, scoring, woi, FAKE, FAKE, sh13, sh2, None, None,
+                                 ctypes.c_float(1e-6), FAKE, FAKE, FAKE, ws, wsb, None)
+
+    assert call(T=1025) == moe.MOE_ERR_UNSUPPORTED               # T * top_k > 2048
+    assert call(E=512) == moe.MOE_ERR_UNSUPPORTED                # E > 256
+    assert call(H=200) == moe.MOE_ERR_INVALID_ARG                # H % 128
+    assert call(scoring=1) == moe.MOE_ERR_INVALID_ARG            # sigmoid needs top_k 1
+    assert call(woi=1) == moe.MOE_ERR_INVALID_ARG                # weight on the input needs top_k 1
+    assert call(sh2=None) == moe.MOE_ERR_INVALID_ARG             # shared weights: both or neither
+    assert call(a1=P(264)) == moe.MOE_ERR_INVALID_ARG            # not 16-byte aligned
+    assert call(ws=None) == moe.MOE_ERR_WORKSPACE
+    assert call(T=0, a1=None) == moe.MOE_OK
+    assert moe.layer_fused_workspace_size(4, 256, 256, 8, 2, True) > moe.layer_fused_workspace_size(4, 256, 256, 8, 2,
+                                                                                                   False)

@@ -97,6 +97,12 @@ SMALL = {
     "deepseek_small_gelu_no_mul": scaled(CONFIGS["deepseek"], T=256, H=512, I=256, E=32, shared_I=256,
                                          activation="gelu_no_mul"),
     "mixtral_small_nvfp4": scaled(CONFIGS["mixtral"], T=200, H=512, I=768, quant="nvfp4"),
+    # the whole step as one launch (moe_layer_fused): round-robin and split GEMM schedules,
+    # with and without the shared expert, residual and RMSNorm
+    "llama_small_single": scaled(CONFIGS["llama8_fused"], T=100, H=384, I=512, shared_I=512),
+    "llama_small_single_T1": scaled(CONFIGS["llama1_fused"], H=2048, I=2048, shared_I=2048),
+    "mixtral_small_single": scaled(CONFIGS["mixtral_fused"], T=200, H=512, I=768),
+    "residual_rms_single": scaled(CONFIGS["mixtral_fused"], T=64, H=256, I=256, residual=True, rms=True),
     # weight on the input before the NVFP4 quantisation, bf16 shared expert beside the NVFP4 experts
     "llama_small_nvfp4": scaled(CONFIGS["llama8"], T=100, H=512, I=512, shared_I=256, quant="nvfp4"),
 }
@@ -116,7 +122,8 @@ def test_layer_small_all_tokens(cuda_dev, name):
 
 @pytest.mark.parametrize("name,sample", [("mixtral", 12), ("deepseek", 3), ("llama1", 1), ("llama8", 8),
                                          ("llama64", 6), ("llama512", 6), ("mixtral_nvfp4", 12),
-                                         ("llama1_nvfp4", 1)])
+                                         ("llama1_nvfp4", 1), ("llama1_fused", 1), ("llama64_fused", 6),
+                                         ("mixtral_fused", 12)])
 def test_layer_full_size_sampled_tokens(cuda_dev, name, sample):
     cfg = CONFIGS[name]
     inp = make_inputs(cfg, device=cuda_dev)   # full-size weights drawn on the device
@@ -133,4 +140,21 @@ def test_layer_full_size_sampled_tokens(cuda_dev, name, sample):
     _check(cfg, out[tokens], ref, name)
     # properties that hold at any size: finite everywhere, every routed expert row written
     assert torch.isfinite(out.float()).all()
-    assert int(layer.al.expert_offsets[-1]) == cfg.T * cfg.top_k
+    if not cfg.single_launch:
+        assert int(layer.al.expert_offsets[-1]) == cfg.T * cfg.top_k
+
+
+def test_single_launch_matches_the_separate_calls(cuda_dev):
+    """The one-launch step routes exactly like moe_route and, its GEMMs being the same
+    units in the same order, gives the separate calls' output up to the finalize's fp32
+    summation order."""
+    cfg = scaled(CONFIGS["llama8_fused"], T=40, H=1024, I=1024, shared_I=1024, residual=True, rms=True)
+    inp = make_inputs(cfg, device=cuda_dev)
+    single = MoELayer(inp)
+    sep = MoELayer(make_inputs(scaled(cfg, single_launch=False), device=cuda_dev))
+    o1 = single.forward(inp.logits, inp.a1).clone()
+    o2 = sep.forward(inp.logits, inp.a1)
+    torch.cuda.synchronize()
+    assert moe.moe_device_status() == moe.MOE_OK
+    assert torch.equal(single.topk_ids, sep.topk_ids) and torch.equal(single.topk_weights, sep.topk_weights)
+    check_bf16(o1, o2.double(), "single launch vs separate calls", slack=ulp_bf16(o2.double().cpu().numpy()))
