@@ -103,6 +103,10 @@ SMALL = {
     "llama_small_single_T1": scaled(CONFIGS["llama1_fused"], H=2048, I=2048, shared_I=2048),
     "mixtral_small_single": scaled(CONFIGS["mixtral_fused"], T=200, H=512, I=768),
     "residual_rms_single": scaled(CONFIGS["mixtral_fused"], T=64, H=256, I=256, residual=True, rms=True),
+    # the single launch's limits: E = 256 with top-8 (eight logits per lane, many small experts),
+    # and T * top_k = 2048 slots
+    "single_e256_top8": scaled(CONFIGS["mixtral_fused"], T=64, H=256, I=256, E=256, top_k=8),
+    "single_max_slots": scaled(CONFIGS["mixtral_fused"], T=256, H=256, I=256, E=64, top_k=8),
     # weight on the input before the NVFP4 quantisation, bf16 shared expert beside the NVFP4 experts
     "llama_small_nvfp4": scaled(CONFIGS["llama8"], T=100, H=512, I=512, shared_I=256, quant="nvfp4"),
 }
