@@ -84,7 +84,6 @@ struct Warps {
 // many units as CTAs (decode-sized work); otherwise whole units are dealt
 // round-robin, where a short tail costs less than the split's fixed costs.
 constexpr int SPLIT_BELOW_UNITS_PER_CTA_X2 = 1;
-constexpr int L2_PREFETCH_AHEAD = 8;     // weight tiles prefetched into L2 ahead of the TMA loads
 
 enum Kind { kGemm1 = 0, kGemm2 = 1 };
 
@@ -391,33 +390,6 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
     // ------------------------------------------------------------ TMA producer
     const uint64_t pol_a = policy_evict_last();
     const uint64_t pol_b = policy_evict_first();
-    // L2 prefetch cursor: walks the same (unit, K block) sequence L2_PREFETCH_AHEAD
-    // iterations ahead of the loads (lane 0 only), so more weight bytes are in
-    // flight from HBM than the shared-memory stages hold
-    Sched pfs = sched;
-    int pf_kb = 0, pf_kb1 = 0, pf_prob = 0;
-    Unit pit{};
-    auto prefetch_next = [&](bool issue) {
-      if (pf_kb >= pf_kb1) {
-        int pu;
-        if (!pfs.next(pu, pf_kb, pf_kb1)) return;
-        pf_prob = pu >= units0;
-        pit = decode<MG>(pp.p[pf_prob], pu - (pf_prob ? units0 : 0));
-      }
-      if (issue) {
-        const CUtensorMap* mB = pf_prob ? &tmB_1 : &tmB;
-        if (kPair)
-          tma_prefetch_3d(mB, pf_kb * C::kMapK, pit.n * 128, 2 * pit.e);
-        else
-          tma_prefetch_2d(mB, pf_kb * C::kMapK, pit.e * pp.p[pf_prob].b_rows + pit.n * 256);
-      }
-      ++pf_kb;
-    };
-    // (round-robin schedules already keep every SM streaming whole units; there the
-    // extra requests only cost, so the cursor runs in stream-K mode alone).  The cursor
-    // starts after the iterations the first STAGES fills load, and its first batch is
-    // issued after those loads, so that they are not queued behind it.
-    const bool l2_prefetch = !sched.rr;
     int stage = 0;
     uint32_t phase = 0;
     long long fills = 0;
@@ -477,14 +449,6 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
             tma_load_3d(sB, mB, kx, brow, 2 * it.e, &full[stage], pol_b);
           else
             tma_load_2d(sB, mB, kx, brow, &full[stage], pol_b);
-          if (l2_prefetch) {
-            if (fills + 1 == STAGES) {
-              for (int i = 0; i < STAGES; ++i) prefetch_next(false);
-              for (int i = 0; i < L2_PREFETCH_AHEAD; ++i) prefetch_next(true);
-            } else if (fills + 1 > STAGES) {
-              prefetch_next(true);
-            }
-          }
         }
         __syncwarp();
         ++fills;
