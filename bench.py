@@ -23,6 +23,7 @@ from __future__ import annotations
 import argparse
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -136,14 +137,25 @@ def graph_kernel_nodes(graph):
         return None
 
 
+_CODE_TOKENS = re.compile(r'"(?:\\.|[^"\\])*"|\'(?:\\.|[^\'\\])*\'|//[^\n]*|/\*.*?\*/', re.S)
+
+
+def code_only(src: str) -> str:
+    """C++/CUDA source without its comments and with whitespace runs collapsed: what
+    a comment or formatting edit leaves unchanged."""
+    kept = _CODE_TOKENS.sub(lambda m: m.group(0) if m.group(0)[0] in "\"'" else " ", src)
+    return " ".join(kept.split())
+
+
 def sources_digest(files) -> str:
-    """sha256 over the given csrc/ files (the unit's kernels and their helpers)."""
+    """sha256 over the code of the given csrc/ files (the unit's kernels and their
+    helpers), comments and formatting excluded."""
     import hashlib
     csrc = os.path.join(os.path.dirname(os.path.abspath(__file__)), "mixture_experts_layer_tokens_gb300", "csrc")
     h = hashlib.sha256()
     for f in sorted(files):
-        with open(os.path.join(csrc, f), "rb") as fh:
-            h.update(f.encode() + b"\0" + fh.read())
+        with open(os.path.join(csrc, f), encoding="utf-8") as fh:
+            h.update(f.encode() + b"\0" + code_only(fh.read()).encode())
     return h.hexdigest()
 
 

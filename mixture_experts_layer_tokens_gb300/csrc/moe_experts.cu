@@ -11,46 +11,54 @@
 //   plan   : one block turns the 128-row tile map into the unit groups below and
 //            clears the split-unit flags of both GEMMs
 //   gather : a1q rows -> A rows in expert order (sorted_slot), fp8 scales
-//            transposed to [K/128][rows]; skipped for the bf16 identity case
-//   gemm1  : h = silu(A w13_g^T) * (A w13_u^T), bf16 or fp8 G(128) requantised
+//            transposed to [K/128][rows], NVFP4 scale rows copied beside them;
+//            skipped for the identity case
+//   gemm1  : h = act(A w13_g^T, A w13_u^T), bf16, fp8 G(128) requantised, or bf16
+//            then quantised by a separate pass ("A"/"T" fp8, NVFP4)
 //   gemm2  : y[sorted_slot[p]] = h_p w2^T, bf16 rows scattered token-major
+// moe_layer_fused runs the whole bf16 step (route to finalize) as one cooperative
+// kernel whose GEMM phases are the same GEMM (gemm_body).
 //
 // GEMM design (one persistent CTA per SM):
 //   unit   one weight tile (256 rows of w13 -- 128 gate + 128 up -- or of w2)
 //          times a group of MG 128-row M tiles of one expert.  MG = 2 (bf16
-//          only, when units are few and the iterations are split, see
-//          schedule) loads the weight tile once per K step for up to 256 rows;
-//          MG = 1 otherwise (the fp8 register promotion holds one 128 x 256
-//          tile).  Units run expert by expert, then N tile, then group.
+//          only: when two-tile units of full tiles fill between half a wave and
+//          one wave, as a deep-K gemm2's do) loads the weight tile once per K
+//          step for both tiles; MG = 1 otherwise.  Units run expert by expert,
+//          then N tile, then group.
 //   warp 0 TMA producer: per stage one box of the MG A tiles and one box of
 //          the 256 weight rows (gemm1: a 3-D box of the gate and the up block;
 //          gemm2: 256 consecutive rows), 128-byte swizzle (MG = 2: 3 stages x
-//          64 KB; MG = 1: 4 stages x 48 KB).  Two boxes per stage rather than
-//          one per 128 rows: the copy engine moves about a third more bytes
-//          per SM when its boxes are fewer and larger.
+//          64 KB; MG = 1: 4 stages x 48 KB; NVFP4 adds the stage's 16-byte scale
+//          rows of the A rows and the weight rows, 54 KB).  Two boxes per stage
+//          rather than one per 128 rows: the copy engine moves about a third
+//          more bytes per SM when its boxes are fewer and larger.
 //   warp 1 allocates the 512 TMEM columns and issues tcgen05.mma from one lane
-//          (M=128, N=256 per M tile, fp32 accumulate).
-//   warps 2-9  epilogue: tcgen05.ld of accumulator rows (one TMEM lane per
-//          thread); MG = 2: warp = (lane quarter, M tile); MG = 1: warp = (lane
-//          quarter, column half); bf16 MG = 1 ping-pongs two accumulators so
-//          one unit's epilogue overlaps the next unit's main loop; because the
-//          fp8 block scales change
-//          every 128-deep K block the MMA writes each K block into one of two
-//          partial accumulators that the epilogue scales and adds into fp32
-//          registers (software promotion; the scales are fp32).
+//          (M=128, N=256 per M tile, fp32 accumulate; kind::f16, kind::f8f6f4, or
+//          the block-scaled kind::mxf4nvf4 for NVFP4).
+//   epilogue warps (bf16 and NVFP4: 4, one per TMEM lane quarter; fp8: 8, two
+//          per quarter): tcgen05.ld of accumulator rows (one TMEM lane per
+//          thread).  bf16 MG = 1 ping-pongs two accumulators so one unit's
+//          epilogue overlaps the next unit's main loop.  fp8: the block scales
+//          change every 128-deep K block, so the MMA writes each K block into one
+//          of two partial accumulators that the epilogue scales and adds into
+//          fp32 registers (software promotion; the scales are fp32).  NVFP4: one
+//          accumulator (the other half of the TMEM holds the stages' block
+//          scales, which the epilogue warps copy there from shared memory before
+//          the MMAs of the stage).
 //   problems  one launch may carry two expert problems (moe_experts_multi: a
 //          layer's routed experts and its shared expert): their units are
 //          numbered one after the other and share the schedule below.
-//   schedule  with at least 4 units per CTA, units are dealt round-robin and
-//          units that share a weight tile run side by side on neighbouring
-//          SMs; with fewer (decode, deep-K GEMM2 tails) the (unit, K block)
-//          iterations are split into equal contiguous ranges, one per CTA
-//          ("stream-K").  A unit cut by a range boundary is finished by the CTA
-//          holding its first K blocks: it waits (bounded) for the later
-//          segments' fp32 partials and adds them in segment order, so results
-//          do not depend on timing.  Those later segments are always the first
-//          work of their CTAs and never wait, so the waits cannot form a cycle
-//          while all CTAs are resident.
+//   schedule  decode-sized problems (at most 16 slots per expert, K of 32+
+//          blocks) with fewer units than half the CTAs split the (unit, K block)
+//          iterations into equal contiguous ranges, one per CTA ("stream-K");
+//          otherwise units are dealt round-robin and units that share a weight
+//          tile run side by side on neighbouring SMs.  A unit cut by a range
+//          boundary is finished by the CTA holding its first K blocks: it waits
+//          (bounded) for the later segments' fp32 partials and adds them in
+//          segment order, so results do not depend on timing.  Those later
+//          segments are always the first work of their CTAs and never wait, so
+//          the waits cannot form a cycle while all CTAs are resident.
 //
 // Every wait is bounded: a wait that gives up records MOE_ERR_TIMEOUT and the
 // CTA unwinds, drains its in-flight copies and MMAs, frees its TMEM and

@@ -69,3 +69,13 @@ def test_graph_kernel_count_without_a_graph_is_none():
         def raw_cuda_graph(self):
             raise RuntimeError("no graph")
     assert b.graph_kernel_nodes(NoGraph()) is None
+
+
+def test_traffic_digest_ignores_comments_and_formatting_only():
+    import bench
+    a = 'int f(int x) { return x + 1; }  // one\n/* block\n comment */\nconst char* s = "a // b /* c */";\n'
+    b = 'int f(int x) {\n  return x + 1;\n}\nconst char* s = "a // b /* c */";\n'
+    c = 'int f(int x) { return x + 2; }\nconst char* s = "a // b /* c */";\n'
+    assert bench.code_only(a) == bench.code_only(b)           # comments and layout do not count
+    assert bench.code_only(a) != bench.code_only(c)           # code does
+    assert '"a // b /* c */"' in bench.code_only(a)           # string literals are kept whole
