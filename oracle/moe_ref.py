@@ -27,8 +27,13 @@ finalize, run on one device without dispatch or combine:
   optionally adds the shared-expert row, then (after the all-reduce, absent on
   one GPU) adds the residual, applies RMSNorm and optionally packs NVFP4.
 
+* "Fused MoE Kernel Features", experts table: besides bf16 and fp8 (formats
+  G(128), A, T), nvfp4 is a quantisation type of the experts; the NVFP4 experts
+  below take every operand in the finalize page's NVFP4 encoding.
+
 Where the pages leave a step open (router, alignment, scale formats, finalize
-order) each function below states the plain reading it takes.
+order, the NVFP4 experts' global scales and intermediate) each function below
+states the plain reading it takes.
 
 Parity status: every function here is pinned by ``tests/test_oracle_*.py``
 against invariants, closed forms, brute force or library routines.  The whole
