@@ -79,3 +79,31 @@ def test_traffic_digest_ignores_comments_and_formatting_only():
     assert bench.code_only(a) == bench.code_only(b)           # comments and layout do not count
     assert bench.code_only(a) != bench.code_only(c)           # code does
     assert '"a // b /* c */"' in bench.code_only(a)           # string literals are kept whole
+
+
+def test_nvfp4_inputs_are_seeded_codes_in_their_ranges():
+    from mixture_experts_layer_tokens_gb300.inputs import CONFIGS, NVFP4_A1_GSCALE, NVFP4_H_GSCALE, make_inputs, scaled
+    cfg = scaled(CONFIGS["mixtral_nvfp4"], T=4, H=256, I=256, E=3)
+    a, b = make_inputs(cfg, seed=5), make_inputs(cfg, seed=5)
+    assert torch.equal(a.w13, b.w13) and torch.equal(a.w2_scale, b.w2_scale)      # seeded
+    assert a.w13.shape == (3, 512, 128) and a.w13_scale.shape == (3, 512, 16)
+    assert a.w2.shape == (3, 256, 128) and a.w2_scale.shape == (3, 256, 16)
+    for sf in (a.w13_scale, a.w2_scale):
+        assert int(sf.min()) >= 0x40 and int(sf.max()) < 0x50                    # E4M3 2 .. 7.5
+    assert a.extra["w13_gscale"].shape == (3,) and (a.extra["w13_gscale"] > 0).all()
+    assert a.extra["a1_gscale"] == NVFP4_A1_GSCALE and a.extra["h_gscale"] == NVFP4_H_GSCALE
+
+
+def test_bench_accounting_of_the_formats():
+    import numpy as np
+    import bench
+    from mixture_experts_layer_tokens_gb300.inputs import CONFIGS
+    counts = np.array([1, 0, 2, 1, 0, 0, 1, 1])
+    b16, f16 = bench.experts_algorithmic(CONFIGS["mixtral"], counts)
+    b4, f4 = bench.experts_algorithmic(CONFIGS["mixtral_nvfp4"], counts)
+    touched, H, I = 5, 4096, 14336
+    assert f16 == f4 == 2.0 * 3 * 512 * 2 * H * I                           # the same FLOPs
+    weights = touched * 3 * H * I                                          # of the experts that got rows
+    assert 2.0 < b16 / weights < 2.1                                        # 2 B per bf16 weight + activations
+    assert 0.5625 < b4 / weights < 0.7                                      # 9/16 B per NVFP4 weight + activations
+    assert bench.tensor_ratio("bf16") == 1 and bench.tensor_ratio("fp8") == 2 and bench.tensor_ratio("nvfp4") == 6
