@@ -9,6 +9,11 @@
  *   moe_experts  -> fused_expert_output, unweighted rows      ("experts")
  *   moe_finalize -> output (+ residual_out)                   ("finalize")
  *
+ * with the experts also in other forms: moe_experts_act (other activations),
+ * moe_experts_multi (routed and shared experts in the same launches),
+ * moe_prepare_nvfp4 / moe_experts_nvfp4 (every operand NVFP4); and the whole
+ * bf16 step as one launch for decode-sized problems: moe_layer_fused.
+ *
  * Sources: "[vLLM] MoE Oracle & Prepare/Finalize" blog, section "No DP/EP: the
  * simplest case" (prepare and finalize of MoEPrepareAndFinalizeNoDPEPModular);
  * "Fused MoE Kernel Features" (vLLM design doc), sections "Fused MoE Modular
@@ -22,7 +27,7 @@
  *    allocates every buffer, workspaces included; the library allocates no
  *    device memory.
  *  - Every call is asynchronous on `stream` (a cudaStream_t; NULL is the legacy
- *    default stream) and never synchronises.
+ *    default stream) and never synchronises (moe_device_status excepted).
  *  - Arguments are checked on the host before any launch; a bad argument
  *    returns an error status and launches nothing.  A launch failure returns
  *    MOE_ERR_CUDA.  No call aborts or throws.
