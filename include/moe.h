@@ -169,9 +169,12 @@ int moe_tile_map_capacity(int num_slots, int E, int block_m);
  * a problem needing more (moe_align_workspace_size(T, top_k, E) larger than
  * that) is rejected with MOE_ERR_WORKSPACE before anything is launched.  The
  * call allocates nothing.
- *  - The first call on each device looks up the array's device address
- *    (cudaGetSymbolAddress) with that device current; make that first call
- *    before any stream capture on the device.
+ *  - The first call in each CUDA context looks up the array's device address
+ *    (cudaGetSymbolAddress) with that context current and caches it for the
+ *    context: normally once per device (its primary context), and once more
+ *    after a cudaDeviceReset or in a caller's own context, where the library's
+ *    device code is loaded again at another address.  Make that first call
+ *    before any stream capture in the context.
  *  - All calls share the one array and it keeps the last call's contents (each
  *    call writes every entry it later reads, so nothing needs clearing).  Calls
  *    whose work overlaps on the GPU -- on different streams, or from different

@@ -18,7 +18,7 @@
 //               later warps add the counts of earlier ones without clearing
 //               any table.
 // No result depends on the order in which atomics land.
-#include <atomic>
+#include <mutex>
 
 #include "moe_common.cuh"
 
@@ -303,25 +303,69 @@ extern "C" moe_status_t moe_align(const int32_t* topk_ids, int T, int top_k, int
 // Scratch of moe_align_noalloc: a file-scope device array shared by every call.
 // On the host this name is only a stand-in for the symbol, not a device
 // address: host code passes kernels the address looked up below, once per
-// device.
+// CUDA context (normally once per device).
 static __device__ __align__(256) int32_t g_align_scratch[MOE_ALIGN_NOALLOC_SCRATCH_BYTES / sizeof(int32_t)];
 
 namespace {
-constexpr int kMaxDevices = 64;
-std::atomic<int32_t*> g_scratch_ptr[kMaxDevices];
+// The array's device address belongs to the module as loaded in one CUDA
+// context: a cudaDeviceReset, or a caller's own (non-primary) context, loads
+// the module again at another address.  So the looked-up address is cached per
+// context, keyed on the context's unique id (cuCtxGetId: never reused within
+// the process, unlike the context handle).
+constexpr int kCacheEntries = 64;
+struct ScratchEntry {
+  unsigned long long ctx_id;
+  int32_t* ptr;
+};
+std::mutex g_scratch_mu;
+ScratchEntry g_scratch_cache[kCacheEntries];
+int g_scratch_used = 0;
 
-// Device address of g_align_scratch on the current device, looked up (with
-// that device current) on the first call for the device.
+using PfnCtxGetCurrent = CUresult (*)(CUcontext*);
+using PfnCtxGetId = CUresult (*)(CUcontext, unsigned long long*);
+
+template <class F>
+F driver_fn(const char* name, int version) {
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion(name, &fn, version, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess)
+    return nullptr;
+  return reinterpret_cast<F>(fn);
+}
+
+// Unique id of the current context, or 0 when none is current yet.
+bool current_ctx_id(unsigned long long* id) {
+  static PfnCtxGetCurrent get_current = driver_fn<PfnCtxGetCurrent>("cuCtxGetCurrent", 4000);
+  static PfnCtxGetId get_id = driver_fn<PfnCtxGetId>("cuCtxGetId", 12000);
+  if (!get_current || !get_id) return false;
+  CUcontext ctx = nullptr;
+  if (get_current(&ctx) != CUDA_SUCCESS) return false;
+  *id = 0;
+  return !ctx || get_id(ctx, id) == CUDA_SUCCESS;
+}
+
+// Device address of g_align_scratch in the current context (the current
+// device's primary context unless the caller made another current), looked up
+// with cudaGetSymbolAddress on the first call in that context and cached.
 moe_status_t scratch_on_current_device(int32_t** out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
-  if (dev < 0 || dev >= kMaxDevices) return MOE_ERR_UNSUPPORTED;
-  int32_t* p = g_scratch_ptr[dev].load(std::memory_order_acquire);
-  if (!p) {
-    if (cudaGetSymbolAddress(reinterpret_cast<void**>(&p), g_align_scratch) != cudaSuccess || !p)
-      return MOE_ERR_CUDA;
-    g_scratch_ptr[dev].store(p, std::memory_order_release);
+  unsigned long long id = 0;
+  if (!current_ctx_id(&id)) return MOE_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (id) {
+    for (int i = 0; i < g_scratch_used; ++i)
+      if (g_scratch_cache[i].ctx_id == id) {
+        *out = g_scratch_cache[i].ptr;
+        return MOE_OK;
+      }
   }
+  // (with no context current yet, the lookup itself makes the device's primary
+  // context current; its id is read afterwards)
+  int32_t* p = nullptr;
+  if (cudaGetSymbolAddress(reinterpret_cast<void**>(&p), g_align_scratch) != cudaSuccess || !p) return MOE_ERR_CUDA;
+  if (!id && (!current_ctx_id(&id) || !id)) return MOE_ERR_CUDA;
+  const int slot = g_scratch_used < kCacheEntries ? g_scratch_used++ : (int)(id % kCacheEntries);
+  g_scratch_cache[slot] = {id, p};
   *out = p;
   return MOE_OK;
 }
