@@ -79,15 +79,36 @@ constexpr int BKB = 128;         // bytes of K per stage (one 128-byte swizzle r
 constexpr int A_BYTES = BM * BKB;        // 16 KB per M tile
 constexpr int B_HALF_BYTES = 128 * BKB;  // 16 KB per 128 weight rows
 constexpr int TMEM_COLS = 512;
-// epilogue warps: bf16 4 (one per TMEM lane quarter, all columns of its rows);
-// fp8 8 (two per lane quarter, half of the columns each: the promotion keeps
-// 128 fp32 accumulators per thread)
+// epilogue warps: bf16 4 (warps 2-5, one per TMEM lane quarter, all columns of its
+// rows); fp8 8 (warps 4-11, two per lane quarter, half of the columns each: the
+// promotion keeps 128 fp32 accumulators per thread).  The fp8 block is three full
+// warpgroups -- warps 2 and 3 idle -- so that the registers can be moved between
+// them (setmaxnreg): the producer and MMA warpgroup gives up most of its share and
+// the epilogue warpgroups take it, enough to stage 64 accumulator columns per
+// tensor-memory load beside the 128 promoted sums.
 template <bool kFP8>
 struct Warps {
   static constexpr int EPI = kFP8 ? 8 : 4;
-  static constexpr int THREADS = 64 + EPI * 32;
+  static constexpr int FIRST_EPI = kFP8 ? 4 : 2;
+  static constexpr int THREADS = (FIRST_EPI + EPI) * 32;
   static constexpr int EPI_THREADS = EPI * 32;
 };
+// fp8 register split: launched at kLaunchRegs per thread (the most 384 threads can
+// have), the first warpgroup drops to kLowRegs and the two epilogue warpgroups rise
+// to kHighRegs.  The sum must equal what the block was launched with:
+// 128 * kLowRegs + 256 * kHighRegs == 384 * kLaunchRegs (the host checks the
+// kernel's register count before the first launch).
+constexpr int kLaunchRegs = 168, kLowRegs = 40, kHighRegs = 232;
+static_assert(128 * kLowRegs + 256 * kHighRegs == 384 * kLaunchRegs, "register split must balance");
+
+template <int N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
 // Units are split across CTAs (stream-K) only when there are fewer than half as
 // many units as CTAs (decode-sized work); otherwise whole units are dealt
 // round-robin, where a short tail costs less than the split's fixed costs.
@@ -163,14 +184,23 @@ struct Unit {
   int e, row0, row_end, n;  // rows [row0, row_end) of expert e (at most MG*BM), N tile n
 };
 
-template <int MG>
+// Loads of the schedule's tables (offsets, group map, unit count, sorted slots).
+// kCoh: the tables were written earlier in the same kernel (the single-launch
+// layer), so they are read coherently (ld.global.cg); otherwise an earlier launch
+// wrote them and the read-only path (ld.global.nc) is used.
+template <bool kCoh>
+__device__ __forceinline__ int ld_tab(const int32_t* p) {
+  return kCoh ? __ldcg(p) : __ldg(p);
+}
+
+template <int MG, bool kCoh>
 __device__ __forceinline__ Unit decode(const GemmParams& p, int u) {
   Unit it;
   const int gb = u / p.NT;  // a group of the unit's expert
-  it.e = __ldg(p.group_map + 2 * gb);
-  const int r0 = __ldg(p.group_map + 2 * gb + 1);
-  const int off = __ldg(p.offsets + it.e);
-  const int end = __ldg(p.offsets + it.e + 1);
+  it.e = ld_tab<kCoh>(p.group_map + 2 * gb);
+  const int r0 = ld_tab<kCoh>(p.group_map + 2 * gb + 1);
+  const int off = ld_tab<kCoh>(p.offsets + it.e);
+  const int end = ld_tab<kCoh>(p.offsets + it.e + 1);
   const int gstart = gb - (r0 - off) / (MG * BM);
   const int gcnt = (end - off + MG * BM - 1) / (MG * BM);
   const int local = u - gstart * p.NT;
@@ -233,7 +263,7 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity) {
 // finishes at most one split unit per launch (its last segment), so the
 // barrier's phase is always 0.  Bounded: false after a timeout.
 __device__ __forceinline__ bool wait_split_partials(const int* flag, int target, uint64_t* fixbar) {
-  if ((threadIdx.x >> 5) == 2) {
+  if ((threadIdx.x >> 5) == Warps<false>::FIRST_EPI) {  // (split units are bf16 or NVFP4)
     // the whole first epilogue warp polls in step (one lane loads, a shuffle shares
     // the value): a lone polling lane would be starved by its warp-mates' waits
     const int lane = threadIdx.x & 31;
@@ -291,9 +321,11 @@ __device__ __forceinline__ float act_mul(float g, float u) {
   return act_gate<kAct>(g) * u;
 }
 
-// (a0, a1) += (v0, v1) * s with one packed two-wide fp32 FMA (each lane an IEEE fma)
+// (a0, a1) += (v0, v1) * s with one packed two-wide fp32 FMA (each lane an IEEE fma).
+// volatile: kept in program order between the tensor-memory loads around it, so that
+// one load's 64 staging registers are free before the next load writes them.
 __device__ __forceinline__ void fma2(float& a0, float& a1, float v0, float v1, float s) {
-  asm("{\n\t.reg .b64 a, v, s;\n\t"
+  asm volatile("{\n\t.reg .b64 a, v, s;\n\t"
       "mov.b64 a, {%0, %1};\n\tmov.b64 v, {%2, %3};\n\tmov.b64 s, {%4, %4};\n\t"
       "fma.rn.f32x2 a, v, s, a;\n\tmov.b64 {%0, %1}, a;\n\t}"
       : "+f"(a0), "+f"(a1)
@@ -305,7 +337,7 @@ __device__ __forceinline__ void fma2(float& a0, float& a1, float v0, float v1, f
 // TMEM allocation permit after allocating); otherwise one phase of a longer kernel,
 // which may allocate again and re-initialise the barriers, so they are invalidated at
 // the end.
-template <bool kFP8, int kKind, int kMG, int kAct, bool kHB16, bool kFP4>
+template <bool kFP8, int kKind, int kMG, int kAct, bool kHB16, bool kFP4, bool kCoh = false>
 __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensorMap& tmA2, const CUtensorMap& tmB,
                                           const CUtensorMap& tmA_1, const CUtensorMap& tmA2_1,
                                           const CUtensorMap& tmB_1, const CUtensorMap& tmSA,
@@ -384,8 +416,8 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
   const uint32_t tmem = *tmem_slot;
 
   const GemmParams& p0 = pp.p[0];
-  const int units0 = __ldg(p0.num_groups) * p0.NT;  // problem 1's units follow problem 0's
-  const int units = units0 + (pp.nprob > 1 ? __ldg(pp.p[1].num_groups) * pp.p[1].NT : 0);
+  const int units0 = ld_tab<kCoh>(p0.num_groups) * p0.NT;  // problem 1's units follow problem 0's
+  const int units = units0 + (pp.nprob > 1 ? ld_tab<kCoh>(pp.p[1].num_groups) * pp.p[1].NT : 0);
   const int KB = p0.K / C::kBK;
   Sched sched;
   // fp8 units are never split: its register promotion leaves no room for the split logic
@@ -394,6 +426,10 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
   sched.init(units, KB, gridDim.x, blockIdx.x, kSplit && MG == 1 && p0.allow_split);
   int u, kb0, kb1;
 
+  if (warp < Warps<kFP8>::FIRST_EPI) {
+  // fp8: this warpgroup (producer, MMA issuer, two idle warps) hands registers to the
+  // epilogue warpgroups, which take them at the top of their branch
+  if (kFP8) setmaxnreg_dec<kLowRegs>();
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     const uint64_t pol_a = policy_evict_last();
@@ -408,7 +444,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
       const CUtensorMap* mA = prob ? &tmA_1 : &tmA;
       const CUtensorMap* mA2 = prob ? &tmA2_1 : &tmA2;
       const CUtensorMap* mB = prob ? &tmB_1 : &tmB;
-      const Unit it = decode<MG>(p, u - (prob ? units0 : 0));
+      const Unit it = decode<MG, kCoh>(p, u - (prob ? units0 : 0));
       const int mcnt = (it.row_end - it.row0 + BM - 1) / BM;
       // gemm1: gate block n of expert e and the up block I rows further (3-D map
       // [2E][I][K], z = 2e gate, 2e + 1 up); gemm2: w2 rows [256 n, +256) of expert e
@@ -483,7 +519,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
     bool ok = true;
     while (ok && sched.next(u, kb0, kb1)) {
       const int prob = u >= units0;
-      const Unit it = decode<MG>(pp.p[prob], u - (prob ? units0 : 0));
+      const Unit it = decode<MG, kCoh>(pp.p[prob], u - (prob ? units0 : 0));
       const int mcnt = (it.row_end - it.row0 + BM - 1) / BM;
       if (!kFP8) {
         if (!(ok = warp_wait(&tempty[acc], acc_phase ^ 1))) break;
@@ -536,9 +572,11 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
         if (acc == 0) acc_phase ^= 1;
       }
     }
+  }
   } else {
     // ------------------------------------------------------------ epilogue
-    const int q = warp - 2;
+    if (kFP8) setmaxnreg_inc<kHighRegs>();
+    const int q = warp - Warps<kFP8>::FIRST_EPI;
     const int quarter = warp & 3;        // TMEM lanes this warp may access
     const int sub = q / 4;               // fp8: column half (bf16: always 0)
     const int r = quarter * 32 + lane;   // row within an M tile == TMEM lane
@@ -556,7 +594,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
       const int prob = u >= units0;
       const GemmParams& p = pp.p[prob];
       const int lu = u - (prob ? units0 : 0);  // the unit within its problem (split flags)
-      const Unit it = decode<MG>(p, lu);
+      const Unit it = decode<MG, kCoh>(p, lu);
       const int prow = it.row0 + r;  // row of the first M tile (fp8: the only one)
       const bool valid = prow < it.row_end;
       // split-unit role: 0 whole, 1 first segment (finishes the unit), 2 later segment
@@ -703,7 +741,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
                 const int row = i >> 7, col = 2 * (i & 127);
                 if (col >= ncols) continue;
                 const int mrow = it.row0 + row;
-                const int f = p.sorted_slot ? __ldg(p.sorted_slot + mrow) : mrow;
+                const int f = p.sorted_slot ? ld_tab<kCoh>(p.sorted_slot + mrow) : mrow;
                 const float* x = fix + row * FIX_STRIDE + col;
                 *reinterpret_cast<uint32_t*>(static_cast<__nv_bfloat16*>(p.out) + (size_t)f * p.H + it.n * 256 + col) =
                     pack_bf16x2(x[0], x[1]);
@@ -790,7 +828,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
               }
             }
           } else {
-            const int f = mvalid ? (p.sorted_slot ? __ldg(p.sorted_slot + mrow) : mrow) : 0;
+            const int f = mvalid ? (p.sorted_slot ? ld_tab<kCoh>(p.sorted_slot + mrow) : mrow) : 0;
             __nv_bfloat16* yrow = static_cast<__nv_bfloat16*>(p.out) + (size_t)f * p.H + it.n * 256;
             const int ncols = min(256, p.H - it.n * 256);
 #pragma unroll 1
@@ -848,16 +886,16 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
           tc_fence_after();
           const uint32_t tb = tmem + lane_addr + acc * BN;
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            // gemm1: chunks 0,1 gate, 2,3 up; gemm2: 4 consecutive chunks
-            const int col = kPair ? (c < 2 ? 64 * half + 32 * c : 128 + 64 * half + 32 * (c - 2))
-                                            : 128 * half + 32 * c;
-            float v[32];
-            tmem_ld32(tb + col, v);
+          for (int c = 0; c < 2; ++c) {
+            // two loads of 64 columns: gemm1 the gate block, then the up block; gemm2
+            // two consecutive chunks
+            const int col = kPair ? (c == 0 ? 64 * half : 128 + 64 * half) : 128 * half + 64 * c;
+            float v[64];
+            tmem_ld64(tb + col, v);
             tmem_ld_wait();
-            const float sc = (kPair && c >= 2) ? s1 : s0;
+            const float sc = (kPair && c == 1) ? s1 : s0;
 #pragma unroll
-            for (int i = 0; i < 32; i += 2) fma2(accv[32 * c + i], accv[32 * c + i + 1], v[i], v[i + 1], sc);
+            for (int i = 0; i < 64; i += 2) fma2(accv[64 * c + i], accv[64 * c + i + 1], v[i], v[i + 1], sc);
           }
           tc_fence_before();
           __syncwarp();
@@ -954,7 +992,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
         } else {
           const int c0 = it.n * 256 + 128 * half;
           if (valid && c0 < p.H) {
-            const int f = p.sorted_slot ? __ldg(p.sorted_slot + prow) : prow;
+            const int f = p.sorted_slot ? ld_tab<kCoh>(p.sorted_slot + prow) : prow;
             uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + (size_t)f * p.H + c0);
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
@@ -1290,6 +1328,15 @@ cudaError_t launch_gemm(const GemmMaps* m, const GemmProblems& pp, int grid, cud
     cudaError_t e = cudaFuncSetAttribute(gemm_kernel<kFP8, kKind, kMG, kAct, kHB16, kFP4>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
+    if (kFP8) {
+      // the fp8 kernel moves registers between its warpgroups (setmaxnreg): the split
+      // balances only when the block launches with kLaunchRegs per thread; with fewer
+      // the epilogue's increase could never be granted, so such a build never launches
+      cudaFuncAttributes fa;
+      e = cudaFuncGetAttributes(&fa, gemm_kernel<kFP8, kKind, kMG, kAct, kHB16, kFP4>);
+      if (e != cudaSuccess) return e;
+      if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidConfiguration;
+    }
     configured[dev] = 1;
   }
   const GemmMaps& m1 = pp.nprob > 1 ? m[1] : m[0];
@@ -1768,7 +1815,9 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
       for (long long v = (long long)(blockIdx.x - c0) * blockDim.x + threadIdx.x; v < nvec;
            v += (long long)nc * blockDim.x) {
         const int t = (int)(v * 8 / H);
-        const float w = __bfloat162float(__float2bfloat16_rn(__ldg(fp.topk_weights + t)));  // top_k == 1
+        // (the weights and every table below were written by earlier phases of this
+        // kernel: coherent loads, not the read-only path)
+        const float w = __bfloat162float(__float2bfloat16_rn(__ldcg(fp.topk_weights + t)));  // top_k == 1
         float x[8];
         load_bf16x8(fp.a1 + v * 8, x);
         reinterpret_cast<uint4*>(fp.a1q)[v] =
@@ -1784,10 +1833,10 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     const __nv_bfloat16* src = fp.weight_on_input ? fp.a1q : fp.a1;
     const int nv = H / 8;
     for (int p = gwarp; p < S; p += gwarps) {
-      const int t = __ldg(fp.sorted_slot + p) / k;
+      const int t = __ldcg(fp.sorted_slot + p) / k;
       const uint4* s4 = reinterpret_cast<const uint4*>(src + (size_t)t * H);
       uint4* d4 = reinterpret_cast<uint4*>(fp.A + (size_t)p * H);
-      for (int i = lane; i < nv; i += 32) d4[i] = s4[i];
+      for (int i = lane; i < nv; i += 32) d4[i] = __ldcg(s4 + i);
     }
   }
   grid_barrier(fp.grid_ctr, ++bar);
@@ -1795,12 +1844,12 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
   // the expert GEMMs (the routed experts and the shared expert in the same units)
   // (after a failed phase the tile maps may be unset: the GEMMs are skipped)
   if (!status_failed())
-    gemm_body<false, kGemm1, 1, MOE_ACT_SILU, false, false>(g1a, g1a, g1b, g1a_s, g1a_s, g1b_s, g1a, g1a, pp1,
-                                                            smem_raw, false);
+    gemm_body<false, kGemm1, 1, MOE_ACT_SILU, false, false, true>(g1a, g1a, g1b, g1a_s, g1a_s, g1b_s, g1a, g1a, pp1,
+                                                                  smem_raw, false);
   grid_barrier(fp.grid_ctr, ++bar);
   if (!status_failed())
-    gemm_body<false, kGemm2, 1, MOE_ACT_SILU, false, false>(g2a, g2a, g2b, g2a_s, g2a_s, g2b_s, g2a, g2a, pp2,
-                                                            smem_raw, false);
+    gemm_body<false, kGemm2, 1, MOE_ACT_SILU, false, false, true>(g2a, g2a, g2b, g2a_s, g2a_s, g2b_s, g2a, g2a, pp2,
+                                                                  smem_raw, false);
   grid_barrier(fp.grid_ctr, ++bar);
 
   // finalize: one CTA per token; sums in fp32 (the weighted expert rows, the shared row,
@@ -1818,15 +1867,15 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
 #pragma unroll
       for (int i = 0; i < 8; ++i) o[j][i] = 0.f;
       for (int kk = 0; kk < k; ++kk) {
-        const float w = fp.weight_on_input ? 1.0f : __ldg(fp.topk_weights + (size_t)t * k + kk);
+        const float w = fp.weight_on_input ? 1.0f : __ldcg(fp.topk_weights + (size_t)t * k + kk);
         float x[8];
-        load_bf16x8(fp.y + ((size_t)t * k + kk) * H + v * 8, x);
+        load_bf16x8_cg(fp.y + ((size_t)t * k + kk) * H + v * 8, x);
 #pragma unroll
         for (int i = 0; i < 8; ++i) o[j][i] = fmaf(w, x[i], o[j][i]);
       }
       if (fp.has_shared) {
         float x[8];
-        load_bf16x8(fp.ys + (size_t)t * H + v * 8, x);
+        load_bf16x8_cg(fp.ys + (size_t)t * H + v * 8, x);
 #pragma unroll
         for (int i = 0; i < 8; ++i) o[j][i] += x[i];
       }
@@ -2068,6 +2117,31 @@ extern "C" size_t moe_workspace_size(int T, int H, int I, int E, int top_k, cons
   const moe_experts_problem q = one_problem(nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
                                             nullptr, nullptr, T, I, E, top_k, nullptr);
   return ws_layout(&q, 1, H, qc->act == MOE_DT_FP8_E4M3, gemm_grid(), qc->act_group).total;
+}
+
+extern "C" moe_status_t moe_workspace_intermediate(int T, int H, int I, int E, int top_k, const moe_quant_config* qc,
+                                                   size_t* h_offset, size_t* h_scale_offset, int* scale_stride) {
+  MOE_CHECK_ARG(qc && h_offset && h_scale_offset && scale_stride && T >= 0 && H > 0 && I > 0 && E >= 1 && top_k >= 1);
+  if (!quant_ok(qc)) return MOE_ERR_UNSUPPORTED;
+  const moe_experts_problem q = one_problem(nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
+                                            nullptr, nullptr, T, I, E, top_k, nullptr);
+  const bool fp8 = qc->act == MOE_DT_FP8_E4M3;
+  const WsLayout L = ws_layout(&q, 1, H, fp8, gemm_grid(), qc->act_group);
+  *h_offset = L.p[0].h;
+  *h_scale_offset = fp8 ? L.p[0].hs : 0;
+  *scale_stride = !fp8 ? 0 : (qc->act_group == 128 ? L.p[0].s_pad : 1);
+  return MOE_OK;
+}
+
+extern "C" moe_status_t moe_workspace_intermediate_nvfp4(int T, int H, int I, int E, int top_k, size_t* hb_offset,
+                                                         size_t* hq_offset, size_t* hsf_offset) {
+  MOE_CHECK_ARG(hb_offset && hq_offset && hsf_offset && T >= 0 && H > 0 && H % 256 == 0 && I > 0 && I % 256 == 0 &&
+                E >= 1 && top_k >= 1);
+  const Fp4Layout L = ws_layout_nvfp4((long long)T * top_k, H, I, E, gemm_grid());
+  *hb_offset = L.hb;
+  *hq_offset = L.hq;
+  *hsf_offset = L.hsf;
+  return MOE_OK;
 }
 
 extern "C" size_t moe_workspace_size_multi(const moe_experts_problem* problems, int num_problems, int H,
