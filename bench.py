@@ -4,9 +4,13 @@
 A step is the whole hot path on one batch of synthetic input already resident
 in HBM: moe_route -> moe_align -> moe_prepare -> moe_experts (+ the shared
 expert when the layer has one) -> moe_finalize, all through the C ABI on one
-stream.  Default workload: the Mixtral-8x7B-like layer (T=512, H=4096,
-I=14336, E=8, top-2, bf16), whose 2.8 GB of expert weights stream from HBM
-every step (far more than the 129 MB L2, so no flush is needed).
+stream.  Default workload: the DeepSeek-V3-like layer (T=4096, H=7168, I=2048,
+E=256, top-8, fp8 G(128) experts + a bf16 shared expert), the largest
+configuration that fits one GPU, whose 11.4 GB of expert weights stream from
+HBM every step (far more than the 129 MB L2, so no flush is needed).  Workloads
+whose step touches less than the L2 (the tiny layer, the finalize kernel alone)
+rotate through copies of their inputs that together exceed 4x the L2, so no
+step reads what an earlier step left in the L2.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
 
@@ -22,6 +26,7 @@ from __future__ import annotations
 
 import argparse
 import json
+import math
 import os
 import re
 import statistics
@@ -46,7 +51,7 @@ def parse():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--workload", default="mixtral", choices=sorted(CONFIGS))
+    ap.add_argument("--workload", default="deepseek", choices=sorted(CONFIGS))
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile-unit", action="store_true",
@@ -322,16 +327,99 @@ def max_over_ranks(x, ws, device):
     return float(t.item())
 
 
-L2_BYTES = 129e6  # GB300 L2
+L2_BYTES = 129e6  # GB300 L2 (the device attribute is used when a GPU is present)
 
 
-def l2_note(cfg, unit_bytes):
-    """How the timed steps stand to the L2 (no flush between steps in either case)."""
-    if not cfg.finalize_only and unit_bytes > L2_BYTES:
-        return (f"no flush: each step streams {unit_bytes / 1e9:.2f} GB through the experts "
-                f"(more than the 129 MB L2)")
-    return (f"no flush: the step's {unit_bytes / 1e6:.0f} MB fit in the 129 MB L2, so back-to-back steps "
-            f"can reuse it (a small-workload line)")
+def l2_bytes():
+    try:
+        if torch.cuda.is_available():
+            return float(torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size)
+    except Exception:
+        pass
+    return L2_BYTES
+
+
+def step_bytes_estimate(cfg):
+    """Bytes one step touches, from the configuration alone (every expert counted as
+    touched): what decides whether the timed steps need rotating input sets."""
+    if cfg.finalize_only:
+        return finalize_algorithmic(cfg, True) + cfg.T * cfg.H * 2
+    mats = 2 if cfg.activation.endswith("_no_mul") else 3
+    esz = {"bf16": 2.0, "nvfp4": 9 / 16}.get(cfg.quant, 1.0)
+    w = cfg.E * mats * cfg.H * cfg.I * esz + 3 * cfg.H * cfg.shared_I * 2
+    return w + cfg.T * cfg.H * 2 * 3 + cfg.T * cfg.top_k * cfg.H * 2
+
+
+def rotation_sets(cfg):
+    """1 when a step touches more than the L2; otherwise the number of input sets,
+    each a copy of the step's inputs, weights and outputs, that together exceed 4x the
+    L2 (the timed steps cycle through them)."""
+    est = step_bytes_estimate(cfg)
+    l2 = l2_bytes()
+    return 1 if est > l2 else int(math.ceil(4.0 * l2 / est)) + 1
+
+
+def l2_note(cfg, nsets):
+    est = step_bytes_estimate(cfg)
+    if nsets == 1:
+        return f"no flush: each step touches ~{est / 1e9:.2f} GB (more than the {l2_bytes() / 1e6:.0f} MB L2)"
+    return (f"rotating inputs: {nsets} copies of the step's inputs, weights and outputs (~{est / 1e6:.0f} MB "
+            f"each, {nsets * est / 1e6:.0f} MB in all, > 4x the {l2_bytes() / 1e6:.0f} MB L2), one per step in turn")
+
+
+def clone_inputs(inp):
+    """A copy of every tensor of a workload's inputs (same values, other memory)."""
+    from mixture_experts_layer_tokens_gb300.inputs import LayerInputs
+    cl = lambda v: v.clone() if isinstance(v, torch.Tensor) else v
+    d = {k: cl(v) for k, v in inp.__dict__.items() if k != "extra"}
+    d["extra"] = {k: cl(v) for k, v in inp.extra.items()}
+    return LayerInputs(**d)
+
+
+def measure_fp8_peak(dev):
+    """Dense fp8 (E4M3 x E4M3, fp32 accumulate, bf16 out) throughput of cuBLASLt through
+    torch._scaled_mm at 8192^3 on this GPU, timed with CUDA events: best of 10 (burst)
+    and back to back for about 2 s (sustained).  None when the call is unavailable."""
+    try:
+        N = 8192
+        a = torch.randn(N, N, device=dev).to(torch.float8_e4m3fn)
+        b = torch.randn(N, N, device=dev).to(torch.float8_e4m3fn).t()
+        one = torch.ones((), device=dev)
+        mm = lambda: torch._scaled_mm(a, b, scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
+        for _ in range(5):
+            mm()
+        torch.cuda.synchronize(dev)
+        best = float("inf")
+        for _ in range(10):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            mm()
+            e1.record()
+            torch.cuda.synchronize(dev)
+            best = min(best, e0.elapsed_time(e1))
+        n, t0 = 0, time.time()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        while time.time() - t0 < 2.0:
+            for _ in range(20):
+                mm()
+            n += 20
+            torch.cuda.synchronize(dev)
+        e1.record()
+        torch.cuda.synchronize(dev)
+        flop = 2.0 * N ** 3
+        del a, b
+        return {"burst_tflops": round(flop / (best * 1e-3) / 1e12, 1),
+                "sustained_tflops": round(flop * n / (e0.elapsed_time(e1) * 1e-3) / 1e12, 1),
+                "how": "torch._scaled_mm e4m3 x e4m3 -> bf16, 8192^3, CUDA events: best of 10; back to back ~2 s"}
+    except Exception:
+        return None
+
+
+def common_config(cfg, ws, nsets):
+    """The `config` object of both arms' lines (the workload, not how it ran)."""
+    return {"workload": cfg.description, "T": cfg.T, "H": cfg.H, "I": cfg.I, "E": cfg.E, "top_k": cfg.top_k,
+            "parallelism": f"replicas{ws}", "l2": l2_note(cfg, nsets)}
 
 
 # ------------------------------------------------------------------ reference arm
@@ -353,8 +441,7 @@ def run_reference(args, ws, rank):
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / len(times),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": cfg.description, "T": cfg.T, "H": cfg.H, "I": cfg.I, "E": cfg.E,
-                       "top_k": cfg.top_k},
+            "config": common_config(cfg, args.gpus, rotation_sets(cfg)),
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                              "sample": f"{per_step} token of the {cfg.name} workload per step (fp64 oracle), "
                                        f"CPU {cpu_model()}"},
@@ -375,47 +462,58 @@ def run_gpu(args, ws, rank, local):
     dev = torch.device("cuda", local)
     cfg = CONFIGS[args.workload]
     inp = make_inputs(cfg, seed=rank, device=dev)
+    # small working sets: copies of the inputs, one per step in turn (see rotation_sets)
+    nsets = rotation_sets(cfg)
+    sets = [inp] + [clone_inputs(inp) for _ in range(nsets - 1)]
     stream = torch.cuda.Stream(device=dev)
     hbm_peak, bf16_peak, peak_kind = peaks()
 
     with torch.cuda.stream(stream):
         if cfg.finalize_only:
-            step_obj = FinalizeStep(inp)
-            step_obj.weights()
+            step_objs = [FinalizeStep(x) for x in sets]
+            for so in step_objs:
+                so.weights()
 
-            def step():
-                step_obj.weights()
-                step_obj.finalize(True)
+            def make_step(so):
+                def step():
+                    so.weights()
+                    so.finalize(True)
+                return step
+            steps = [make_step(so) for so in step_objs]
             launches_per_step = 2  # estimate; replaced by the captured graph's kernel count
         else:
-            layer = MoELayer(inp, stream=stream)
+            layers = [MoELayer(x, stream=stream) for x in sets]
+            layer = layers[0]
 
-            def step():
-                layer.forward(inp.logits, inp.a1)
+            def make_step(ly, x):
+                def step():
+                    ly.forward(x.logits, x.a1)
+                return step
+            steps = [make_step(ly, x) for ly, x in zip(layers, sets)]
             # estimate (route, align, prepare, plan + gather + 2 GEMMs, finalize); replaced by
             # the captured graph's kernel count when the graph can be read
             launches_per_step = 1 + 1 + (0 if layer.passthrough else 1) + 4 + 1
-        for _ in range(args.warmup):
-            step()
+        for i in range(max(args.warmup, nsets)):
+            steps[i % nsets]()
         torch.cuda.synchronize(dev)
         assert moe.moe_device_status() == moe.MOE_OK
 
-        # the dominant unit: the kernel group the roofline reports
+        # the dominant unit: the kernel group the roofline reports (one call per input set)
         if cfg.finalize_only:
             dom_name = "moe_finalize (NVFP4 out)"
             nbytes = finalize_algorithmic(cfg, True)
             flops = 0.0
-            step_obj.weights()
-
-            def dom_call():
-                step_obj.finalize(True)
+            for so in step_objs:
+                so.weights()
+            dom_calls = [(lambda so=so: so.finalize(True)) for so in step_objs]
         else:
             # the routed experts and, when the layer has one, the shared expert (one
             # moe_experts_multi call when they share launches, else two calls)
             dom_name = (f"moe_experts (plan + gather + GEMM1 {cfg.activation} + GEMM2 scatter)"
                         + ("" if not cfg.shared_I else
                            " + shared expert" + (" in the same launches" if layer.fused_shared else "")))
-            layer.forward(inp.logits, inp.a1)  # route/align/prepare state for the experts call
+            for st in steps:
+                st()  # route/align/prepare state for the experts calls
             if layer.single:
                 counts = torch.bincount(layer.topk_ids.reshape(-1).long(), minlength=cfg.E).cpu().numpy()
             else:
@@ -424,10 +522,13 @@ def run_gpu(args, ws, rank, local):
             if cfg.shared_I:
                 nbytes += 3 * cfg.H * cfg.shared_I * 2 + 2 * cfg.T * cfg.H * 2 + 2 * cfg.T * cfg.shared_I * 2
                 flops += 6.0 * cfg.T * cfg.H * cfg.shared_I
-            a1q_dom = inp.a1 if layer.passthrough else layer.a1q
 
-            def dom_call():
-                layer.experts(a1q_dom, layer.a1q_scale, inp.a1)
+            def make_dom(ly, x):
+                a1q = x.a1 if ly.passthrough else ly.a1q
+                if ly.single:
+                    return lambda: ly.forward(x.logits, x.a1)
+                return lambda: ly.experts(a1q, ly.a1q_scale, x.a1)
+            dom_calls = [make_dom(ly, x) for ly, x in zip(layers, sets)]
             if layer.single:
                 # one launch is the whole step: the experts' bytes plus the router logits and the
                 # finalize's reads (expert rows, shared row, residual) and its output
@@ -436,15 +537,12 @@ def run_gpu(args, ws, rank, local):
                 S = cfg.T * cfg.top_k
                 nbytes += cfg.T * cfg.E * 4 + S * cfg.H * 2 + cfg.T * cfg.H * 2 * (
                     1 + (cfg.shared_I > 0) + (inp.residual is not None))
-
-                def dom_call():
-                    layer.forward(inp.logits, inp.a1)
         if args.profile_unit or args.profile_step:
             # one call between profiler start and stop (ncu --profile-from-start off), then exit
-            (dom_call if args.profile_unit else step)()
+            (dom_calls[0] if args.profile_unit else steps[0])()
             torch.cuda.synchronize(dev)
             torch.cuda.profiler.start()
-            (dom_call if args.profile_unit else step)()
+            (dom_calls[0] if args.profile_unit else steps[0])()
             torch.cuda.synchronize(dev)
             torch.cuda.profiler.stop()
             assert moe.moe_device_status() == moe.MOE_OK
@@ -452,36 +550,41 @@ def run_gpu(args, ws, rank, local):
                 print(json.dumps({"profiled": "unit" if args.profile_unit else "step", "workload": cfg.name,
                                   "kernel": dom_name}), flush=True)
             return
-        graph = None
+        graphs = None
         launches_counted = False
         if not args.no_graph:
-            # the step's library calls captured once and replayed: same kernels, no per-call host work
-            try:
-                graph = torch.cuda.CUDAGraph(keep_graph=True)
-            except TypeError:
-                graph = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(graph, stream=stream):
-                step()
-            counted = graph_kernel_nodes(graph)
+            # each set's step captured once and replayed: same kernels, no per-call host work
+            graphs = []
+            for st in steps:
+                try:
+                    g = torch.cuda.CUDAGraph(keep_graph=True)
+                except TypeError:
+                    g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    st()
+                graphs.append(g)
+            counted = graph_kernel_nodes(graphs[0])
             if counted:
                 launches_per_step = counted
                 launches_counted = True
-            if hasattr(graph, "instantiate"):
-                graph.instantiate()
+            for g in graphs:
+                if hasattr(g, "instantiate"):
+                    g.instantiate()
             for _ in range(3):
-                graph.replay()
+                for g in graphs:
+                    g.replay()
             torch.cuda.synchronize(dev)
             assert moe.moe_device_status() == moe.MOE_OK
-        run_step = graph.replay if graph is not None else step
+        run_steps = [g.replay for g in graphs] if graphs is not None else steps
 
-        # ---- timed region: K steps, events on the launching stream
+        # ---- timed region: K steps (input set i % nsets at step i), events on the launching stream
         clocks = ClockSampler(local) if rank == 0 else None
         barrier(ws)
         torch.cuda.synchronize(dev)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        for _ in range(args.steps):
-            run_step()
+        for i in range(args.steps):
+            run_steps[i % nsets]()
         e1.record(stream)
         torch.cuda.synchronize(dev)
         barrier(ws)
@@ -490,24 +593,24 @@ def run_gpu(args, ws, rank, local):
         ms_max = max_over_ranks(ms, ws, dev)
         value = ws * cfg.T / (ms_max * 1e-3)
 
-        # ---- dominant unit: R back-to-back calls captured in one graph, replayed;
-        # CUDA events on the launching stream give the device time per call
-        R = 10
-        for _ in range(3):
-            dom_call()
+        # ---- dominant unit: R back-to-back calls (cycling through the input sets) captured in
+        # one graph, replayed; CUDA events on the launching stream give the device time per call
+        R = nsets * max(1, math.ceil(10 / nsets))
+        for c in dom_calls:
+            c()
         torch.cuda.synchronize(dev)
         reps = max(1, args.steps // R)
         if args.no_graph:
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
-            for _ in range(reps * R):
-                dom_call()
+            for i in range(reps * R):
+                dom_calls[i % nsets]()
             b.record(stream)
         else:
             dom_graph = torch.cuda.CUDAGraph()
             with torch.cuda.graph(dom_graph, stream=stream):
-                for _ in range(R):
-                    dom_call()
+                for i in range(R):
+                    dom_calls[i % nsets]()
             dom_graph.replay()
             torch.cuda.synchronize(dev)
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -517,9 +620,17 @@ def run_gpu(args, ws, rank, local):
             b.record(stream)
         torch.cuda.synchronize(dev)
         dom_ms = a.elapsed_time(b) / (reps * R)
-        # the binding roof: HBM bytes or tensor FLOPs (fp8 / NVFP4 peak = measured bf16 x the
-        # nominal 2x / 6x)
-        tensor_peak = bf16_peak * tensor_ratio(cfg.quant)
+        # the binding roof: HBM bytes or tensor FLOPs.  fp8: the measured fp8 peak of this GPU
+        # (torch._scaled_mm) when it can be taken, else the measured bf16 peak x the nominal 2x;
+        # NVFP4: measured bf16 x the nominal 6x
+        fp8_peak = measure_fp8_peak(dev) if cfg.quant.startswith("fp8") else None
+        if fp8_peak:
+            tensor_peak = fp8_peak["burst_tflops"]
+            tensor_kind = "measured fp8 (this run, burst: " + fp8_peak["how"] + ")"
+        else:
+            tensor_peak = bf16_peak * tensor_ratio(cfg.quant)
+            tensor_kind = peak_kind + ("" if cfg.quant == "bf16" else
+                                       f" bf16 x{tensor_ratio(cfg.quant):g} (nominal {cfg.quant}:bf16)")
         t_hbm = nbytes / (hbm_peak * 1e9)
         t_tensor = flops / (tensor_peak * 1e12) if flops else 0.0
         if t_tensor > t_hbm:
@@ -528,8 +639,7 @@ def run_gpu(args, ws, rank, local):
                         "unit": "TFLOP/s", "frac": round(achieved / tensor_peak, 4),
                         "traffic": measured_traffic(cfg.name),
                         "kernel": dom_name, "algorithmic_flops": flops, "ms": round(dom_ms, 4),
-                        "peak_kind": peak_kind + ("" if cfg.quant == "bf16" else
-                                                  f" bf16 x{tensor_ratio(cfg.quant):g} (nominal {cfg.quant}:bf16)")}
+                        "peak_kind": tensor_kind}
             roofline["hbm_gbs"] = round(nbytes / (dom_ms * 1e-3) / 1e9, 1)
         else:
             achieved = nbytes / (dom_ms * 1e-3) / 1e9
@@ -540,6 +650,10 @@ def run_gpu(args, ws, rank, local):
             if flops:
                 roofline["tflops"] = round(flops / (dom_ms * 1e-3) / 1e12, 1)
                 roofline["tensor_frac"] = round(flops / (dom_ms * 1e-3) / 1e12 / tensor_peak, 4)
+                roofline["tensor_peak_kind"] = tensor_kind
+        if fp8_peak:
+            roofline["fp8_peak_sustained"] = fp8_peak["sustained_tflops"]
+            roofline["fp8_peak_nominal_ratio"] = round(bf16_peak * tensor_ratio(cfg.quant), 1)
 
         # ---- end to end through the public API with host buffers
         if cfg.finalize_only:
@@ -627,12 +741,10 @@ def run_gpu(args, ws, rank, local):
             "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": {"bf16": "bf16", "nvfp4": "nvfp4"}.get(cfg.quant, "fp8"),
             "data": "synthetic",
-            "config": {"workload": cfg.description, "T": cfg.T, "H": cfg.H, "I": cfg.I, "E": cfg.E,
-                       "top_k": cfg.top_k, "parallelism": f"replicas{ws}",
-                       "launch": "cuda_graph" if not args.no_graph else "eager",
+            "config": common_config(cfg, ws, nsets),
+            "launch": {"mode": "cuda_graph" if not args.no_graph else "eager",
                        "gpu_launches_per_step": launches_per_step,
-                       "gpu_launches_from": "captured graph's kernel nodes" if launches_counted else "estimate",
-                       "l2": l2_note(cfg, nbytes)},
+                       "gpu_launches_from": "captured graph's kernel nodes" if launches_counted else "estimate"},
             "roofline": roofline, "cpu_baseline": cpu, "clocks": clk, "e2e": e2e,
             "gpu_launches": launches_per_step * args.steps}
     print(json.dumps(line), flush=True)

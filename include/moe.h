@@ -243,6 +243,21 @@ moe_status_t moe_experts_act(const void *a1q, const float *a1q_scale, const void
                              moe_stream_t stream);
 size_t moe_workspace_size(int T, int H, int I, int E, int top_k, const moe_quant_config *qc);
 
+/* Where moe_experts / moe_experts_act leave the intermediate h in their workspace
+ * (it stays there until the workspace is used again), for inspection of the stage
+ * between the two GEMMs.  Rows are the S = T * top_k sorted rows p (expert order):
+ *   *h_offset       byte offset in ws of h [S, I]: bf16, or E4M3 codes for fp8;
+ *   *h_scale_offset fp8 only (0 otherwise): byte offset of h's fp32 scales --
+ *                   G(128): [I/128][*scale_stride], transposed (the scale of row p and
+ *                   128-column group g at g * *scale_stride + p); "A" and "T": [S],
+ *                   one per row (*scale_stride = 1; "T" repeats the tensor's scale);
+ *   *scale_stride   as above (0 for bf16).
+ * Same sizes and qc as the moe_experts call.  Returns MOE_ERR_INVALID_ARG on a bad
+ * size or null pointer, MOE_ERR_UNSUPPORTED for a qc moe_experts rejects.  The
+ * pages have no counterpart: it exposes a stage of the experts to the caller. */
+moe_status_t moe_workspace_intermediate(int T, int H, int I, int E, int top_k, const moe_quant_config *qc,
+                                        size_t *h_offset, size_t *h_scale_offset, int *scale_stride);
+
 /* Several expert problems with the same hidden size H in the same two GEMM
  * launches -- typically a layer's routed experts and its shared expert (E = 1,
  * top_k = 1, sorted_slot NULL).  Not in the pages: their shared-expert row is a
@@ -317,6 +332,12 @@ moe_status_t moe_experts_nvfp4(const void *a1q, const void *a1q_sf, const float 
                                int activation, void *fused_expert_output, void *ws, size_t ws_bytes,
                                moe_stream_t stream);
 size_t moe_workspace_size_nvfp4(int T, int H, int I, int E, int top_k);
+/* Where moe_experts_nvfp4 leaves the intermediate in its workspace: byte offsets of
+ * the bf16 h [S, I] that the first GEMM writes, and of its NVFP4 codes [S, I/2] and
+ * scale codes [S, I/16] that the second GEMM reads (S = T * top_k sorted rows).
+ * H % 256 == 0 and I % 256 == 0, else MOE_ERR_INVALID_ARG. */
+moe_status_t moe_workspace_intermediate_nvfp4(int T, int H, int I, int E, int top_k, size_t *hb_offset,
+                                              size_t *hq_offset, size_t *hsf_offset);
 
 /* ------------------------------------------------------------------ single-launch layer
  * The whole bf16 layer step in one cooperative kernel launch -- the monolithic form of
@@ -375,6 +396,16 @@ moe_status_t moe_finalize(void *output, const void *fused_expert_output, const f
  * kernel return.  moe_device_status synchronises the current device, returns
  * the recorded status (MOE_OK when none) and clears it when `clear` != 0. */
 moe_status_t moe_device_status(int clear);
+
+/* Self-test of that failure path (the pages have no counterpart; it is not a step of the
+ * layer): launches one thread that waits, with the same bounded wait the GEMM kernels
+ * use, on a barrier no thread ever arrives on, giving up after limit_ns nanoseconds
+ * (1e3 .. 1e10) instead of the usual two seconds.  The wait runs out, MOE_ERR_TIMEOUT is
+ * recorded in the device status word and the kernel returns normally: the context stays
+ * usable, moe_device_status reports the timeout (and clears it when asked).  Nothing
+ * faults, traps or hangs.  Asynchronous on stream; MOE_ERR_INVALID_ARG for a limit out of
+ * range. */
+moe_status_t moe_selftest_wait_timeout(uint64_t limit_ns, moe_stream_t stream);
 const char *moe_status_string(moe_status_t status);
 
 #ifdef __cplusplus

@@ -2104,6 +2104,22 @@ moe_status_t experts_nvfp4_run(const void* a1q, const void* a1q_sf, const float*
   return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
+// Self-test of the failure path of the device-side waits: one thread waits (bounded) on an
+// mbarrier that no thread arrives on, with the GEMMs' wait routine and a caller-chosen
+// limit; the wait gives up, records MOE_ERR_TIMEOUT and the kernel returns.
+__global__ void __launch_bounds__(32) selftest_wait_kernel(uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+  if (threadIdx.x == 0) {
+    mbar_wait(&bar, 0, false, limit_ns);  // phase 0 never completes: no arrival
+    mbar_inval(&bar);
+  }
+}
+
 }  // namespace
 
 MOE_DEFINE_STATUS_READER(experts_status)
@@ -2349,4 +2365,10 @@ extern "C" moe_status_t moe_layer_fused(const float* logits, const void* a1, int
                          fp) != cudaSuccess)
     return MOE_ERR_CUDA;
   return MOE_OK;
+}
+
+extern "C" moe_status_t moe_selftest_wait_timeout(uint64_t limit_ns, moe_stream_t stream) {
+  MOE_CHECK_ARG(limit_ns >= 1000ull && limit_ns <= 10000000000ull);
+  selftest_wait_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(limit_ns);
+  return launch_status();
 }

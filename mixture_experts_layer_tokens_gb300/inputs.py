@@ -75,6 +75,12 @@ def _cfgs():
     for T in (4096, 8192):
         c[f"mixtral_T{T}"] = LayerConfig(f"mixtral_T{T}", T, 4096, 14336, 8, 2,
                                          description=f"Mixtral-8x7B-like layer T{T} H4096 I14336 E8 top2 bf16 (prefill)")
+    # Qwen3-MoE-like layers: the Qwen3-30B-A3B expert shape (128 experts of intermediate size 768
+    # over hidden 2048, top-8, no shared expert, softmax top-k renormalised), ~256 rows per expert
+    c["qwen3"] = LayerConfig("qwen3", 4096, 2048, 768, 128, 8,
+                             description="Qwen3-MoE-like layer T4096 H2048 I768 E128 top8 bf16")
+    c["qwen3_fp8"] = LayerConfig("qwen3_fp8", 4096, 2048, 768, 128, 8, quant="fp8",
+                                 description="Qwen3-MoE-like layer T4096 H2048 I768 E128 top8 fp8 G(128)")
     c["deepseek_T16384"] = LayerConfig("deepseek_T16384", 16384, 7168, 2048, 256, 8, quant="fp8", shared_I=2048,
                                        description="DeepSeek-V3-like layer T16384 H7168 I2048 E256 top8 fp8 + bf16 shared (prefill)")
     # same per-expert shape as the DeepSeek-V3-like layer (~128 rows per expert), a quarter of the

@@ -80,6 +80,8 @@ SIGNATURES = {
     "moe_experts_multi": ([_EPP, _I, _I, _QCP, _I, _P, _Z, _P], _I),
     "moe_workspace_size_multi": ([_EPP, _I, _I, _QCP], _Z),
     "moe_workspace_size": ([_I, _I, _I, _I, _I, _QCP], _Z),
+    "moe_workspace_intermediate": ([_I, _I, _I, _I, _I, _QCP, _P, _P, _P], _I),
+    "moe_workspace_intermediate_nvfp4": ([_I, _I, _I, _I, _I, _P, _P, _P], _I),
     "moe_prepare_nvfp4": ([_P, _P, _I, _I, _I, _I, _P, _P, _P, _P], _I),
     "moe_experts_nvfp4": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P,
                            _Z, _P], _I),
@@ -88,6 +90,7 @@ SIGNATURES = {
     "moe_layer_fused_workspace_size": ([_I, _I, _I, _I, _I, _I], _Z),
     "moe_finalize": ([_P, _P, _P, _P, _P, _P, _P, _F, _I, _I, _I, _I, _I, _P, _F, _P, _P], _I),
     "moe_device_status": ([_I], _I),
+    "moe_selftest_wait_timeout": ([ctypes.c_uint64, _P], _I),
     "moe_status_string": ([_I], ctypes.c_char_p),
 }
 
@@ -239,6 +242,42 @@ def moe_prepare(a1: torch.Tensor, topk_weights: Optional[torch.Tensor], top_k: i
 
 def workspace_size(T: int, H: int, I: int, E: int, top_k: int, quant: str) -> int:
     return int(lib().moe_workspace_size(T, H, I, E, top_k, ctypes.byref(_qc(quant))))
+
+
+def experts_intermediate(ws: torch.Tensor, T: int, H: int, I: int, E: int, top_k: int, quant: str):
+    """Views into a moe_experts workspace of the intermediate h that the call left
+    there (``moe_workspace_intermediate``): h [S, I] (bf16, or uint8 E4M3 codes for the
+    fp8 formats) and its fp32 scales -- G(128): [I/128, S] (transposed, row stride
+    s_pad), "A"/"T": [S] -- or None for bf16.  S = T * top_k rows in expert order."""
+    off, soff, stride = ctypes.c_size_t(), ctypes.c_size_t(), ctypes.c_int()
+    _check("moe_workspace_intermediate", lib().moe_workspace_intermediate(
+        T, H, I, E, top_k, ctypes.byref(_qc(quant)), ctypes.byref(off), ctypes.byref(soff), ctypes.byref(stride)))
+    S = T * top_k
+    fp8 = quant != "bf16"
+    esz = 1 if fp8 else 2
+    h = ws[off.value:off.value + S * I * esz]
+    h = h.view(S, I) if fp8 else h.view(torch.bfloat16).view(S, I)
+    if not fp8:
+        return h, None
+    if quant == "fp8":
+        n = (I // 128) * stride.value
+        sc = ws[soff.value:soff.value + 4 * n].view(torch.float32).view(I // 128, stride.value)[:, :S]
+    else:
+        sc = ws[soff.value:soff.value + 4 * S].view(torch.float32)
+    return h, sc
+
+
+def experts_intermediate_nvfp4(ws: torch.Tensor, T: int, H: int, I: int, E: int, top_k: int):
+    """Views into a moe_experts_nvfp4 workspace (``moe_workspace_intermediate_nvfp4``):
+    the bf16 h [S, I] of the first GEMM and its NVFP4 codes [S, I/2] and scale codes
+    [S, I/16] that the second GEMM read."""
+    hb, hq, hsf = ctypes.c_size_t(), ctypes.c_size_t(), ctypes.c_size_t()
+    _check("moe_workspace_intermediate_nvfp4", lib().moe_workspace_intermediate_nvfp4(
+        T, H, I, E, top_k, ctypes.byref(hb), ctypes.byref(hq), ctypes.byref(hsf)))
+    S = T * top_k
+    return (ws[hb.value:hb.value + S * I * 2].view(torch.bfloat16).view(S, I),
+            ws[hq.value:hq.value + S * I // 2].view(S, I // 2),
+            ws[hsf.value:hsf.value + S * I // 16].view(S, I // 16))
 
 
 def moe_experts(a1q: torch.Tensor, a1q_scale: Optional[torch.Tensor], w13: torch.Tensor,
@@ -440,3 +479,9 @@ def moe_finalize(fused_expert_output: torch.Tensor, topk_weights: Optional[torch
 
 def moe_device_status(clear: bool = True) -> int:
     return int(lib().moe_device_status(int(clear)))
+
+
+def moe_selftest_wait_timeout(limit_ns: int, stream=None) -> None:
+    """Launch the library's self-test of a device-side wait that runs out (see moe.h):
+    afterwards moe_device_status() reports MOE_ERR_TIMEOUT."""
+    _check("moe_selftest_wait_timeout", lib().moe_selftest_wait_timeout(int(limit_ns), _stream(stream)))

@@ -14,28 +14,63 @@ import torch
 from mixture_experts_layer_tokens_gb300 import moe
 from mixture_experts_layer_tokens_gb300.inputs import CONFIGS, make_inputs, scaled
 from oracle import moe_ref
-from parity_util import check_bf16, check_fp8, half_ulp_bf16, to64
+from parity_util import (E4M3_VALUES, check_bf16, check_fp8, check_fp8_intermediate, fp8_row_scales, half_ulp_bf16,
+                         to64)
 
 pytestmark = pytest.mark.gpu
 
 
-def _run(inp, ids, dev, quant, identity=False, act="silu", w13=None, w13_scale=None):
+def _run(inp, ids, dev, quant, identity=False, act="silu", w13=None, w13_scale=None, stages=False):
     cfg = inp.cfg
     E, k = cfg.E, ids.shape[1]
+    T, H = inp.a1.shape
+    I = inp.w2.shape[2]
     w13 = inp.w13 if w13 is None else w13
     w13_scale = inp.w13_scale if w13_scale is None else w13_scale
     al = moe.moe_align(ids.to(dev), E)
     a1q, sc = moe.moe_prepare(inp.a1.to(dev), None, k, False, quant)
     d = lambda t: None if t is None else t.to(dev)
+    ws = torch.empty(max(moe.workspace_size(T, H, I, E, k, quant), 16), dtype=torch.uint8, device=dev)
     y = moe.moe_experts(a1q, sc, d(w13), d(w13_scale), d(inp.w2), d(inp.w2_scale), al, quant,
-                        identity=identity, activation=act)
+                        identity=identity, activation=act, ws=ws)
     torch.cuda.synchronize()
     assert moe.moe_device_status() == moe.MOE_OK
     ral = moe_ref.align(ids, E, 128)
     rq, rs = moe_ref.prepare(inp.a1, None, False, quant)
     assert torch.equal(a1q.cpu(), rq)
     yref = moe_ref.experts(rq, rs, w13, w13_scale, inp.w2, inp.w2_scale, ral, k, quant, act)
+    if stages:
+        _fp8_stages(inp, ral, rq, rs, w13, w13_scale, quant, act, ws, y, f"experts {quant} {act}")
     return y, yref
+
+
+def _fp8_stages(inp, ral, rq, rs, w13, w13_scale, quant, act, ws, y, what):
+    """The fp8 experts stage by stage: the GPU's intermediate (codes and scales left in
+    the workspace) against the oracle's quantisation of its own h, then the GPU's
+    expert rows against the oracle's second GEMM applied to the GPU's intermediate, at
+    the bf16 bound (both sides then hold the same h)."""
+    T, H = inp.a1.shape
+    E, k, I = w13.shape[0], int(ral.sorted_slot.numel()) // max(T, 1), inp.w2.shape[2]
+    h_gpu, hs_gpu = moe.experts_intermediate(ws, T, H, I, E, k, quant)
+    offs, order = ral.expert_offsets.numpy(), ral.sorted_slot.numpy()
+    S = int(offs[-1])
+    codes = h_gpu[:S].cpu().numpy()
+    scales = fp8_row_scales(hs_gpu, quant, np.arange(S), I // 128)
+    h_ref = np.zeros((S, I))
+    for e in range(E):
+        p0, p1 = int(offs[e]), int(offs[e + 1])
+        if p0 < p1:
+            A = moe_ref._act64(rq, rs, order[p0:p1] // k, quant)
+            h_ref[p0:p1] = moe_ref.activation(A @ moe_ref._weights64(w13, w13_scale, e, quant).T, act).numpy()
+    check_fp8_intermediate(codes, scales, h_ref, quant, what)
+    h_deq = E4M3_VALUES[codes] * np.repeat(scales, 128, axis=1)
+    y2 = torch.zeros((S, H), dtype=torch.float64)
+    for e in range(E):
+        p0, p1 = int(offs[e]), int(offs[e + 1])
+        if p0 < p1:
+            y2[torch.from_numpy(order[p0:p1].astype(np.int64))] = moe_ref._expert_out(
+                h_deq[p0:p1], moe_ref._weights64(inp.w2, inp.w2_scale, e, quant))
+    check_bf16(y, y2, what + ": second GEMM on the GPU's intermediate", slack=_stored_pair_slack(y2))
 
 
 def _stored_pair_slack(yref):
@@ -82,8 +117,9 @@ def test_experts_bf16(cuda_dev, T, H, I, E, k, skew):
 ])
 def test_experts_fp8(cuda_dev, T, H, I, E, k, skew):
     inp = make_inputs(scaled(CONFIGS["deepseek"], T=T, H=H, I=I, E=E, top_k=k, shared_I=0))
-    y, yref = _run(inp, _ids(T, k, E, T + I, skew), cuda_dev, "fp8")
-    check_fp8(y, yref, "experts fp8")
+    y, yref = _run(inp, _ids(T, k, E, T + I, skew), cuda_dev, "fp8", stages=True)
+    rel, _ = check_fp8(y, yref, "experts fp8")
+    print(f"experts fp8 T{T} H{H} I{I} E{E} k{k}: relative Frobenius vs the oracle {rel:.2e} (bound 3e-2)")
 
 
 def test_experts_identity_permutation(cuda_dev):
@@ -133,9 +169,11 @@ def test_experts_activations(cuda_dev, T, H, I, E, k, quant, act):
     if act.endswith("_no_mul"):
         w13 = w13[:, :I].contiguous()
         w13_scale = None if w13_scale is None else w13_scale[:, :I // 128].contiguous()
-    y, yref = _run(inp, _ids(T, k, E, T + I + 7), cuda_dev, quant, act=act, w13=w13, w13_scale=w13_scale)
+    y, yref = _run(inp, _ids(T, k, E, T + I + 7), cuda_dev, quant, act=act, w13=w13, w13_scale=w13_scale,
+                   stages=quant != "bf16")
     if quant != "bf16":
-        check_fp8(y, yref, f"experts {quant} {act}")
+        rel, _ = check_fp8(y, yref, f"experts {quant} {act}")
+        print(f"experts {quant} {act}: relative Frobenius vs the oracle {rel:.2e} (bound 3e-2)")
     else:
         check_bf16(y, yref, f"experts bf16 {act}", slack=_stored_pair_slack(yref))
 

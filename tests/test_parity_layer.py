@@ -109,6 +109,10 @@ SMALL = {
     "single_max_slots": scaled(CONFIGS["mixtral_fused"], T=256, H=256, I=256, E=64, top_k=8),
     # weight on the input before the NVFP4 quantisation, bf16 shared expert beside the NVFP4 experts
     "llama_small_nvfp4": scaled(CONFIGS["llama8"], T=100, H=512, I=512, shared_I=256, quant="nvfp4"),
+    # the Qwen3-MoE-like expert shape (H 2048, I 768: six 128-column groups of h) with 16 rows per
+    # expert on average over 128 experts
+    "qwen3_small": scaled(CONFIGS["qwen3"], T=256),
+    "qwen3_small_fp8": scaled(CONFIGS["qwen3_fp8"], T=256),
 }
 
 
@@ -124,7 +128,8 @@ def test_layer_small_all_tokens(cuda_dev, name):
     _check(cfg, out, ref, name)
 
 
-@pytest.mark.parametrize("name,sample", [("mixtral", 12), ("deepseek", 3), ("llama1", 1), ("llama8", 8),
+@pytest.mark.parametrize("name,sample", [("mixtral", 12), ("deepseek", 3), ("qwen3", 8), ("qwen3_fp8", 8),
+                                         ("llama1", 1), ("llama8", 8),
                                          ("llama64", 6), ("llama512", 6), ("mixtral_nvfp4", 12),
                                          ("llama1_nvfp4", 1), ("llama1_fused", 1), ("llama64_fused", 6),
                                          ("mixtral_fused", 12)])
@@ -162,3 +167,53 @@ def test_single_launch_matches_the_separate_calls(cuda_dev):
     assert moe.moe_device_status() == moe.MOE_OK
     assert torch.equal(single.topk_ids, sep.topk_ids) and torch.equal(single.topk_weights, sep.topk_weights)
     check_bf16(o1, o2.double(), "single launch vs separate calls", slack=ulp_bf16(o2.double().cpu().numpy()))
+
+
+def test_deepseek_full_size_sampled_expert_rows(cuda_dev):
+    """The DeepSeek-V3-like layer at full size (T 4096, 256 experts of ~128 rows, fp8
+    G(128)), run as the bench runs it, checked stage by stage on one sorted row of each
+    of 48 experts: the last row of 24 experts that have a second, partial 128-row tile,
+    and a row of 24 experts with one tile (their first and last rows among them).  For
+    each row: prepare bit-exact for its token; the intermediate h (codes and scales left
+    in the workspace) against the oracle's quantisation of its own h; the expert row
+    against the oracle's second GEMM on the GPU's intermediate, at the bf16 bound."""
+    from parity_util import E4M3_VALUES, check_fp8_intermediate, fp8_row_scales, half_ulp_bf16
+    cfg = CONFIGS["deepseek"]
+    T, H, I, E, k = cfg.T, cfg.H, cfg.I, cfg.E, cfg.top_k
+    inp = make_inputs(cfg, device=cuda_dev)
+    layer = MoELayer(inp)
+    layer.forward(inp.logits, inp.a1)
+    torch.cuda.synchronize()
+    assert moe.moe_device_status() == moe.MOE_OK
+    offs = layer.al.expert_offsets.cpu().numpy()
+    order = layer.al.sorted_slot.cpu().numpy()
+    counts = np.diff(offs)
+    rng = np.random.default_rng(7)
+    two = [e for e in range(E) if counts[e] > 128]
+    one = [e for e in range(E) if 0 < counts[e] <= 128]
+    assert len(two) >= 24 and len(one) >= 24
+    picks = [(int(e), int(offs[e + 1] - 1)) for e in rng.choice(two, 24, replace=False)]
+    singles = rng.choice(one, 24, replace=False)
+    for i, e in enumerate(singles):
+        r = 0 if i == 0 else (counts[e] - 1 if i == 1 else int(rng.integers(0, counts[e])))
+        picks.append((int(e), int(offs[e] + r)))
+    h_gpu, hs_gpu = moe.experts_intermediate(layer.ws, T, H, I, E, k, "fp8")
+    rows = np.array([p for _, p in picks])
+    codes = h_gpu[torch.from_numpy(rows).to(cuda_dev)].cpu().numpy()
+    scales = fp8_row_scales(hs_gpu, "fp8", rows, I // 128)
+    h_ref = np.zeros((len(picks), I))
+    y_gpu = torch.zeros((len(picks), H), dtype=torch.float64)
+    y_ref = torch.zeros((len(picks), H), dtype=torch.float64)
+    h_deq = E4M3_VALUES[codes] * np.repeat(scales, 128, axis=1)
+    for i, (e, p) in enumerate(picks):
+        f = int(order[p])
+        t = f // k
+        rq, rs = moe_ref.prepare(inp.a1[t:t + 1].cpu(), None, False, "fp8")
+        assert torch.equal(layer.a1q[t:t + 1].cpu(), rq) and torch.equal(layer.a1q_scale[t:t + 1].cpu(), rs)
+        A = moe_ref._act64(rq, rs, np.array([0]), "fp8")
+        h_ref[i] = moe_ref.silu_and_mul(A @ moe_ref._weights64(inp.w13, inp.w13_scale, e, "fp8").T).numpy()[0]
+        y_ref[i] = moe_ref._expert_out(h_deq[i:i + 1], moe_ref._weights64(inp.w2, inp.w2_scale, e, "fp8"))[0]
+        y_gpu[i] = layer.y[f].double().cpu()
+    check_fp8_intermediate(codes, scales, h_ref, "fp8", "deepseek full size: sampled rows")
+    check_bf16(y_gpu, y_ref, "deepseek full size: second GEMM on the GPU's intermediate",
+               slack=half_ulp_bf16(y_ref.numpy()))

@@ -13,7 +13,7 @@ import torch
 from mixture_experts_layer_tokens_gb300 import moe
 from mixture_experts_layer_tokens_gb300.inputs import CONFIGS, NVFP4_A1_GSCALE, NVFP4_H_GSCALE, make_inputs, scaled
 from oracle import codecs, moe_ref
-from parity_util import check_nvfp4
+from parity_util import check_bf16, check_nvfp4, half_ulp_bf16, ulp_bf16
 
 pytestmark = pytest.mark.gpu
 
@@ -56,17 +56,49 @@ def _run(T, H, I, E, k, ids, dev, act="silu", identity=False, seed=0):
     d = lambda t: t.to(dev)
     al = moe.moe_align(d(ids), E)
     q, sf = moe.moe_prepare_nvfp4(d(inp.a1), None, k, False, NVFP4_A1_GSCALE)
+    ws = torch.empty(max(moe.workspace_size_nvfp4(T, H, I, E, k), 16), dtype=torch.uint8, device=dev)
     y = moe.moe_experts_nvfp4(q, sf, NVFP4_A1_GSCALE, d(inp.w13), d(inp.w13_scale), d(inp.extra["w13_gscale"]),
                               d(inp.w2), d(inp.w2_scale), d(inp.extra["w2_gscale"]), NVFP4_H_GSCALE, al,
-                              identity=identity, activation=act)
+                              identity=identity, activation=act, ws=ws)
     torch.cuda.synchronize()
     assert moe.moe_device_status() == moe.MOE_OK
     rq, rsf = moe_ref.prepare_nvfp4(inp.a1, None, False, NVFP4_A1_GSCALE)
     _same_codes(q, sf, rq, rsf)
-    yref = moe_ref.experts_nvfp4(rq, rsf, NVFP4_A1_GSCALE, inp.w13, inp.w13_scale, inp.extra["w13_gscale"], inp.w2,
-                                 inp.w2_scale, inp.extra["w2_gscale"], NVFP4_H_GSCALE, moe_ref.align(ids, E, 128), k,
-                                 act)
+    ral = moe_ref.align(ids, E, 128)
+    yref, h_ref = moe_ref.experts_nvfp4(rq, rsf, NVFP4_A1_GSCALE, inp.w13, inp.w13_scale, inp.extra["w13_gscale"],
+                                        inp.w2, inp.w2_scale, inp.extra["w2_gscale"], NVFP4_H_GSCALE, ral, k, act,
+                                        return_h=True)
+    _stages(inp, ral, ws, y, h_ref, T, H, I, E, k, f"experts nvfp4 T{T} H{H} I{I} E{E} k{k} {act}")
     return y, yref
+
+
+def _stages(inp, ral, ws, y, h_ref, T, H, I, E, k, what):
+    """NVFP4 experts stage by stage.  GEMM1: the GPU's bf16 h (left in the workspace)
+    against the oracle's fp64 h, within one bf16 step (plus 1e-3 of the row's RMS for
+    the fp32 summation order).  Quantisation: the GPU's codes and scale codes equal the
+    oracle quantiser's on the GPU's own bf16 h, bit for bit.  GEMM2: the expert rows
+    against the oracle's second GEMM on the GPU's codes, at the bf16 bound."""
+    hb, hq, hsf = moe.experts_intermediate_nvfp4(ws, T, H, I, E, k)
+    offs, order = ral.expert_offsets.numpy(), ral.sorted_slot.numpy()
+    S = int(offs[-1])
+    if S == 0:
+        return
+    hb64 = hb[:S].double().cpu().numpy()
+    rms = np.sqrt((h_ref ** 2).mean(axis=1, keepdims=True))
+    over = np.abs(hb64 - h_ref) > ulp_bf16(h_ref) + 1e-3 * rms
+    assert not over.any(), f"{what}: {int(over.sum())} elements of the bf16 intermediate beyond one bf16 step"
+    rq, rsf = moe_ref.nvfp4_quantize_fp32(hb64, NVFP4_H_GSCALE)
+    _same_codes(hq[:S], hsf[:S], torch.from_numpy(rq), torch.from_numpy(rsf))
+    hdeq = moe_ref.nvfp4_dequantize(hq[:S].cpu().numpy(), hsf[:S].cpu().numpy(), NVFP4_H_GSCALE)
+    g2 = inp.extra["w2_gscale"].double().numpy().reshape(-1)
+    y2 = torch.zeros((S, H), dtype=torch.float64)
+    for e in range(E):
+        p0, p1 = int(offs[e]), int(offs[e + 1])
+        if p0 < p1:
+            W2 = moe_ref.nvfp4_dequantize(inp.w2[e].numpy(), inp.w2_scale[e].numpy(), g2[e])
+            y2[torch.from_numpy(order[p0:p1].astype(np.int64))] = moe_ref._expert_out(hdeq[p0:p1],
+                                                                                        torch.from_numpy(W2))
+    check_bf16(y, y2, what + ": second GEMM on the GPU's intermediate", slack=half_ulp_bf16(y2.numpy()))
 
 
 @pytest.mark.parametrize("T,H,I,E,k,skew", [
