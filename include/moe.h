@@ -339,6 +339,52 @@ size_t moe_workspace_size_nvfp4(int T, int H, int I, int E, int top_k);
 moe_status_t moe_workspace_intermediate_nvfp4(int T, int H, int I, int E, int top_k, size_t *hb_offset,
                                               size_t *hq_offset, size_t *hsf_offset);
 
+/* ------------------------------------------------------------------ batched activation format
+ * The "batched" format of the prepare output ("Fused MoE Kernel Features", section "Fused MoE
+ * Modular All2All backends": a prepare returns its activations in the standard or the batched
+ * format and the finalize takes that format back to standard; "Fused Experts Kernels" lists
+ * batched entry points).  The pages leave the layout to another document; the reading here:
+ * one slab per expert, [E, max_tokens, H]: expert e's slab holds, in ascending slot order, the
+ * prepared rows of the tokens that chose e, and expert_num_tokens[e] counts them.  Rows past a
+ * count are neither written nor read.
+ *
+ * moe_prepare_batched: moe_prepare (same qc, same weight on the input) of every token, then
+ *   token t's prepared row copied to the slab of each expert it chose.  expert_offsets and
+ *   sorted_slot are moe_align's (they give each expert's slots in ascending order).  Outputs:
+ *   a1q_b [E, max_tokens, H] (bf16 or E4M3 codes); a1q_b_scale: G(128) [E, max_tokens, H/128],
+ *   "A" [E, max_tokens], "T" [1] (fp32; unused for bf16, may be NULL); expert_num_tokens [E]
+ *   int32 (each count capped at max_tokens).  A slot past max_tokens in its expert's slab is
+ *   left out and MOE_ERR_INVALID_ARG is recorded in the device status word (moe_device_status);
+ *   nothing is written out of bounds.  ws: moe_prepare_batched_workspace_size(T, H, qc) bytes
+ *   (bf16 without the weight on the input needs none: the rows come from a1 itself).
+ * moe_experts_batched: the experts of moe_experts_act on the slabs: for every expert e and row
+ *   m < expert_num_tokens[e] (taken as min(max(count, 0), max_tokens)), out_b[e, m] =
+ *   expert_e(a1q_b[e, m]); out_b [E, max_tokens, H] bf16, unweighted; other rows untouched.
+ *   Same weights, qc, activations and intermediate as moe_experts_act.  ws:
+ *   moe_workspace_size_batched(E, max_tokens, H, I, qc) bytes.  H % 128 == 0, I % 128 == 0.
+ * moe_finalize_batched: moe_finalize reading the expert row of slot f = t * top_k + j from
+ *   expert_output_b [E, max_tokens, H] at (e = topk_ids[f], inv_slot[f] - expert_offsets[e])
+ *   (moe_align's inv_slot and expert_offsets); every other argument, output and check as for
+ *   moe_finalize. */
+size_t moe_prepare_batched_workspace_size(int T, int H, const moe_quant_config *qc);
+moe_status_t moe_prepare_batched(const void *a1, const float *topk_weights, const int32_t *expert_offsets,
+                                 const int32_t *sorted_slot, int T, int H, int top_k, int E, int max_tokens,
+                                 int apply_router_weight_on_input, const moe_quant_config *qc, void *a1q_b,
+                                 float *a1q_b_scale, int32_t *expert_num_tokens, void *ws, size_t ws_bytes,
+                                 moe_stream_t stream);
+size_t moe_workspace_size_batched(int E, int max_tokens, int H, int I, const moe_quant_config *qc);
+moe_status_t moe_experts_batched(const void *a1q_b, const float *a1q_b_scale, const void *w13,
+                                 const float *w13_scale, const void *w2, const float *w2_scale,
+                                 const int32_t *expert_num_tokens, int E, int max_tokens, int H, int I,
+                                 const moe_quant_config *qc, int activation, void *out_b, void *ws,
+                                 size_t ws_bytes, moe_stream_t stream);
+moe_status_t moe_finalize_batched(void *output, const void *expert_output_b, int max_tokens,
+                                  const float *topk_weights, const int32_t *topk_ids, const int32_t *inv_slot,
+                                  const int32_t *expert_offsets, const void *shared, const void *residual,
+                                  const void *rms_weight, float eps, int T, int H, int top_k,
+                                  int apply_router_weight_on_input, moe_dtype_t out_dtype, uint8_t *out_scale,
+                                  float out_global_scale, void *residual_out, moe_stream_t stream);
+
 /* ------------------------------------------------------------------ single-launch layer
  * The whole bf16 layer step in one cooperative kernel launch -- the monolithic form of
  * the experts ("[vLLM] MoE Oracle & Prepare/Finalize", section "Modular vs

@@ -25,7 +25,9 @@ extern "C" moe_status_t moe_device_status(int clear) {
   if (cudaDeviceSynchronize() != cudaSuccess) return MOE_ERR_CUDA;
   const moe_status_t a = experts_status(clear);
   const moe_status_t b = align_status(clear);
-  return a != MOE_OK ? a : b;
+  const moe_status_t c = prepare_status(clear);
+  const moe_status_t d = finalize_status(clear);
+  return a != MOE_OK ? a : (b != MOE_OK ? b : (c != MOE_OK ? c : d));
 }
 
 extern "C" const char* moe_status_string(moe_status_t status) {

@@ -53,6 +53,8 @@ static __device__ int g_moe_status = 0;
 
 moe_status_t align_status(int clear);
 moe_status_t experts_status(int clear);
+moe_status_t prepare_status(int clear);
+moe_status_t finalize_status(int clear);
 
 __device__ __forceinline__ void record_status(int code) { atomicCAS(&g_moe_status, 0, code); }
 

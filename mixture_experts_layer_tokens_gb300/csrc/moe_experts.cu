@@ -148,7 +148,8 @@ struct Cfg {
 };
 
 struct GemmParams {
-  const int32_t* offsets;      // [E + 1]
+  const int32_t* offsets;      // [E + 1] (batched format: expert e's slab starts at offsets[e])
+  const int32_t* counts;       // batched format: [E] rows of each slab; NULL: rows end at offsets[e + 1]
   const int32_t* group_map;    // [groups][2] (expert, first row), built by plan_kernel
   const int32_t* num_groups;   // [1]
   const int32_t* sorted_slot;  // gemm2 scatter target rows; NULL = identity
@@ -200,7 +201,7 @@ __device__ __forceinline__ Unit decode(const GemmParams& p, int u) {
   it.e = ld_tab<kCoh>(p.group_map + 2 * gb);
   const int r0 = ld_tab<kCoh>(p.group_map + 2 * gb + 1);
   const int off = ld_tab<kCoh>(p.offsets + it.e);
-  const int end = ld_tab<kCoh>(p.offsets + it.e + 1);
+  const int end = p.counts ? off + ld_tab<kCoh>(p.counts + it.e) : ld_tab<kCoh>(p.offsets + it.e + 1);
   const int gstart = gb - (r0 - off) / (MG * BM);
   const int gcnt = (end - off + MG * BM - 1) / (MG * BM);
   const int local = u - gstart * p.NT;
@@ -1010,10 +1011,12 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
   }
 
   // ------------------------------------------------------------ teardown
-  // After a failed wait some MMAs may still be in flight: wait (bounded) for
-  // the MMA pipe to drain before the TMEM is released.  (A phase of a longer kernel
-  // always drains: every commit must have arrived before its barriers are reused.)
-  if (warp == 1 && (status_failed() || !standalone)) {
+  // The MMA pipe drains (bounded wait) before the TMEM is released and the CTA exits:
+  // after a failed wait MMAs may still be in flight, and on a normal exit the last
+  // stages' commit arrivals on their empty barriers may still be pending -- once the CTA
+  // has exited, its shared memory can belong to another CTA (a phase of a longer kernel
+  // reuses its barriers too).
+  if (warp == 1) {
     if (lane == 0) {
       tc_commit(drain);
       mbar_wait(drain, 0, false, 100000000ull);
@@ -1378,7 +1381,8 @@ struct WsLayout {
 
 // group: the fp8 activation format (128, MOE_GROUP_TOKEN or MOE_GROUP_TENSOR); the
 // "A"/"T" formats add the bf16 intermediate and the tensor format's amax word.
-WsLayout ws_layout(const moe_experts_problem* pr, int n, int H, bool fp8, int grid, int group) {
+WsLayout ws_layout(const moe_experts_problem* pr, int n, int H, bool fp8, int grid, int group,
+                   bool rows_in_place = false) {
   WsLayout L{};
   const int esz = fp8 ? 1 : 2;
   const int MG = fp8 ? 1 : 2;  // the larger bound of either GEMM
@@ -1394,7 +1398,7 @@ WsLayout ws_layout(const moe_experts_problem* pr, int n, int H, bool fp8, int gr
     P.nflags2 = cap_groups * ((H + 255) / 256);
     L.nflags += P.nflags1 + P.nflags2;
     P.A = off;
-    off = al256(off + (size_t)S * H * esz);
+    off = al256(off + (rows_in_place ? 0 : (size_t)S * H * esz));
     P.As = off;
     off = al256(off + (fp8 ? (size_t)(H / 128) * P.s_pad * 4 : 0));
     P.h = off;
@@ -1972,6 +1976,198 @@ FusedLayout fused_layout(int T, int H, int I, int E, int top_k, bool shared, int
   return L;
 }
 
+// ------------------------------------------------------------------ batched activation format
+// The experts on the batched format ("Fused MoE Kernel Features": the prepare output is
+// "standard" or "batched"; "Fused Experts Kernels" lists batched entry points): one slab
+// per expert [E, max_tokens, H] with a row count per expert.  The slabs are the GEMMs'
+// rows in place (expert e's rows start at e * max_tokens), so there is no gather of rows;
+// a plan launch writes the slab bases, the counts clamped to max_tokens and the tile map
+// of the counted rows, and the GEMMs are those of moe_experts, ending each expert's rows
+// at its count.  The output rows take the same places in an [E, max_tokens, H] output.
+__global__ void __launch_bounds__(1024)
+    batched_plan_kernel(const int32_t* __restrict__ counts_in, int E, int max_tokens, int32_t* __restrict__ offsets,
+                        int32_t* __restrict__ counts, int32_t* __restrict__ tile_map, int32_t* __restrict__ num_tiles,
+                        int* __restrict__ flags, int nflags) {
+  __shared__ int warp_tot[32];
+  __shared__ int carry;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int i = threadIdx.x; i < nflags; i += 1024) flags[i] = 0;
+  if (threadIdx.x == 0) carry = 0;
+  for (int e = threadIdx.x; e <= E; e += 1024) offsets[e] = e * max_tokens;
+  __syncthreads();
+  for (int base = 0; base < E; base += 1024) {
+    const int e = base + threadIdx.x;
+    int c = 0;
+    if (e < E) {
+      c = min(max(counts_in[e], 0), max_tokens);
+      counts[e] = c;
+    }
+    const int nt = (c + BM - 1) / BM;
+    int x = nt;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, off);
+      if (lane >= off) x += y;
+    }
+    if (lane == 31) warp_tot[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+      const int w = warp_tot[lane];
+      int wx = w;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, wx, off);
+        if (lane >= off) wx += y;
+      }
+      warp_tot[lane] = wx - w;
+    }
+    __syncthreads();
+    const int first = carry + warp_tot[warp] + x - nt;
+    for (int i = 0; i < nt; ++i) {
+      tile_map[2 * (first + i)] = e;
+      tile_map[2 * (first + i) + 1] = e * max_tokens + i * BM;
+    }
+    __syncthreads();
+    if (threadIdx.x == 1023) carry = first + nt;
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) *num_tiles = carry;
+}
+
+struct BatchedLayout {
+  WsLayout L;
+  size_t offsets, counts, tiles, ntiles, total;
+  int cap;
+};
+
+BatchedLayout batched_layout(int E, int M, int H, int I, const moe_quant_config* qc, int grid) {
+  BatchedLayout B{};
+  const moe_experts_problem q = one_problem(nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
+                                            nullptr, nullptr, E * M, I, E, 1, nullptr);
+  B.L = ws_layout(&q, 1, H, qc->act == MOE_DT_FP8_E4M3, grid, qc->act_group, true);
+  B.cap = std::max(1, E * ((M + BM - 1) / BM));
+  size_t off = B.L.total;
+  B.offsets = off;
+  off = al256(off + (size_t)(E + 1) * 4);
+  B.counts = off;
+  off = al256(off + (size_t)E * 4);
+  B.tiles = off;
+  off = al256(off + (size_t)B.cap * 8);
+  B.ntiles = off;
+  off = al256(off + 4);
+  B.total = off;
+  return B;
+}
+
+moe_status_t experts_batched_run(const void* a1q_b, const float* a1q_b_scale, const void* w13, const float* w13_scale,
+                                 const void* w2, const float* w2_scale, const int32_t* expert_num_tokens, int E, int M,
+                                 int H, int I, const moe_quant_config* qc, int activation, void* out_b, void* ws,
+                                 size_t ws_bytes, cudaStream_t s) {
+  MOE_CHECK_ARG(qc && E >= 1 && M >= 1 && H > 0 && I > 0 && H % 128 == 0 && I % 128 == 0);
+  if (activation < MOE_ACT_SILU || activation > MOE_ACT_GELU_NO_MUL || !quant_ok(qc)) return MOE_ERR_UNSUPPORTED;
+  MOE_CHECK_ARG(fits_int32((long long)E * M + 4 * BM) && fits_int32((long long)E * 2 * I) &&
+                fits_int32((long long)E * H) && fits_int32((long long)H * 8));
+  const bool fp8 = qc->act == MOE_DT_FP8_E4M3;
+  const int group = qc->act_group;
+  const bool hb16 = fp8 && group != 128;
+  const bool no_mul = activation == MOE_ACT_SILU_NO_MUL || activation == MOE_ACT_GELU_NO_MUL;
+  MOE_CHECK_ARG(a1q_b && w13 && w2 && expert_num_tokens && out_b);
+  MOE_CHECK_ARG(!fp8 || (a1q_b_scale && w13_scale && w2_scale));
+  MOE_CHECK_ARG(aligned16(a1q_b) && aligned16(w13) && aligned16(w2) && aligned16(out_b));
+  const int grid = gemm_grid();
+  const BatchedLayout B = batched_layout(E, M, H, I, qc, grid);
+  if (!ws || ws_bytes < B.total) return MOE_ERR_WORKSPACE;
+  MOE_CHECK_ARG(aligned16(ws));
+  uint8_t* wsb = static_cast<uint8_t*>(ws);
+  const ProbLayout& P = B.L.p[0];
+  const long long S = (long long)E * M;
+  auto* offsets = reinterpret_cast<int32_t*>(wsb + B.offsets);
+  auto* counts = reinterpret_cast<int32_t*>(wsb + B.counts);
+  auto* tiles = reinterpret_cast<int32_t*>(wsb + B.tiles);
+  auto* ntiles = reinterpret_cast<int32_t*>(wsb + B.ntiles);
+  batched_plan_kernel<<<1, 1024, 0, s>>>(expert_num_tokens, E, M, offsets, counts, tiles, ntiles,
+                                         reinterpret_cast<int*>(wsb + B.L.flags), B.L.nflags);
+  if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+  float* As = fp8 ? reinterpret_cast<float*>(wsb + P.As) : nullptr;
+  if (fp8) {
+    // the slabs' activation scales transposed to [K/128][rows] (no rows move)
+    gather_kernel<<<(unsigned)((S + 7) / 8), 256, 0, s>>>(
+        nullptr, a1q_b_scale, nullptr, (int)S, 1, 0, hb16 ? 1 : H / 128, nullptr, As, P.s_pad,
+        group == 128 ? H / 128 : (group == MOE_GROUP_TOKEN ? 1 : 0), nullptr, 0, nullptr, 0, nullptr);
+    if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  void* h = wsb + P.h;
+  float* hs = fp8 ? reinterpret_cast<float*>(wsb + P.hs) : nullptr;
+  GemmMaps m1 = {}, m2 = {};
+  const int a2_rows = 256;
+  const bool b1_ok = no_mul ? make_map(&m1.b, w13, fp8, H, (long long)E * I, 256) : make_map_gate_up(&m1.b, w13, fp8, H, I, E);
+  if (!b1_ok || !make_map(&m1.a, a1q_b, fp8, H, S, 128) || !make_map(&m1.a2, a1q_b, fp8, H, S, a2_rows) ||
+      !make_map(&m2.a, h, fp8, I, S, 128) || !make_map(&m2.a2, h, fp8, I, S, a2_rows) ||
+      !make_map(&m2.b, w2, fp8, I, (long long)E * H, 256))
+    return MOE_ERR_CUDA;
+  GemmProblems g1 = {}, g2 = {};
+  g1.nprob = g2.nprob = 1;
+  GemmParams& p1 = g1.p[0];
+  p1.offsets = offsets;
+  p1.counts = counts;
+  p1.group_map = tiles;
+  p1.num_groups = ntiles;
+  p1.sorted_slot = nullptr;
+  p1.K = H;
+  p1.NT = no_mul ? (I + 255) / 256 : I / 128;
+  p1.I = I;
+  p1.H = H;
+  p1.b_rows = no_mul ? I : 2 * I;
+  p1.s_pad = P.s_pad;
+  p1.a_kstride = hb16 ? 0 : P.s_pad;
+  p1.a_scale_t = As;
+  p1.w_scale = w13_scale;
+  p1.out = hb16 ? (void*)(wsb + P.hb) : h;
+  p1.out_scale_t = hb16 ? nullptr : hs;
+  p1.flags = reinterpret_cast<int*>(wsb + P.flags1);
+  p1.partials = reinterpret_cast<float*>(wsb + B.L.partials);
+  p1.allow_split = 0;
+  GemmParams& p2 = g2.p[0];
+  p2 = p1;
+  p2.K = I;
+  p2.NT = (H + 255) / 256;
+  p2.b_rows = H;
+  p2.a_scale_t = hs;
+  p2.w_scale = w2_scale;
+  p2.out = out_b;
+  p2.out_scale_t = nullptr;
+  p2.flags = reinterpret_cast<int*>(wsb + P.flags2);
+  cudaError_t e;
+  if (fp8) {
+    if (hb16 && group == MOE_GROUP_TENSOR &&
+        cudaMemsetAsync(wsb + P.hb, 0, (size_t)S * I * 2, s) != cudaSuccess)  // uncounted rows: no amax
+      return MOE_ERR_CUDA;
+    e = hb16 ? launch_gemm1<true, 1, true>(activation, &m1, g1, grid, s) : launch_gemm1<true, 1>(activation, &m1, g1, grid, s);
+    if (e == cudaSuccess && hb16) {
+      const auto* hbp = reinterpret_cast<const __nv_bfloat16*>(wsb + P.hb);
+      uint8_t* hq = wsb + P.h;
+      if (group == MOE_GROUP_TOKEN) {
+        hquant_token_kernel<<<(unsigned)S, 256, 0, s>>>(hbp, I, offsets, E, hq, hs);
+      } else {
+        unsigned* amax = reinterpret_cast<unsigned*>(wsb + P.hamax);
+        e = cudaMemsetAsync(amax, 0, sizeof(unsigned), s);
+        const long long nvec = S * (I / 8);
+        const unsigned gb = (unsigned)((nvec + 255) / 256);
+        if (e == cudaSuccess) {
+          hquant_tensor_amax_kernel<<<std::min<unsigned>(gb, 4u * grid), 256, 0, s>>>(hbp, I, offsets, E, amax);
+          hquant_tensor_kernel<<<gb, 256, 0, s>>>(hbp, I, offsets, E, amax, hq, hs);
+        }
+      }
+      if (e == cudaSuccess) e = cudaGetLastError();
+    }
+    if (e == cudaSuccess) e = launch_gemm<true, kGemm2, 1, 0>(&m2, g2, grid, s);
+  } else {
+    e = launch_gemm1<false, 1>(activation, &m1, g1, grid, s);
+    if (e == cudaSuccess) e = launch_gemm<false, kGemm2, 1, 0>(&m2, g2, grid, s);
+  }
+  return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
 // ------------------------------------------------------------------ NVFP4 experts
 // Workspace of an NVFP4 call: gathered A rows and their scale rows, the bf16
 // intermediate, its NVFP4 codes and scales, the split flags of both GEMMs and one
@@ -2371,4 +2567,18 @@ extern "C" moe_status_t moe_selftest_wait_timeout(uint64_t limit_ns, moe_stream_
   MOE_CHECK_ARG(limit_ns >= 1000ull && limit_ns <= 10000000000ull);
   selftest_wait_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(limit_ns);
   return launch_status();
+}
+
+extern "C" size_t moe_workspace_size_batched(int E, int max_tokens, int H, int I, const moe_quant_config* qc) {
+  if (!qc || E < 1 || max_tokens < 1 || H <= 0 || I <= 0) return 0;
+  return batched_layout(E, max_tokens, H, I, qc, gemm_grid()).total;
+}
+
+extern "C" moe_status_t moe_experts_batched(const void* a1q_b, const float* a1q_b_scale, const void* w13,
+                                            const float* w13_scale, const void* w2, const float* w2_scale,
+                                            const int32_t* expert_num_tokens, int E, int max_tokens, int H, int I,
+                                            const moe_quant_config* qc, int activation, void* out_b, void* ws,
+                                            size_t ws_bytes, moe_stream_t stream) {
+  return experts_batched_run(a1q_b, a1q_b_scale, w13, w13_scale, w2, w2_scale, expert_num_tokens, E, max_tokens, H, I,
+                             qc, activation, out_b, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
 }

@@ -20,6 +20,8 @@ namespace moe {
 namespace {
 
 constexpr int kThreads = 128;
+// largest dynamic shared memory of the staged (bulk-copy) finalize: (k + 2) row slices
+constexpr int kMaxBulkSmem = 96 * 1024;
 enum OutKind { kOutBF16 = 0, kOutF32 = 1, kOutNVFP4 = 2 };
 
 __device__ __forceinline__ uint4 ldg_nc(const void* p) {
@@ -59,13 +61,44 @@ __device__ __forceinline__ float ld_dsmem_f32(const float* local, uint32_t rank)
   return v;
 }
 
+// Where the expert rows of the slots are: token-major rows y[t * top_k + j] (the standard
+// format), or, for the batched format, the row of slot f in an [E, max_tokens, H] output:
+// expert e = ids[f], rank inv_slot[f] - offsets[e] among that expert's slots.
+struct SlotRows {
+  const int32_t* ids;      // NULL: token-major rows
+  const int32_t* inv_slot;
+  const int32_t* offsets;
+  int max_tokens;
+  __device__ __forceinline__ size_t row(int t, int top_k, int j) const {
+    const int f = t * top_k + j;
+    if (!ids) return (size_t)f;
+    const int e = __ldg(ids + f);
+    return (size_t)e * max_tokens + (__ldg(inv_slot + f) - __ldg(offsets + e));
+  }
+};
+
+// Bulk asynchronous copy of `bytes` (a multiple of 16, both addresses 16-byte aligned) from
+// global memory into this CTA's shared memory, completing on `bar` (transaction bytes).
+__device__ __forceinline__ void bulk_g2s(void* smem_dst, const void* gmem_src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(smem_dst)),
+      "l"(gmem_src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
 // NV: 16-byte vectors per thread (upper bound); kC: CTAs per token (cluster size).
-template <int kC, int NV, int kOut>
+// kBulk: the k expert-row slices and the shared and residual slices of the token are staged
+// in shared memory by bulk asynchronous copies that one thread issues at once (one memory
+// round trip for all of them, no registers held by loads in flight; dynamic shared memory of
+// (k + 2) slices); otherwise every thread loads its vectors into registers.
+template <int kC, int NV, int kOut, bool kBulk>
 __global__ void __launch_bounds__(kThreads)
     finalize_kernel(void* __restrict__ output, const __nv_bfloat16* __restrict__ y, const float* __restrict__ topk_w,
                     const __nv_bfloat16* __restrict__ shared, const __nv_bfloat16* __restrict__ residual,
                     const __nv_bfloat16* __restrict__ gamma, float eps, int H, int top_k, int weights_on_input,
-                    uint8_t* __restrict__ out_scale, float gscale, __nv_bfloat16* __restrict__ residual_out) {
+                    uint8_t* __restrict__ out_scale, float gscale, __nv_bfloat16* __restrict__ residual_out,
+                    const SlotRows rows) {
   __shared__ float red[kThreads / 32];
   __shared__ float cta_ss;
   const int t = blockIdx.x / kC;
@@ -74,22 +107,58 @@ __global__ void __launch_bounds__(kThreads)
   const int v0 = (int)rank * vslice;            // first vector of the slice within the row
   const size_t row = (size_t)t * H;
 
-  if (threadIdx.x == 0) {
-    // one CTA per token: its expert rows 1..k-1 (row 0 is loaded at once; measured: with
-    // clusters, whose slices are short, the extra requests cost more than they save)
-    if (kC == 1)
-      for (int j = 1; j < top_k; ++j)
-        prefetch_l2(y + ((size_t)t * top_k + j) * H, (uint32_t)H * 2);
-    // then the shared and residual slices
-    if (shared) prefetch_l2(shared + row + (size_t)v0 * 8, (uint32_t)vslice * 16);
-    if (residual) prefetch_l2(residual + row + (size_t)v0 * 8, (uint32_t)vslice * 16);
-  }
-
   float o[NV][8];
 #pragma unroll
   for (int u = 0; u < NV; ++u)
 #pragma unroll
     for (int i = 0; i < 8; ++i) o[u][i] = 0.f;
+
+  if constexpr (kBulk) {
+    extern __shared__ uint4 stage[];  // [top_k + 2][vslice]: expert rows, shared, residual
+    __shared__ uint64_t bar;
+    const uint32_t sbytes = (uint32_t)vslice * 16;
+    if (threadIdx.x == 0) {
+      mbar_init(&bar, 1);
+      fence_mbar_init();
+      const uint32_t nrows = top_k + (shared ? 1 : 0) + (residual ? 1 : 0);
+      mbar_arrive_expect_tx(&bar, nrows * sbytes);
+      for (int j = 0; j < top_k; ++j)
+        bulk_g2s(stage + (size_t)j * vslice, y + rows.row(t, top_k, j) * H + (size_t)v0 * 8, sbytes, &bar);
+      if (shared) bulk_g2s(stage + (size_t)top_k * vslice, shared + row + (size_t)v0 * 8, sbytes, &bar);
+      if (residual) bulk_g2s(stage + (size_t)(top_k + 1) * vslice, residual + row + (size_t)v0 * 8, sbytes, &bar);
+    }
+    __syncthreads();
+    if (!mbar_wait(&bar, 0, false)) {
+      // gave up (recorded): wait once more, bounded, for the copies still landing in this
+      // CTA's shared memory before it may exit
+      mbar_wait(&bar, 0, false, 100000000ull);
+    }
+    for (int j = 0; j < top_k; ++j) {
+      const float w = weights_on_input ? 1.0f : __ldg(topk_w + (size_t)t * top_k + j);
+#pragma unroll
+      for (int u = 0; u < NV; ++u) {
+        const int vi = threadIdx.x + u * kThreads;
+        if (vi < vslice) add_bf16x8(o[u], stage[(size_t)j * vslice + vi], w);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < NV; ++u) {
+      const int vi = threadIdx.x + u * kThreads;
+      if (vi >= vslice) continue;
+      if (shared) add_bf16x8(o[u], stage[(size_t)top_k * vslice + vi], 1.0f);
+      if (residual) add_bf16x8(o[u], stage[(size_t)(top_k + 1) * vslice + vi], 1.0f);
+    }
+  } else {
+  if (threadIdx.x == 0) {
+    // one CTA per token: its expert rows 1..k-1 (row 0 is loaded at once; measured: with
+    // clusters, whose slices are short, the extra requests cost more than they save)
+    if (kC == 1)
+      for (int j = 1; j < top_k; ++j)
+        prefetch_l2(y + rows.row(t, top_k, j) * H, (uint32_t)H * 2);
+    // then the shared and residual slices
+    if (shared) prefetch_l2(shared + row + (size_t)v0 * 8, (uint32_t)vslice * 16);
+    if (residual) prefetch_l2(residual + row + (size_t)v0 * 8, (uint32_t)vslice * 16);
+  }
 
   // Short slices (a few vectors per thread, the cluster launches of small T): every row's
   // loads are issued before the first add, so the k + 2 rows cost one memory round trip
@@ -102,7 +171,7 @@ __global__ void __launch_bounds__(kThreads)
     for (int j = 0; j < kMaxBatchK; ++j) {
       if (j < top_k) {
         wj[j] = weights_on_input ? 1.0f : __ldg(topk_w + (size_t)t * top_k + j);
-        const __nv_bfloat16* yr = y + ((size_t)t * top_k + j) * H + (size_t)v0 * 8;
+        const __nv_bfloat16* yr = y + rows.row(t, top_k, j) * H + (size_t)v0 * 8;
 #pragma unroll
         for (int u = 0; u < NV; ++u) {
           const int vi = threadIdx.x + u * kThreads;
@@ -131,7 +200,7 @@ __global__ void __launch_bounds__(kThreads)
   } else {
     for (int j = 0; j < top_k; ++j) {
       const float w = weights_on_input ? 1.0f : __ldg(topk_w + (size_t)t * top_k + j);
-      const __nv_bfloat16* yr = y + ((size_t)t * top_k + j) * H + (size_t)v0 * 8;
+      const __nv_bfloat16* yr = y + rows.row(t, top_k, j) * H + (size_t)v0 * 8;
       uint4 v[NV];
 #pragma unroll
       for (int u = 0; u < NV; ++u) {
@@ -157,6 +226,7 @@ __global__ void __launch_bounds__(kThreads)
       }
     }
   }
+  }  // register loads
   if (residual_out) {
 #pragma unroll
     for (int u = 0; u < NV; ++u) {
@@ -261,14 +331,26 @@ __global__ void __launch_bounds__(kThreads)
   }
 }
 
-template <int kC, int NV, int kOut>
+template <int kC, int NV, int kOut, bool kBulk>
 cudaError_t launch_finalize(cudaStream_t s, int T, void* output, const void* y, const float* w, const void* shared,
                             const void* residual, const void* gamma, float eps, int H, int top_k, int won,
-                            uint8_t* out_scale, float gscale, void* residual_out) {
+                            uint8_t* out_scale, float gscale, void* residual_out, const SlotRows& rows) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)T * kC);
   cfg.blockDim = dim3(kThreads);
   cfg.stream = s;
+  if (kBulk) {
+    cfg.dynamicSmemBytes = (size_t)(top_k + 2) * (H / kC) * 2;
+    static bool configured[64] = {false};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 64 && !configured[dev]) {
+      const cudaError_t e = cudaFuncSetAttribute(finalize_kernel<kC, NV, kOut, kBulk>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxBulkSmem);
+      if (e != cudaSuccess) return e;
+      configured[dev] = true;
+    }
+  }
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = kC;
@@ -276,20 +358,23 @@ cudaError_t launch_finalize(cudaStream_t s, int T, void* output, const void* y, 
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, finalize_kernel<kC, NV, kOut>, output,
+  return cudaLaunchKernelEx(&cfg, finalize_kernel<kC, NV, kOut, kBulk>, output,
                             static_cast<const __nv_bfloat16*>(y), w, static_cast<const __nv_bfloat16*>(shared),
                             static_cast<const __nv_bfloat16*>(residual), static_cast<const __nv_bfloat16*>(gamma),
-                            eps, H, top_k, won, out_scale, gscale, static_cast<__nv_bfloat16*>(residual_out));
+                            eps, H, top_k, won, out_scale, gscale, static_cast<__nv_bfloat16*>(residual_out), rows);
 }
 
 template <int kOut>
-cudaError_t dispatch_finalize(int C, int nv, cudaStream_t s, int T, void* output, const void* y, const float* w,
+cudaError_t dispatch_finalize(int C, int nv, bool bulk, cudaStream_t s, int T, void* output, const void* y, const float* w,
                               const void* shared, const void* residual, const void* gamma, float eps, int H,
-                              int top_k, int won, uint8_t* out_scale, float gscale, void* residual_out) {
-#define MOE_FIN(CC, NVV)                                                                                       \
-  if (C == CC && nv <= NVV)                                                                                    \
-    return launch_finalize<CC, NVV, kOut>(s, T, output, y, w, shared, residual, gamma, eps, H, top_k, won, \
-                                          out_scale, gscale, residual_out);
+                              int top_k, int won, uint8_t* out_scale, float gscale, void* residual_out,
+                              const SlotRows& rows) {
+#define MOE_FIN(CC, NVV)                                                                                         \
+  if (C == CC && nv <= NVV)                                                                                      \
+    return bulk ? launch_finalize<CC, NVV, kOut, true>(s, T, output, y, w, shared, residual, gamma, eps, H, top_k, \
+                                                       won, out_scale, gscale, residual_out, rows)               \
+                : launch_finalize<CC, NVV, kOut, false>(s, T, output, y, w, shared, residual, gamma, eps, H, top_k, \
+                                                        won, out_scale, gscale, residual_out, rows);
   MOE_FIN(1, 2) MOE_FIN(1, 4) MOE_FIN(1, 8)
   MOE_FIN(2, 2) MOE_FIN(2, 4) MOE_FIN(2, 8)
   MOE_FIN(4, 2) MOE_FIN(4, 4) MOE_FIN(4, 8)
@@ -298,16 +383,18 @@ cudaError_t dispatch_finalize(int C, int nv, cudaStream_t s, int T, void* output
 }
 
 }  // namespace
+
+MOE_DEFINE_STATUS_READER(finalize_status)
+
 }  // namespace moe
 
 using namespace moe;
 
-extern "C" moe_status_t moe_finalize(void* output, const void* fused_expert_output, const float* topk_weights,
-                                     const int32_t* topk_ids, const void* shared, const void* residual,
-                                     const void* rms_weight, float eps, int T, int H, int top_k,
-                                     int apply_router_weight_on_input, moe_dtype_t out_dtype, uint8_t* out_scale,
-                                     float out_global_scale, void* residual_out, moe_stream_t stream) {
-  (void)topk_ids;
+namespace {
+moe_status_t finalize_run(void* output, const void* fused_expert_output, const float* topk_weights, const void* shared,
+                          const void* residual, const void* rms_weight, float eps, int T, int H, int top_k,
+                          int apply_router_weight_on_input, moe_dtype_t out_dtype, uint8_t* out_scale,
+                          float out_global_scale, void* residual_out, const SlotRows& rows, moe_stream_t stream) {
   MOE_CHECK_ARG(T >= 0 && H > 0 && H % 8 == 0 && top_k >= 1 && top_k <= 32);
   MOE_CHECK_ARG(out_dtype == MOE_DT_BF16 || out_dtype == MOE_DT_FP32 || out_dtype == MOE_DT_NVFP4);
   MOE_CHECK_ARG(out_dtype != MOE_DT_NVFP4 || (H % 16 == 0 && out_global_scale > 0.f));
@@ -331,19 +418,47 @@ extern "C" moe_status_t moe_finalize(void* output, const void* fused_expert_outp
   if (!slice_ok(C)) return MOE_ERR_UNSUPPORTED;
   while (C < 4 && (long long)T * C < 4LL * nsm && slice_ok(2 * C) && (H / 8) / (2 * C) >= kThreads) C *= 2;
   const int per_cta = (H / 8) / C;
+  // staged rows when the k + 2 slices of a CTA fit the shared-memory budget
+  const bool bulk = (size_t)(top_k + 2) * per_cta * 16 <= (size_t)kMaxBulkSmem;
   const int nv = (per_cta + kThreads - 1) / kThreads;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const int won = apply_router_weight_on_input ? 1 : 0;
   cudaError_t err;
   if (out_dtype == MOE_DT_BF16)
-    err = dispatch_finalize<kOutBF16>(C, nv, s, T, output, fused_expert_output, topk_weights, shared, residual,
-                                      rms_weight, eps, H, top_k, won, out_scale, out_global_scale, residual_out);
+    err = dispatch_finalize<kOutBF16>(C, nv, bulk, s, T, output, fused_expert_output, topk_weights, shared, residual,
+                                      rms_weight, eps, H, top_k, won, out_scale, out_global_scale, residual_out, rows);
   else if (out_dtype == MOE_DT_FP32)
-    err = dispatch_finalize<kOutF32>(C, nv, s, T, output, fused_expert_output, topk_weights, shared, residual,
-                                     rms_weight, eps, H, top_k, won, out_scale, out_global_scale, residual_out);
+    err = dispatch_finalize<kOutF32>(C, nv, bulk, s, T, output, fused_expert_output, topk_weights, shared, residual,
+                                     rms_weight, eps, H, top_k, won, out_scale, out_global_scale, residual_out, rows);
   else
-    err = dispatch_finalize<kOutNVFP4>(C, nv, s, T, output, fused_expert_output, topk_weights, shared, residual,
-                                       rms_weight, eps, H, top_k, won, out_scale, out_global_scale, residual_out);
+    err = dispatch_finalize<kOutNVFP4>(C, nv, bulk, s, T, output, fused_expert_output, topk_weights, shared, residual,
+                                       rms_weight, eps, H, top_k, won, out_scale, out_global_scale, residual_out, rows);
   if (err != cudaSuccess) return MOE_ERR_CUDA;
   return launch_status();
+}
+}  // namespace
+
+extern "C" moe_status_t moe_finalize(void* output, const void* fused_expert_output, const float* topk_weights,
+                                     const int32_t* topk_ids, const void* shared, const void* residual,
+                                     const void* rms_weight, float eps, int T, int H, int top_k,
+                                     int apply_router_weight_on_input, moe_dtype_t out_dtype, uint8_t* out_scale,
+                                     float out_global_scale, void* residual_out, moe_stream_t stream) {
+  (void)topk_ids;
+  const SlotRows rows{nullptr, nullptr, nullptr, 0};
+  return finalize_run(output, fused_expert_output, topk_weights, shared, residual, rms_weight, eps, T, H, top_k,
+                      apply_router_weight_on_input, out_dtype, out_scale, out_global_scale, residual_out, rows, stream);
+}
+
+extern "C" moe_status_t moe_finalize_batched(void* output, const void* expert_output_b, int max_tokens,
+                                             const float* topk_weights, const int32_t* topk_ids,
+                                             const int32_t* inv_slot, const int32_t* expert_offsets, const void* shared,
+                                             const void* residual, const void* rms_weight, float eps, int T, int H,
+                                             int top_k, int apply_router_weight_on_input, moe_dtype_t out_dtype,
+                                             uint8_t* out_scale, float out_global_scale, void* residual_out,
+                                             moe_stream_t stream) {
+  MOE_CHECK_ARG(max_tokens >= 1);
+  if (T > 0) MOE_CHECK_ARG(topk_ids && inv_slot && expert_offsets);
+  const SlotRows rows{topk_ids, inv_slot, expert_offsets, max_tokens};
+  return finalize_run(output, expert_output_b, topk_weights, shared, residual, rms_weight, eps, T, H, top_k,
+                      apply_router_weight_on_input, out_dtype, out_scale, out_global_scale, residual_out, rows, stream);
 }

@@ -208,3 +208,119 @@ extern "C" moe_status_t moe_prepare(const void* a1, const float* topk_weights, c
   }
   return launch_status();
 }
+
+// ------------------------------------------------------------------ batched activation format
+// The batched prepare ("Fused MoE Kernel Features", section "Fused MoE Modular All2All
+// backends": the prepare output is "standard" or "batched"): the standard prepare of every
+// token into the workspace, then one warp per sorted row p places the prepared row of its
+// token in the slab of its expert, at rank p - expert_offsets[e] (the expert's slots in
+// ascending order, as moe_align sorts them).  A row whose rank reaches max_tokens is left
+// out and MOE_ERR_INVALID_ARG is recorded in the status word.
+namespace moe {
+namespace {
+
+// Expert of sorted row p: the last e with offsets[e] <= p (offsets ascending, offsets[E] = S).
+__device__ __forceinline__ int expert_of_row(const int32_t* __restrict__ offsets, int E, int p) {
+  int lo = 0, hi = E - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(offsets + mid) <= p)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  return lo;
+}
+
+// row_bytes: bytes of one prepared row; nscale: fp32 scales per row (G(128): H/128, "A": 1,
+// bf16 and "T": 0 -- the tensor scale is copied once).
+__global__ void __launch_bounds__(256)
+    dispatch_batched_kernel(const uint8_t* __restrict__ a1q, const float* __restrict__ a1q_scale,
+                            const int32_t* __restrict__ offsets, const int32_t* __restrict__ sorted_slot, int S,
+                            int top_k, int E, int max_tokens, int row_bytes, int nscale, int tensor_scale,
+                            uint8_t* __restrict__ a1q_b, float* __restrict__ a1q_b_scale,
+                            int32_t* __restrict__ expert_num_tokens) {
+  const int gtid = blockIdx.x * 256 + threadIdx.x;
+  if (gtid < E) expert_num_tokens[gtid] = min(__ldg(offsets + gtid + 1) - __ldg(offsets + gtid), max_tokens);
+  if (gtid == 0 && tensor_scale) a1q_b_scale[0] = __ldg(a1q_scale);
+  const int p = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (p >= S) return;
+  const int e = expert_of_row(offsets, E, p);
+  const int m = p - __ldg(offsets + e);
+  if (m >= max_tokens) {
+    if (lane == 0) record_status((int)MOE_ERR_INVALID_ARG);
+    return;
+  }
+  const int t = __ldg(sorted_slot + p) / top_k;
+  const size_t dst_row = (size_t)e * max_tokens + m;
+  const uint4* src = reinterpret_cast<const uint4*>(a1q + (size_t)t * row_bytes);
+  uint4* dst = reinterpret_cast<uint4*>(a1q_b + dst_row * row_bytes);
+  for (int i = lane; i < row_bytes / 16; i += 32) dst[i] = __ldg(src + i);
+  for (int g = lane; g < nscale; g += 32) a1q_b_scale[dst_row * nscale + g] = __ldg(a1q_scale + (size_t)t * nscale + g);
+}
+
+size_t batched_prepare_ws(int T, int H, const moe_quant_config* qc, size_t* scale_off) {
+  const bool fp8 = qc->act == MOE_DT_FP8_E4M3;
+  const size_t codes = (((size_t)T * H * (fp8 ? 1 : 2)) + 255) & ~size_t(255);
+  size_t scales = 0;
+  if (fp8) scales = qc->act_group == 128 ? (size_t)T * (H / 128) * 4 : (qc->act_group == MOE_GROUP_TOKEN ? (size_t)T * 4 : 16);
+  *scale_off = codes;
+  return codes + ((scales + 255) & ~size_t(255));
+}
+
+}  // namespace
+
+MOE_DEFINE_STATUS_READER(prepare_status)
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" size_t moe_prepare_batched_workspace_size(int T, int H, const moe_quant_config* qc) {
+  if (!qc || T < 0 || H <= 0) return 0;
+  size_t so = 0;
+  return std::max<size_t>(batched_prepare_ws(T, H, qc, &so), 256);
+}
+
+extern "C" moe_status_t moe_prepare_batched(const void* a1, const float* topk_weights, const int32_t* expert_offsets,
+                                            const int32_t* sorted_slot, int T, int H, int top_k, int E,
+                                            int max_tokens, int apply_router_weight_on_input,
+                                            const moe_quant_config* qc, void* a1q_b, float* a1q_b_scale,
+                                            int32_t* expert_num_tokens, void* ws, size_t ws_bytes,
+                                            moe_stream_t stream) {
+  MOE_CHECK_ARG(qc && T >= 0 && H > 0 && top_k >= 1 && E >= 1 && E <= 1024 && top_k <= E && max_tokens >= 1);
+  const bool fp8 = qc->act == MOE_DT_FP8_E4M3;
+  MOE_CHECK_ARG(fits_int32((long long)T * top_k) && fits_int32((long long)E * max_tokens) &&
+                fits_int32((long long)E * max_tokens * (H / 8)));
+  MOE_CHECK_ARG(expert_num_tokens && a1q_b && aligned16(a1q_b) && (!fp8 || a1q_b_scale));
+  size_t scale_off = 0;
+  size_t need = batched_prepare_ws(T, H, qc, &scale_off);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (T == 0) {  // every expert empty
+    return cudaMemsetAsync(expert_num_tokens, 0, (size_t)E * 4, s) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  }
+  MOE_CHECK_ARG(expert_offsets && sorted_slot);
+  if (!fp8 && !apply_router_weight_on_input) need = 0;
+  if (need && (!ws || ws_bytes < need)) return MOE_ERR_WORKSPACE;
+  MOE_CHECK_ARG(!need || aligned16(ws));
+  uint8_t* wsb = static_cast<uint8_t*>(ws);
+  float* sc = fp8 ? reinterpret_cast<float*>(wsb + scale_off) : nullptr;
+  // (bf16 without the weight on the input: the rows are a1 itself, placed straight from it)
+  const bool direct = !fp8 && !apply_router_weight_on_input;
+  MOE_CHECK_ARG(a1 && aligned16(a1));
+  if (!direct) {
+    const moe_status_t st = moe_prepare(a1, topk_weights, nullptr, T, H, top_k, apply_router_weight_on_input, qc,
+                                        wsb, sc, stream);
+    if (st != MOE_OK) return st;
+  }
+  const uint8_t* rows = direct ? static_cast<const uint8_t*>(a1) : wsb;
+  const int S = T * top_k;
+  const int nscale = !fp8 ? 0 : (qc->act_group == 128 ? H / 128 : (qc->act_group == MOE_GROUP_TOKEN ? 1 : 0));
+  const int tensor = fp8 && qc->act_group == MOE_GROUP_TENSOR;
+  const unsigned grid = (unsigned)std::max<long long>((S + 7) / 8, (E + 255) / 256);
+  dispatch_batched_kernel<<<grid, 256, 0, s>>>(rows, sc, expert_offsets, sorted_slot, S, top_k, E, max_tokens,
+                                               H * (fp8 ? 1 : 2), nscale, tensor, static_cast<uint8_t*>(a1q_b),
+                                               a1q_b_scale, expert_num_tokens);
+  return launch_status();
+}

@@ -89,6 +89,11 @@ SIGNATURES = {
     "moe_layer_fused": ([_P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _F, _P, _P, _P, _P, _Z, _P], _I),
     "moe_layer_fused_workspace_size": ([_I, _I, _I, _I, _I, _I], _Z),
     "moe_finalize": ([_P, _P, _P, _P, _P, _P, _P, _F, _I, _I, _I, _I, _I, _P, _F, _P, _P], _I),
+    "moe_prepare_batched_workspace_size": ([_I, _I, _QCP], _Z),
+    "moe_prepare_batched": ([_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _QCP, _P, _P, _P, _P, _Z, _P], _I),
+    "moe_workspace_size_batched": ([_I, _I, _I, _I, _QCP], _Z),
+    "moe_experts_batched": ([_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _QCP, _I, _P, _P, _Z, _P], _I),
+    "moe_finalize_batched": ([_P, _P, _I, _P, _P, _P, _P, _P, _P, _P, _F, _I, _I, _I, _I, _I, _P, _F, _P, _P], _I),
     "moe_device_status": ([_I], _I),
     "moe_selftest_wait_timeout": ([ctypes.c_uint64, _P], _I),
     "moe_status_string": ([_I], ctypes.c_char_p),
@@ -485,3 +490,73 @@ def moe_selftest_wait_timeout(limit_ns: int, stream=None) -> None:
     """Launch the library's self-test of a device-side wait that runs out (see moe.h):
     afterwards moe_device_status() reports MOE_ERR_TIMEOUT."""
     _check("moe_selftest_wait_timeout", lib().moe_selftest_wait_timeout(int(limit_ns), _stream(stream)))
+
+
+# ------------------------------------------------------------------ batched activation format
+def batched_scale_shape(quant: str, E: int, M: int, H: int):
+    """Shape of a1q_b_scale in the batched format (None for bf16)."""
+    return {"bf16": None, "fp8": (E, M, H // 128), "fp8_token": (E, M), "fp8_tensor": (1,)}[quant]
+
+
+def moe_prepare_batched(a1: torch.Tensor, topk_weights: Optional[torch.Tensor], al: "Alignment", E: int,
+                        max_tokens: int, apply_router_weight_on_input: bool, quant: str, stream=None):
+    """Prepare into the batched format (``moe_prepare_batched``): returns (a1q_b
+    [E, max_tokens, H], a1q_b_scale or None, expert_num_tokens [E] int32)."""
+    _need(a1, torch.bfloat16, "a1")
+    T, H = a1.shape
+    fp8 = quant != "bf16"
+    qb = torch.empty((E, max_tokens, H), dtype=torch.uint8 if fp8 else torch.bfloat16, device=a1.device)
+    shp = batched_scale_shape(quant, E, max_tokens, H)
+    sb = None if shp is None else torch.empty(shp, dtype=torch.float32, device=a1.device)
+    counts = torch.empty((E,), dtype=torch.int32, device=a1.device)
+    qc = _qc(quant)
+    nws = int(lib().moe_prepare_batched_workspace_size(T, H, ctypes.byref(qc)))
+    ws = torch.empty(max(nws, 16), dtype=torch.uint8, device=a1.device)
+    _check("moe_prepare_batched", lib().moe_prepare_batched(
+        _ptr(a1), _ptr(topk_weights), _ptr(al.expert_offsets), _ptr(al.sorted_slot), T, H, al.top_k, E, max_tokens,
+        int(apply_router_weight_on_input), ctypes.byref(qc), _ptr(qb), _ptr(sb), _ptr(counts), _ptr(ws), ws.numel(),
+        _stream(stream)))
+    return qb, sb, counts
+
+
+def workspace_size_batched(E: int, max_tokens: int, H: int, I: int, quant: str) -> int:
+    return int(lib().moe_workspace_size_batched(E, max_tokens, H, I, ctypes.byref(_qc(quant))))
+
+
+def moe_experts_batched(a1q_b: torch.Tensor, a1q_b_scale: Optional[torch.Tensor], w13: torch.Tensor,
+                        w13_scale: Optional[torch.Tensor], w2: torch.Tensor, w2_scale: Optional[torch.Tensor],
+                        expert_num_tokens: torch.Tensor, quant: str, out: Optional[torch.Tensor] = None,
+                        ws: Optional[torch.Tensor] = None, activation: str = "silu", stream=None) -> torch.Tensor:
+    """The experts on the batched format (``moe_experts_batched``): out [E, max_tokens, H] bf16."""
+    if activation not in ACTIVATIONS:
+        raise ValueError(f"unknown activation {activation!r}")
+    E, M, H = a1q_b.shape
+    _, rows13, _ = w13.shape
+    I = rows13 if activation.endswith("_no_mul") else rows13 // 2
+    _need(expert_num_tokens, torch.int32, "expert_num_tokens")
+    if out is None:
+        out = torch.empty((E, M, H), dtype=torch.bfloat16, device=a1q_b.device)
+    if ws is None:
+        ws = torch.empty(max(workspace_size_batched(E, M, H, I, quant), 16), dtype=torch.uint8, device=a1q_b.device)
+    _check("moe_experts_batched", lib().moe_experts_batched(
+        _ptr(a1q_b), _ptr(a1q_b_scale), _ptr(w13), _ptr(w13_scale), _ptr(w2), _ptr(w2_scale), _ptr(expert_num_tokens),
+        E, M, H, I, ctypes.byref(_qc(quant)), ACTIVATIONS[activation], _ptr(out), _ptr(ws), ws.numel(),
+        _stream(stream)))
+    return out
+
+
+def moe_finalize_batched(out_b: torch.Tensor, topk_weights: Optional[torch.Tensor], topk_ids: torch.Tensor,
+                         al: "Alignment", apply_router_weight_on_input: bool, shared=None, residual=None,
+                         rms_weight=None, eps: float = 1e-6, output: Optional[torch.Tensor] = None,
+                         residual_out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """moe_finalize reading each slot's row from a batched output [E, max_tokens, H]
+    (``moe_finalize_batched``); bf16 output [T, H]."""
+    E, M, H = out_b.shape
+    T, k = topk_ids.shape
+    if output is None:
+        output = torch.empty((T, H), dtype=torch.bfloat16, device=out_b.device)
+    _check("moe_finalize_batched", lib().moe_finalize_batched(
+        _ptr(output), _ptr(out_b), M, _ptr(topk_weights), _ptr(topk_ids), _ptr(al.inv_slot), _ptr(al.expert_offsets),
+        _ptr(shared), _ptr(residual), _ptr(rms_weight), eps, T, H, k, int(apply_router_weight_on_input), MOE_DT_BF16,
+        None, 1.0, _ptr(residual_out), _stream(stream)))
+    return output

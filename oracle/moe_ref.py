@@ -27,6 +27,9 @@ finalize, run on one device without dispatch or combine:
   optionally adds the shared-expert row, then (after the all-reduce, absent on
   one GPU) adds the residual, applies RMSNorm and optionally packs NVFP4.
 
+* "Fused MoE Kernel Features", section "Fused MoE Modular All2All backends": the
+  prepare output comes in a "standard" or a "batched" format (the batched
+  functions at the end of this file state the layout read for it).
 * "Fused MoE Kernel Features", experts table: besides bf16 and fp8 (formats
   G(128), A, T), nvfp4 is a quantisation type of the experts; the NVFP4 experts
   below take every operand in the finalize page's NVFP4 encoding.
@@ -574,3 +577,118 @@ def experts_nvfp4(a1q, a1q_sf, a1_gscale: float, w13, w13_sf, w13_gscale, w2, w2
         y[torch.from_numpy(slots.astype(np.int64))] = _expert_out(nvfp4_dequantize(hq, hsf, h_gscale),
                                                                   torch.from_numpy(W2))
     return (y, h_all) if return_h else y
+
+
+# =========================================================================== batched activation format
+# "Fused MoE Kernel Features" (vLLM design doc), section "Fused MoE Modular All2All
+# backends": the prepare step outputs its activations in one of two formats, "standard"
+# or "batched"; every prepare takes standard activations in and every finalize gives
+# standard activations back, so a finalize takes the format its prepare produced.  The
+# "Fused Experts Kernels" table lists batched entry points beside the standard ones
+# (batched triton, batched deep gemm, cutlass batched fp8, naive batched).  The pages
+# leave the layout itself to another document.  Reading taken here: the batched
+# activations are one slab per expert, [E, max_tokens, H]; expert e's slab holds, in
+# ascending slot order f = t*k + j, the prepared rows of the tokens that chose e, and
+# expert_num_tokens[e] counts them; rows past the count hold nothing (zeros here).  The
+# experts compute every counted row of every slab into an output slab of the same layout
+# (unweighted bf16 rows); the finalize reads the row of slot f at (the expert of f, the
+# rank of f among that expert's slots) and reduces like the standard finalize.
+
+def batched_positions(topk_ids, num_experts: int):
+    """The place of every slot in the batched layout: (expert of f, rank of f among the
+    slots of that expert, counting in ascending f), and the per-expert counts."""
+    ids = _np(topk_ids).reshape(-1).astype(np.int64)
+    counts = np.zeros(num_experts, dtype=np.int64)
+    rank = np.empty(len(ids), dtype=np.int64)
+    for f in range(len(ids)):
+        e = ids[f]
+        rank[f] = counts[e]
+        counts[e] += 1
+    return ids, rank, counts
+
+
+def prepare_batched(a1, topk_ids, topk_weights, apply_router_weight_on_input: bool, quant: str,
+                    num_experts: int, max_tokens: int):
+    """Prepare into the batched format: the standard prepare of every token (``prepare``),
+    then token t's prepared row placed at (expert, rank) of each of its slots.  Returns
+    (a1q_b [E, max_tokens, H] of the prepared type, scales in the same per-row layout --
+    G(128): [E, max_tokens, H/128], "A": [E, max_tokens], "T": the tensor's [1]; None for
+    bf16 -- and expert_num_tokens [E] int32).  A count above max_tokens is an error."""
+    a1q, sc = prepare(a1, topk_weights, apply_router_weight_on_input, quant)
+    ids, rank, counts = batched_positions(topk_ids, num_experts)
+    if len(counts) and counts.max() > max_tokens:
+        raise ValueError(f"an expert receives {int(counts.max())} slots, more than max_tokens = {max_tokens}")
+    k = _np(topk_ids).shape[1]
+    H = a1q.shape[1]
+    q = torch.zeros((num_experts, max_tokens, H), dtype=a1q.dtype)
+    s = None
+    if quant == "fp8":
+        s = torch.zeros((num_experts, max_tokens, H // 128), dtype=torch.float32)
+    elif quant == "fp8_token":
+        s = torch.zeros((num_experts, max_tokens), dtype=torch.float32)
+    elif quant == "fp8_tensor":
+        s = sc.clone()
+    for f in range(len(ids)):
+        q[ids[f], rank[f]] = a1q[f // k]
+        if quant in ("fp8", "fp8_token"):
+            s[ids[f], rank[f]] = sc[f // k]
+    return q, s, torch.from_numpy(counts.astype(np.int32))
+
+
+def experts_batched(a1q_b, a1q_b_scale, expert_num_tokens, w13, w13_scale, w2, w2_scale, quant: str,
+                    act: str = "silu") -> torch.Tensor:
+    """The experts on the batched format: slab e's first expert_num_tokens[e] rows through
+    expert e (``expert_rows``: GEMM1, activation, the intermediate stored as in the
+    standard path, GEMM2), written at the same place of an [E, max_tokens, H] output
+    (fp64 holding bf16 values; uncounted rows zero).  "T": one intermediate scale over
+    the counted rows of every slab, as ``experts`` does over every expert's rows."""
+    E, M, H = a1q_b.shape
+    counts = _np(expert_num_tokens).astype(np.int64)
+    y = torch.zeros((E, M, H), dtype=F64)
+    sc = None if a1q_b_scale is None else _np(a1q_b_scale)
+
+    def rows_of(e):
+        n = int(counts[e])
+        if quant == "bf16":
+            return torch.from_numpy(_np(a1q_b[e])[:n])
+        if quant == "fp8_tensor":
+            return torch.from_numpy(dequant_fp8(_np(a1q_b[e])[:n].astype(np.uint8), sc, quant))
+        return torch.from_numpy(dequant_fp8(_np(a1q_b[e])[:n].astype(np.uint8), sc[e][:n], quant))
+
+    if quant == "fp8_tensor":
+        hs, used = [], []
+        for e in range(E):
+            if counts[e]:
+                x = rows_of(e) @ _weights64(w13, w13_scale, e, quant).T
+                h = silu_and_mul(x) if act == "silu" else activation(x, act)
+                hs.append(codecs.round_bf16(h.numpy()))
+                used.append(e)
+        if not hs:
+            return y
+        q, s = quantize_fp8_tensor(np.concatenate(hs, 0))
+        h_all = dequant_fp8(q, s, quant)
+        r = 0
+        for e, h in zip(used, hs):
+            n = h.shape[0]
+            y[e, :n] = _expert_out(h_all[r:r + n], _weights64(w2, w2_scale, e, quant))
+            r += n
+        return y
+    for e in range(E):
+        if counts[e]:
+            y[e, :int(counts[e])] = expert_rows(rows_of(e), _weights64(w13, w13_scale, e, quant),
+                                                _weights64(w2, w2_scale, e, quant), quant, act)
+    return y
+
+
+def unbatch(y_b, topk_ids) -> torch.Tensor:
+    """Token-major expert rows [T*k, H] from a batched output: row f is the output row at
+    (the expert of f, the rank of f) -- what the finalize reads for slot f."""
+    E = y_b.shape[0]
+    ids, rank, _ = batched_positions(topk_ids, E)
+    yb = y_b if isinstance(y_b, torch.Tensor) else torch.from_numpy(np.asarray(y_b))
+    return yb[torch.from_numpy(ids), torch.from_numpy(rank)].to(F64)
+
+
+def finalize_batched(y_b, topk_ids, topk_weights, top_k: int, apply_router_weight_on_input: bool, **kw) -> FinalizeOut:
+    """The finalize of the batched format: ``finalize`` of the rows ``unbatch`` reads."""
+    return finalize(unbatch(y_b, topk_ids), topk_weights, top_k, apply_router_weight_on_input, **kw)
