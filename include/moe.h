@@ -426,7 +426,9 @@ size_t moe_layer_fused_workspace_size(int T, int H, int I, int E, int top_k, int
  *                 sf = e4m3(amax / (6 g)), q = e2m1(x / (sf g)), g =
  *                 out_global_scale > 0.
  * fused_expert_output [T*top_k, H] bf16; topk_weights [T, top_k] fp32;
- * shared, residual, residual_out [T, H] bf16; rms_weight [H] bf16.  topk_ids
+ * shared, residual, residual_out [T, H] bf16; rms_weight [H] bf16.  residual_out
+ * may be residual itself (the sum is then written over the residual, in place);
+ * any other overlap between inputs and outputs is not allowed.  topk_ids
  * is accepted for parity with the pages' signature and unused (may be NULL).
  * H % 8 == 0 (H % 16 == 0 for NVFP4), 1 <= top_k <= 32. */
 moe_status_t moe_finalize(void *output, const void *fused_expert_output, const float *topk_weights,

@@ -14,14 +14,14 @@
 // flashinfer page, "Code analysis", new dispatch tables).
 #include <cuda_fp4.h>
 
+#include <algorithm>
+
 #include "moe_common.cuh"
 
 namespace moe {
 namespace {
 
 constexpr int kThreads = 128;
-// largest dynamic shared memory of the staged (bulk-copy) finalize: (k + 2) row slices
-constexpr int kMaxBulkSmem = 96 * 1024;
 enum OutKind { kOutBF16 = 0, kOutF32 = 1, kOutNVFP4 = 2 };
 
 __device__ __forceinline__ uint4 ldg_nc(const void* p) {
@@ -31,6 +31,10 @@ __device__ __forceinline__ uint4 ldg_nc(const void* p) {
                : "l"(p));
   return v;
 }
+
+// Coherent 16-byte load (ld.global.cg): the residual row when the call writes residual_out
+// over it (in place), which the read-only path may not be used for.
+__device__ __forceinline__ uint4 ldg_cg(const void* p) { return __ldcg(reinterpret_cast<const uint4*>(p)); }
 
 __device__ __forceinline__ void add_bf16x8(float (&o)[8], uint4 v, float w) {
   const uint32_t u[4] = {v.x, v.y, v.z, v.w};
@@ -77,28 +81,17 @@ struct SlotRows {
   }
 };
 
-// Bulk asynchronous copy of `bytes` (a multiple of 16, both addresses 16-byte aligned) from
-// global memory into this CTA's shared memory, completing on `bar` (transaction bytes).
-__device__ __forceinline__ void bulk_g2s(void* smem_dst, const void* gmem_src, uint32_t bytes, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          smem_u32(smem_dst)),
-      "l"(gmem_src), "r"(bytes), "r"(smem_u32(bar))
-      : "memory");
-}
-
 // NV: 16-byte vectors per thread (upper bound); kC: CTAs per token (cluster size).
-// kBulk: the k expert-row slices and the shared and residual slices of the token are staged
-// in shared memory by bulk asynchronous copies that one thread issues at once (one memory
-// round trip for all of them, no registers held by loads in flight; dynamic shared memory of
-// (k + 2) slices); otherwise every thread loads its vectors into registers.
-template <int kC, int NV, int kOut, bool kBulk>
+template <int kC, int NV, int kOut>
 __global__ void __launch_bounds__(kThreads)
     finalize_kernel(void* __restrict__ output, const __nv_bfloat16* __restrict__ y, const float* __restrict__ topk_w,
-                    const __nv_bfloat16* __restrict__ shared, const __nv_bfloat16* __restrict__ residual,
+                    const __nv_bfloat16* __restrict__ shared, const __nv_bfloat16* residual,
                     const __nv_bfloat16* __restrict__ gamma, float eps, int H, int top_k, int weights_on_input,
-                    uint8_t* __restrict__ out_scale, float gscale, __nv_bfloat16* __restrict__ residual_out,
+                    uint8_t* __restrict__ out_scale, float gscale, __nv_bfloat16* residual_out,
                     const SlotRows rows) {
+  // residual_out may be residual itself (the in-place add + RMSNorm): each element is read
+  // by the thread that later writes it, through coherent loads in that case
+  const bool res_in_place = residual_out != nullptr && residual_out == residual;
   __shared__ float red[kThreads / 32];
   __shared__ float cta_ss;
   const int t = blockIdx.x / kC;
@@ -113,42 +106,6 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
     for (int i = 0; i < 8; ++i) o[u][i] = 0.f;
 
-  if constexpr (kBulk) {
-    extern __shared__ uint4 stage[];  // [top_k + 2][vslice]: expert rows, shared, residual
-    __shared__ uint64_t bar;
-    const uint32_t sbytes = (uint32_t)vslice * 16;
-    if (threadIdx.x == 0) {
-      mbar_init(&bar, 1);
-      fence_mbar_init();
-      const uint32_t nrows = top_k + (shared ? 1 : 0) + (residual ? 1 : 0);
-      mbar_arrive_expect_tx(&bar, nrows * sbytes);
-      for (int j = 0; j < top_k; ++j)
-        bulk_g2s(stage + (size_t)j * vslice, y + rows.row(t, top_k, j) * H + (size_t)v0 * 8, sbytes, &bar);
-      if (shared) bulk_g2s(stage + (size_t)top_k * vslice, shared + row + (size_t)v0 * 8, sbytes, &bar);
-      if (residual) bulk_g2s(stage + (size_t)(top_k + 1) * vslice, residual + row + (size_t)v0 * 8, sbytes, &bar);
-    }
-    __syncthreads();
-    if (!mbar_wait(&bar, 0, false)) {
-      // gave up (recorded): wait once more, bounded, for the copies still landing in this
-      // CTA's shared memory before it may exit
-      mbar_wait(&bar, 0, false, 100000000ull);
-    }
-    for (int j = 0; j < top_k; ++j) {
-      const float w = weights_on_input ? 1.0f : __ldg(topk_w + (size_t)t * top_k + j);
-#pragma unroll
-      for (int u = 0; u < NV; ++u) {
-        const int vi = threadIdx.x + u * kThreads;
-        if (vi < vslice) add_bf16x8(o[u], stage[(size_t)j * vslice + vi], w);
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < NV; ++u) {
-      const int vi = threadIdx.x + u * kThreads;
-      if (vi >= vslice) continue;
-      if (shared) add_bf16x8(o[u], stage[(size_t)top_k * vslice + vi], 1.0f);
-      if (residual) add_bf16x8(o[u], stage[(size_t)(top_k + 1) * vslice + vi], 1.0f);
-    }
-  } else {
   if (threadIdx.x == 0) {
     // one CTA per token: its expert rows 1..k-1 (row 0 is loaded at once; measured: with
     // clusters, whose slices are short, the extra requests cost more than they save)
@@ -183,7 +140,9 @@ __global__ void __launch_bounds__(kThreads)
     for (int u = 0; u < NV; ++u) {
       const int vi = threadIdx.x + u * kThreads;
       if (shared && vi < vslice) sv[u] = ldg_nc(shared + row + (size_t)(v0 + vi) * 8);
-      if (residual && vi < vslice) rv[u] = ldg_nc(residual + row + (size_t)(v0 + vi) * 8);
+      if (residual && vi < vslice)
+        rv[u] = res_in_place ? ldg_cg(residual + row + (size_t)(v0 + vi) * 8)
+                             : ldg_nc(residual + row + (size_t)(v0 + vi) * 8);
     }
 #pragma unroll
     for (int j = 0; j < kMaxBatchK; ++j)
@@ -222,11 +181,12 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
       for (int u = 0; u < NV; ++u) {
         const int vi = threadIdx.x + u * kThreads;
-        if (vi < vslice) add_bf16x8(o[u], ldg_nc(residual + row + (size_t)(v0 + vi) * 8), 1.0f);
+        if (vi < vslice)
+          add_bf16x8(o[u], res_in_place ? ldg_cg(residual + row + (size_t)(v0 + vi) * 8)
+                                        : ldg_nc(residual + row + (size_t)(v0 + vi) * 8), 1.0f);
       }
     }
   }
-  }  // register loads
   if (residual_out) {
 #pragma unroll
     for (int u = 0; u < NV; ++u) {
@@ -331,7 +291,7 @@ __global__ void __launch_bounds__(kThreads)
   }
 }
 
-template <int kC, int NV, int kOut, bool kBulk>
+template <int kC, int NV, int kOut>
 cudaError_t launch_finalize(cudaStream_t s, int T, void* output, const void* y, const float* w, const void* shared,
                             const void* residual, const void* gamma, float eps, int H, int top_k, int won,
                             uint8_t* out_scale, float gscale, void* residual_out, const SlotRows& rows) {
@@ -339,18 +299,6 @@ cudaError_t launch_finalize(cudaStream_t s, int T, void* output, const void* y, 
   cfg.gridDim = dim3((unsigned)T * kC);
   cfg.blockDim = dim3(kThreads);
   cfg.stream = s;
-  if (kBulk) {
-    cfg.dynamicSmemBytes = (size_t)(top_k + 2) * (H / kC) * 2;
-    static bool configured[64] = {false};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev < 64 && !configured[dev]) {
-      const cudaError_t e = cudaFuncSetAttribute(finalize_kernel<kC, NV, kOut, kBulk>,
-                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxBulkSmem);
-      if (e != cudaSuccess) return e;
-      configured[dev] = true;
-    }
-  }
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = kC;
@@ -358,23 +306,21 @@ cudaError_t launch_finalize(cudaStream_t s, int T, void* output, const void* y, 
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, finalize_kernel<kC, NV, kOut, kBulk>, output,
+  return cudaLaunchKernelEx(&cfg, finalize_kernel<kC, NV, kOut>, output,
                             static_cast<const __nv_bfloat16*>(y), w, static_cast<const __nv_bfloat16*>(shared),
                             static_cast<const __nv_bfloat16*>(residual), static_cast<const __nv_bfloat16*>(gamma),
                             eps, H, top_k, won, out_scale, gscale, static_cast<__nv_bfloat16*>(residual_out), rows);
 }
 
 template <int kOut>
-cudaError_t dispatch_finalize(int C, int nv, bool bulk, cudaStream_t s, int T, void* output, const void* y, const float* w,
+cudaError_t dispatch_finalize(int C, int nv, cudaStream_t s, int T, void* output, const void* y, const float* w,
                               const void* shared, const void* residual, const void* gamma, float eps, int H,
                               int top_k, int won, uint8_t* out_scale, float gscale, void* residual_out,
                               const SlotRows& rows) {
-#define MOE_FIN(CC, NVV)                                                                                         \
-  if (C == CC && nv <= NVV)                                                                                      \
-    return bulk ? launch_finalize<CC, NVV, kOut, true>(s, T, output, y, w, shared, residual, gamma, eps, H, top_k, \
-                                                       won, out_scale, gscale, residual_out, rows)               \
-                : launch_finalize<CC, NVV, kOut, false>(s, T, output, y, w, shared, residual, gamma, eps, H, top_k, \
-                                                        won, out_scale, gscale, residual_out, rows);
+#define MOE_FIN(CC, NVV)                                                                                       \
+  if (C == CC && nv <= NVV)                                                                                    \
+    return launch_finalize<CC, NVV, kOut>(s, T, output, y, w, shared, residual, gamma, eps, H, top_k, won, \
+                                          out_scale, gscale, residual_out, rows);
   MOE_FIN(1, 2) MOE_FIN(1, 4) MOE_FIN(1, 8)
   MOE_FIN(2, 2) MOE_FIN(2, 4) MOE_FIN(2, 8)
   MOE_FIN(4, 2) MOE_FIN(4, 4) MOE_FIN(4, 8)
@@ -410,6 +356,9 @@ moe_status_t finalize_run(void* output, const void* fused_expert_output, const f
   // CTAs per SM (measured: T=512 at H=7168 is 3% faster with 2-CTA clusters
   // than with one CTA per token).  With NVFP4 output the slices are whole
   // 16-element groups.
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const int won = apply_router_weight_on_input ? 1 : 0;
+  cudaError_t err;
   const int nsm = num_sms();
   const int grp = out_dtype == MOE_DT_NVFP4 ? 16 : 8;
   auto slice_ok = [&](int c) { return H % (grp * c) == 0 && (H / 8) / c <= 8 * kThreads; };
@@ -418,20 +367,15 @@ moe_status_t finalize_run(void* output, const void* fused_expert_output, const f
   if (!slice_ok(C)) return MOE_ERR_UNSUPPORTED;
   while (C < 4 && (long long)T * C < 4LL * nsm && slice_ok(2 * C) && (H / 8) / (2 * C) >= kThreads) C *= 2;
   const int per_cta = (H / 8) / C;
-  // staged rows when the k + 2 slices of a CTA fit the shared-memory budget
-  const bool bulk = (size_t)(top_k + 2) * per_cta * 16 <= (size_t)kMaxBulkSmem;
   const int nv = (per_cta + kThreads - 1) / kThreads;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  const int won = apply_router_weight_on_input ? 1 : 0;
-  cudaError_t err;
   if (out_dtype == MOE_DT_BF16)
-    err = dispatch_finalize<kOutBF16>(C, nv, bulk, s, T, output, fused_expert_output, topk_weights, shared, residual,
+    err = dispatch_finalize<kOutBF16>(C, nv, s, T, output, fused_expert_output, topk_weights, shared, residual,
                                       rms_weight, eps, H, top_k, won, out_scale, out_global_scale, residual_out, rows);
   else if (out_dtype == MOE_DT_FP32)
-    err = dispatch_finalize<kOutF32>(C, nv, bulk, s, T, output, fused_expert_output, topk_weights, shared, residual,
+    err = dispatch_finalize<kOutF32>(C, nv, s, T, output, fused_expert_output, topk_weights, shared, residual,
                                      rms_weight, eps, H, top_k, won, out_scale, out_global_scale, residual_out, rows);
   else
-    err = dispatch_finalize<kOutNVFP4>(C, nv, bulk, s, T, output, fused_expert_output, topk_weights, shared, residual,
+    err = dispatch_finalize<kOutNVFP4>(C, nv, s, T, output, fused_expert_output, topk_weights, shared, residual,
                                        rms_weight, eps, H, top_k, won, out_scale, out_global_scale, residual_out, rows);
   if (err != cudaSuccess) return MOE_ERR_CUDA;
   return launch_status();

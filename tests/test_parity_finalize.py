@@ -93,3 +93,27 @@ def test_finalize_empty(cuda_dev):
     y = torch.empty((0, 256), dtype=torch.bfloat16, device=cuda_dev)
     out, _ = moe.moe_finalize(y, torch.empty((0, 2), device=cuda_dev), 2)
     assert out.shape == (0, 256)
+
+
+@pytest.mark.parametrize("T,H,k", [(300, 4096, 2), (3, 7168, 4), (512, 7168, 4)])
+def test_finalize_residual_in_place(cuda_dev, T, H, k):
+    """residual_out written over residual (the in-place add + RMSNorm): the outputs are
+    those of the out-of-place call and the residual buffer ends up holding the sum."""
+    g = torch.Generator().manual_seed(T + H)
+    y = torch.randn((T * k, H), generator=g).to(torch.bfloat16)
+    w = torch.softmax(torch.randn((T, k), generator=g), 1)
+    sh = torch.randn((T, H), generator=g).to(torch.bfloat16)
+    res = torch.randn((T, H), generator=g).to(torch.bfloat16)
+    gm = (torch.rand(H, generator=g) + 0.5).to(torch.bfloat16)
+    d = lambda t: t.to(cuda_dev)
+    res_out = torch.empty((T, H), dtype=torch.bfloat16, device=cuda_dev)
+    out_sep, _ = moe.moe_finalize(d(y), d(w), k, False, shared=d(sh), residual=d(res), rms_weight=d(gm),
+                                  residual_out=res_out)
+    res_buf = d(res).clone()
+    out_inp, _ = moe.moe_finalize(d(y), d(w), k, False, shared=d(sh), residual=res_buf, rms_weight=d(gm),
+                                  residual_out=res_buf)
+    torch.cuda.synchronize()
+    assert torch.equal(out_inp, out_sep)
+    assert torch.equal(res_buf, res_out)
+    ref = moe_ref.finalize(y, w, k, False, shared=sh, residual=res, rms_weight=gm, eps=1e-6)
+    check_bf16(res_buf, ref.residual_out.double(), "residual in place")
