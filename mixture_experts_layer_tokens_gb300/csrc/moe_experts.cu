@@ -113,6 +113,10 @@ __device__ __forceinline__ void setmaxnreg_dec() {
 // many units as CTAs (decode-sized work); otherwise whole units are dealt
 // round-robin, where a short tail costs less than the split's fixed costs.
 constexpr int SPLIT_BELOW_UNITS_PER_CTA_X2 = 1;
+// Dynamic schedule (GemmParams::unit_ctr set): the producer warp takes each next unit
+// from a launch-wide counter and hands its index to the MMA and epilogue warps through
+// a ring of UNIT_SLOTS entries in shared memory.
+constexpr int UNIT_SLOTS = 4;
 
 enum Kind { kGemm1 = 0, kGemm2 = 1 };
 
@@ -169,6 +173,8 @@ struct GemmParams {
   int allow_split;             // decode-sized problem: few units may be split across CTAs (bf16 only)
   int* flags;                  // [units] arrivals on split units (zeroed by plan_kernel)
   float* partials;             // [gridDim.x][PARTIAL_FLOATS] one split-segment partial per CTA
+  int* unit_ctr;               // problem 0: launch-wide unit counter (zeroed before the launch) for the
+                               // dynamic schedule; NULL: the static schedule (Sched)
 };
 
 // Up to two expert problems in one launch (moe_experts_multi: typically a layer's
@@ -369,9 +375,17 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
   uint64_t* fixbar = drain + 1;      // stream-K: the later segments' partials of this CTA's split unit are in
   uint64_t* sfull = fixbar + 1;      // fp8 scale ring: [SCALE_SLOTS] slot filled
   uint64_t* sempty = sfull + C::SCALE_SLOTS;  // [SCALE_SLOTS] slot read by every epilogue warp
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sempty + C::SCALE_SLOTS);
+  uint64_t* ufull = sempty + C::SCALE_SLOTS;  // dynamic schedule: [UNIT_SLOTS] unit index written
+  uint64_t* uempty = ufull + UNIT_SLOTS;      // [UNIT_SLOTS] unit index read by the MMA and epilogue warps
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(uempty + UNIT_SLOTS);
+  volatile int* unit_ring = reinterpret_cast<volatile int*>(tmem_slot + 1);  // [UNIT_SLOTS]
   float* scale_ring = reinterpret_cast<float*>(ctrl + 4096);  // fp8: [SCALE_SLOTS][SCALE_SLOT_FLOATS]
-  float* amax_x = reinterpret_cast<float*>(ctrl + 256);  // [2 items][2 halves][BM]
+  float* amax_x = reinterpret_cast<float*>(ctrl + 512);  // [2 items][2 halves][BM]
+  // control block: barriers, TMEM address and unit ring below byte 512, the amax exchange up
+  // to 2560, the NVFP4 scale barriers from 3072, the fp8 scale ring from 4096
+  static_assert((2 * STAGES + 4 + 3 + 2 * C::SCALE_SLOTS + 2 * UNIT_SLOTS) * 8 + 4 + 4 * UNIT_SLOTS <= 512,
+                "control block overlaps the amax exchange");
+  static_assert(512 + 2 * 2 * BM * 4 <= 3072 && 3072 + STAGES * 8 <= 4096, "control block layout");
   uint64_t* sfready = reinterpret_cast<uint64_t*>(ctrl + 3072);  // NVFP4: [STAGES] stage's scales in TMEM
   // bf16 split units: the finished rows (own accumulator + later segments' partials),
   // [BM][FIX_STRIDE] fp32 over the stage buffers
@@ -397,6 +411,10 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
     for (int i = 0; i < C::SCALE_SLOTS; ++i) {
       mbar_init(&sfull[i], 32);  // one cp.async arrival per producer lane
       mbar_init(&sempty[i], EPI_WARPS);
+    }
+    for (int i = 0; i < UNIT_SLOTS; ++i) {
+      mbar_init(&ufull[i], 1);
+      mbar_init(&uempty[i], 1 + EPI_WARPS);
     }
     fence_mbar_init();
     prefetch_tensormap(&tmA);
@@ -431,6 +449,43 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
   // (split units have one M tile: the fix-up below sums one tile's rows)
   sched.init(units, KB, gridDim.x, blockIdx.x, kSplit && MG == 1 && p0.allow_split);
   int u, kb0, kb1;
+  // The dynamic schedule hands whole units to CTAs in the order they ask, so a CTA that
+  // starts late (its SM still held by another kernel) takes fewer of them instead of
+  // finishing late.  Units that share a weight tile are taken at about the same time by
+  // neighbouring askers, as in the static schedule.
+  // (units split across CTAs keep the static ranges: their fix-up needs to know which CTA
+  // holds which segment)
+  const bool dyn = p0.unit_ctr != nullptr && sched.rr;
+  long long useq = 0;  // units taken through the ring by this warp
+  auto next_unit_producer = [&]() -> bool {
+    if (!dyn) return sched.next(u, kb0, kb1);
+    const int slot = (int)(useq % UNIT_SLOTS);
+    if (!warp_wait(&uempty[slot], (uint32_t)(((useq / UNIT_SLOTS) & 1) ^ 1))) return false;
+    int v = 0;
+    if (lane == 0) {
+      v = atomicAdd(p0.unit_ctr, 1);
+      if (v >= units) v = -1;  // no unit left: tells the other warps to stop
+      unit_ring[slot] = v;
+      mbar_arrive(&ufull[slot]);
+    }
+    u = __shfl_sync(0xffffffffu, v, 0);
+    ++useq;
+    kb0 = 0;
+    kb1 = KB;
+    return u >= 0;
+  };
+  auto next_unit_consumer = [&]() -> bool {
+    if (!dyn) return sched.next(u, kb0, kb1);
+    const int slot = (int)(useq % UNIT_SLOTS);
+    if (!warp_wait(&ufull[slot], (uint32_t)((useq / UNIT_SLOTS) & 1))) return false;
+    u = unit_ring[slot];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&uempty[slot]);
+    ++useq;
+    kb0 = 0;
+    kb1 = KB;
+    return u >= 0;
+  };
 
   if (warp < Warps<kFP8>::FIRST_EPI) {
   // fp8: this warpgroup (producer, MMA issuer, two idle warps) hands registers to the
@@ -444,7 +499,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
     uint32_t phase = 0;
     long long fills = 0;
     bool ok = true;
-    while (ok && sched.next(u, kb0, kb1)) {
+    while (ok && next_unit_producer()) {
       const int prob = u >= units0;
       const GemmParams& p = pp.p[prob];
       const CUtensorMap* mA = prob ? &tmA_1 : &tmA;
@@ -523,7 +578,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
     int acc = 0;
     uint32_t acc_phase = 0;
     bool ok = true;
-    while (ok && sched.next(u, kb0, kb1)) {
+    while (ok && next_unit_consumer()) {
       const int prob = u >= units0;
       const Unit it = decode<MG, kCoh>(pp.p[prob], u - (prob ? units0 : 0));
       const int mcnt = (it.row_end - it.row0 + BM - 1) / BM;
@@ -596,7 +651,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
     int fstage = 0;       // NVFP4: stages whose scales this warp has put in TMEM
     uint32_t fphase = 0;
     bool ok = true;
-    while (ok && sched.next(u, kb0, kb1)) {
+    while (ok && next_unit_consumer()) {
       const int prob = u >= units0;
       const GemmParams& p = pp.p[prob];
       const int lu = u - (prob ? units0 : 0);  // the unit within its problem (split flags)
@@ -1061,6 +1116,10 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
       mbar_inval(&sfull[i]);
       mbar_inval(&sempty[i]);
     }
+    for (int i = 0; i < UNIT_SLOTS; ++i) {
+      mbar_inval(&ufull[i]);
+      mbar_inval(&uempty[i]);
+    }
   }
 }
 
@@ -1389,7 +1448,7 @@ struct ProbLayout {
 };
 struct WsLayout {
   ProbLayout p[kMaxProblems];
-  size_t flags, partials, total;
+  size_t flags, ctrs, partials, total;  // ctrs: the two GEMMs' unit counters, right after the flags
   int nflags;
 };
 
@@ -1441,6 +1500,8 @@ WsLayout ws_layout(const moe_experts_problem* pr, int n, int H, bool fp8, int gr
     L.p[i].flags2 = f;
     f += (size_t)L.p[i].nflags2 * 4;
   }
+  L.ctrs = f;  // contiguous with the flags: one clearing pass covers both
+  f += 2 * 4;
   off = al256(f);
   L.partials = off;
   off = al256(off + (size_t)grid * MG * BM * BN * 4);
@@ -1521,6 +1582,8 @@ moe_status_t experts_run(const moe_experts_problem* probs, int nprob, int H, con
   GemmProblems g1 = {}, g2 = {};
   g1.nprob = g2.nprob = n;
   int* flags_all = reinterpret_cast<int*>(wsb + L.flags);
+  int* ctrs = reinterpret_cast<int*>(wsb + L.ctrs);
+  bool ctrs_cleared = false;  // by the plan launch or the first gather launch, else by a memset below
   // The split flags are cleared by the plan launch when there is one (two-tile group
   // maps), else by the first gather launch, else by a plan launch of their own.
   bool gathers = fp8;
@@ -1533,7 +1596,8 @@ moe_status_t experts_run(const moe_experts_problem* probs, int nprob, int H, con
     plan_kernel<<<1, 1024, 0, s>>>(pr[0].tile_map, pr[0].num_tiles, pr[0].expert_offsets, mg1, mg2,
                                    reinterpret_cast<int32_t*>(wsb + P.gmap), reinterpret_cast<int32_t*>(wsb + P.ngroups),
                                    reinterpret_cast<int32_t*>(wsb + P.gmap2), reinterpret_cast<int32_t*>(wsb + P.ngroups2),
-                                   flags_all, L.nflags);
+                                   flags_all, L.nflags + 2);  // (the unit counters follow the flags)
+    ctrs_cleared = true;
     if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
   }
   for (int i = 0; i < n; ++i) {
@@ -1551,9 +1615,11 @@ moe_status_t experts_run(const moe_experts_problem* probs, int nprob, int H, con
       gather_kernel<<<gb, 256, 0, s>>>(static_cast<const uint8_t*>(q.a1q), q.a1q_scale, q.sorted_slot, (int)S,
                                        q.top_k, H * esz, hb16 ? 1 : H / 128, gather_rows ? wsb + P.A : nullptr, As,
                                        P.s_pad, group == 128 ? H / 128 : (group == MOE_GROUP_TOKEN ? 1 : 0),
-                                       flags_pending ? flags_all : nullptr, flags_pending ? L.nflags : 0, nullptr,
-                                       0, nullptr);
+                                       // the split flags when pending, and the unit counters
+                                       ctrs_cleared ? nullptr : (flags_pending ? flags_all : ctrs),
+                                       ctrs_cleared ? 0 : (flags_pending ? L.nflags : 0) + 2, nullptr, 0, nullptr);
       flags_pending = false;
+      ctrs_cleared = true;
       if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
     }
     // A maps with one-tile and two-tile boxes; weight maps with 256-row boxes (gemm2:
@@ -1599,8 +1665,14 @@ moe_status_t experts_run(const moe_experts_problem* probs, int nprob, int H, con
     p2.out_scale_t = nullptr;
     p2.flags = reinterpret_cast<int*>(wsb + P.flags2);
     p2.allow_split = split2;  // (K of at least 32 blocks for a split to pay)
+    // units handed out from a counter (the dynamic schedule of gemm_body) when dealt
+    // round-robin
+    p1.unit_ctr = i == 0 ? ctrs : nullptr;
+    p2.unit_ctr = i == 0 ? ctrs + 1 : nullptr;
   }
 
+  // (no plan and no gather launch: the identity case, e.g. a shared expert alone)
+  if (!ctrs_cleared && cudaMemsetAsync(ctrs, 0, 2 * sizeof(int), s) != cudaSuccess) return MOE_ERR_CUDA;
   cudaError_t e;
   if (fp8) {  // one problem
     const moe_experts_problem& q = pr[0];

@@ -1,9 +1,15 @@
 """One fused-MoE layer step composed from the C-ABI calls, with every buffer
 allocated once up front (PyTorch allocates, the library computes).
 
-Step (all on one stream):
-  moe_route -> moe_align -> moe_prepare -> moe_experts [-> shared expert via
-  moe_experts with one expert and the identity permutation] -> moe_finalize.
+Step: moe_route -> moe_align -> moe_prepare -> moe_experts [-> shared expert via
+  moe_experts with one expert and the identity permutation] -> moe_finalize, on the
+caller's stream.  The shared expert needs no routing: when it runs as calls of its own
+and neither its GEMMs nor the routed experts' split units across CTAs (whose waits
+assume every CTA of the launch resident, which two concurrent launches cannot
+promise), it runs on a second stream forked at the start of the step and joined
+before the finalize, so its GEMMs overlap the routing, quantisation, gather and the
+routed experts' GEMMs (which take their units from a counter, so CTAs that start
+late because the shared expert still holds their SMs take fewer units).
 NVFP4 layers use moe_prepare_nvfp4 and moe_experts_nvfp4 (the shared expert
 stays bf16).  Single-launch layers run the whole step as one moe_layer_fused launch.
 
@@ -58,6 +64,9 @@ class MoELayer:
             self.al_shared = moe.moe_align(ids0, 1, stream=stream)
             self.ws_shared = torch.empty(max(moe.workspace_size(T, H, cfg.shared_I, 1, 1, "bf16"), 16),
                                          dtype=torch.uint8, device=dev)
+            self.side = torch.cuda.Stream(device=dev)
+            self.ev_fork = torch.cuda.Event()
+            self.ev_join = torch.cuda.Event()
         # the whole step as one launch: a bf16 SiLU layer whose shared expert (if any) has the
         # routed experts' I
         self.single = cfg.single_launch
@@ -68,6 +77,11 @@ class MoELayer:
         # a bf16 layer whose shared expert has the routed experts' I and activation runs both
         # in the same GEMM launches (moe_experts_multi)
         self.fused_shared = (cfg.shared_I == I and cfg.quant == "bf16" and cfg.activation == "silu")
+        # the shared expert on the second stream: its own calls, neither they (one expert, T
+        # rows: split only for T <= 16) nor the routed experts (fp8 never; bf16 and NVFP4
+        # at most 16 slots per expert) split units
+        routed_splits = cfg.quant in ("bf16", "nvfp4") and T * k <= 16 * E
+        self.shared_side = bool(cfg.shared_I) and not self.fused_shared and T > 16 and not routed_splits
         if self.fused_shared:
             a_dummy = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
             self.ws_multi = torch.empty(max(moe.workspace_size_multi(
@@ -84,6 +98,13 @@ class MoELayer:
                 shared_w2=inp.shared_w2[0] if cfg.shared_I else None, residual=inp.residual,
                 rms_weight=inp.rms_weight, eps=1e-6, topk_ids=self.topk_ids, topk_weights=self.topk_weights,
                 output=self.out, ws=self.ws_fused, stream=stream)
+        main = stream if stream is not None else torch.cuda.current_stream()
+        if self.shared_side:
+            self.ev_fork.record(main)
+            self.side.wait_event(self.ev_fork)
+            moe.moe_experts(a1, None, inp.shared_w13, None, inp.shared_w2, None, self.al_shared, "bf16",
+                            out=self.shared, ws=self.ws_shared, identity=True, stream=self.side)
+            self.ev_join.record(self.side)
         moe.moe_route(logits, cfg.top_k, self.scoring, self.topk_ids, self.topk_weights, stream=stream)
         moe.moe_align(self.topk_ids, cfg.E, out=self.al, stream=stream)
         if self.passthrough:
@@ -94,14 +115,17 @@ class MoELayer:
         else:
             a1q, a1q_scale = moe.moe_prepare(a1, self.topk_weights, cfg.top_k, cfg.weight_on_input, cfg.quant,
                                              self.a1q, self.a1q_scale, stream=stream)
-        shared = self.experts(a1q, a1q_scale, a1, stream)
+        shared = self.experts(a1q, a1q_scale, a1, stream, shared_launched=self.shared_side)
+        if self.shared_side:
+            main.wait_event(self.ev_join)
         moe.moe_finalize(self.y, self.topk_weights, cfg.top_k, cfg.weight_on_input, shared=shared,
                          residual=inp.residual, rms_weight=inp.rms_weight, output=self.out, stream=stream)
         return self.out
 
-    def experts(self, a1q, a1q_scale, a1, stream=None):
+    def experts(self, a1q, a1q_scale, a1, stream=None, shared_launched=False):
         """The routed experts into self.y and the shared expert (if any) into
-        self.shared -- one moe_experts_multi call when they can share launches.
+        self.shared -- one moe_experts_multi call when they can share launches;
+        shared_launched: the step has already run the shared expert (second stream).
         Returns the shared-expert rows or None."""
         cfg, inp = self.cfg, self.inp
         if self.shared is not None and self.fused_shared:
@@ -119,6 +143,8 @@ class MoELayer:
                             activation=cfg.activation, out=self.y, ws=self.ws, stream=stream)
         if self.shared is None:
             return None
+        if shared_launched:
+            return self.shared
         return moe.moe_experts(a1, None, inp.shared_w13, None, inp.shared_w2, None, self.al_shared, "bf16",
                                out=self.shared, ws=self.ws_shared, identity=True, stream=stream)
 
