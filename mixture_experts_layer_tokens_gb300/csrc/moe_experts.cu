@@ -52,8 +52,10 @@
 //   schedule  decode-sized problems (at most 16 slots per expert, K of 32+
 //          blocks) with fewer units than half the CTAs split the (unit, K block)
 //          iterations into equal contiguous ranges, one per CTA ("stream-K");
-//          otherwise units are dealt round-robin and units that share a weight
-//          tile run side by side on neighbouring SMs.  A unit cut by a range
+//          otherwise whole units go to the CTAs in the order the CTAs ask for
+//          them (a launch-wide counter; round-robin when no counter is given),
+//          so units that share a weight tile run side by side on neighbouring
+//          SMs and a CTA that starts late takes fewer units.  A unit cut by a range
 //          boundary is finished by the CTA holding its first K blocks: it waits
 //          (bounded) for the later segments' fp32 partials and adds them in
 //          segment order, so results do not depend on timing.  Those later
