@@ -454,6 +454,17 @@ moe_status_t moe_device_status(int clear);
  * faults, traps or hangs.  Asynchronous on stream; MOE_ERR_INVALID_ARG for a limit out of
  * range. */
 moe_status_t moe_selftest_wait_timeout(uint64_t limit_ns, moe_stream_t stream);
+
+/* Self-test of the division the fp8 GEMM1 epilogue uses to requantise h (each element
+ * divided by its row group's scale s = max(amax, 1e-10) / 448, "[vLLM] MoE Oracle &
+ * Prepare/Finalize", the G(128) quantisation): the correctly rounded quotient from the
+ * divisor's correctly rounded reciprocal and one fma correction, compared bit for bit with
+ * the IEEE division on n pseudo-random (dividend, divisor) pairs of that domain drawn
+ * from seed on the device.  *mismatches (device memory, zeroed by the caller) receives the
+ * count of differing results.  Asynchronous on stream; MOE_ERR_INVALID_ARG for n < 0 or a
+ * NULL counter. */
+moe_status_t moe_selftest_row_division(long long n, uint32_t seed, unsigned long long *mismatches,
+                                       moe_stream_t stream);
 const char *moe_status_string(moe_status_t status);
 
 #ifdef __cplusplus

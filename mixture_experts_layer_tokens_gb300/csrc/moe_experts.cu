@@ -346,6 +346,19 @@ __device__ __forceinline__ float act_mul(float g, float u) {
   return act_gate<kAct>(g) * u;
 }
 
+// x / s rounded to nearest (the IEEE quotient) for a divisor shared by many
+// dividends, given rs = __frcp_rn(s), its correctly rounded reciprocal: q = RN(x rs) is
+// within one ulp of x / s, the residual x - s q is exact in one fma, and RN(q + r rs) is
+// then the correctly rounded quotient (P. Markstein, "IA-64 and Elementary Functions",
+// 2000, the final correction step of division).  A zero quotient keeps the sign of x.
+// Three operations per element against a full division each; the self-test
+// moe_selftest_row_division compares it with __fdiv_rn bit for bit.
+__device__ __forceinline__ float div_rn_by(float x, float s, float rs) {
+  const float q = __fmul_rn(x, rs);
+  const float r = __fmaf_rn(-q, s, x);
+  return copysignf(__fmaf_rn(r, rs, q), x);
+}
+
 // The persistent GEMM (see the top of the file), run by every CTA of the grid over the
 // dynamic shared memory `smem_raw`.  `standalone`: the CTA's only work (it gives up its
 // TMEM allocation permit after allocating); otherwise one phase of a longer kernel,
@@ -1007,6 +1020,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
             amax = fmaxf(amax, fabsf(accv[i]));
           }
           const float s = __fdiv_rn(fmaxf(amax, 1e-10f), 448.0f);
+          const float rs = __frcp_rn(s);
           if (valid && grp * 128 < p.I) {
             uint8_t* hrow = static_cast<uint8_t*>(p.out) + (size_t)prow * p.I + grp * 128;
 #pragma unroll
@@ -1016,9 +1030,11 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
               for (int j = 0; j < 4; ++j) {
                 const int i0 = 16 * v + 4 * j;
                 const uint32_t lo = (uint32_t)__nv_cvt_float2_to_fp8x2(
-                    make_float2(__fdiv_rn(accv[i0], s), __fdiv_rn(accv[i0 + 1], s)), __NV_SATFINITE, __NV_E4M3);
+                    make_float2(div_rn_by(accv[i0], s, rs), div_rn_by(accv[i0 + 1], s, rs)), __NV_SATFINITE,
+                    __NV_E4M3);
                 const uint32_t hi = (uint32_t)__nv_cvt_float2_to_fp8x2(
-                    make_float2(__fdiv_rn(accv[i0 + 2], s), __fdiv_rn(accv[i0 + 3], s)), __NV_SATFINITE, __NV_E4M3);
+                    make_float2(div_rn_by(accv[i0 + 2], s, rs), div_rn_by(accv[i0 + 3], s, rs)), __NV_SATFINITE,
+                    __NV_E4M3);
                 wds[j] = lo | (hi << 16);
               }
               reinterpret_cast<uint4*>(hrow)[v] = make_uint4(wds[0], wds[1], wds[2], wds[3]);
@@ -1043,6 +1059,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
           xphase ^= 1;
           xbuf ^= 1;
           const float s = __fdiv_rn(fmaxf(amax, 1e-10f), 448.0f);
+          const float rs = __frcp_rn(s);
           if (valid) {
             uint8_t* hrow = static_cast<uint8_t*>(p.out) + (size_t)prow * p.I + it.n * 128 + 64 * half;
 #pragma unroll
@@ -1052,9 +1069,11 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
               for (int j = 0; j < 4; ++j) {
                 const int i0 = 16 * v + 4 * j;
                 const uint32_t lo = (uint32_t)__nv_cvt_float2_to_fp8x2(
-                    make_float2(__fdiv_rn(accv[i0], s), __fdiv_rn(accv[i0 + 1], s)), __NV_SATFINITE, __NV_E4M3);
+                    make_float2(div_rn_by(accv[i0], s, rs), div_rn_by(accv[i0 + 1], s, rs)), __NV_SATFINITE,
+                    __NV_E4M3);
                 const uint32_t hi = (uint32_t)__nv_cvt_float2_to_fp8x2(
-                    make_float2(__fdiv_rn(accv[i0 + 2], s), __fdiv_rn(accv[i0 + 3], s)), __NV_SATFINITE, __NV_E4M3);
+                    make_float2(div_rn_by(accv[i0 + 2], s, rs), div_rn_by(accv[i0 + 3], s, rs)), __NV_SATFINITE,
+                    __NV_E4M3);
                 wds[j] = lo | (hi << 16);
               }
               reinterpret_cast<uint4*>(hrow)[v] = make_uint4(wds[0], wds[1], wds[2], wds[3]);
@@ -2391,6 +2410,41 @@ moe_status_t experts_nvfp4_run(const void* a1q, const void* a1q_sf, const float*
 // Self-test of the failure path of the device-side waits: one thread waits (bounded) on an
 // mbarrier that no thread arrives on, with the GEMMs' wait routine and a caller-chosen
 // limit; the wait gives up, records MOE_ERR_TIMEOUT and the kernel returns.
+// div_rn_by against __fdiv_rn on n (dividend, divisor) pairs drawn from a counter-based
+// hash: divisors are the requantisation scales max(amax, 1e-10) / 448 of amax values over
+// 2^-40 .. 2^40 (with every mantissa), dividends of either sign anywhere in [0, amax]
+// (their mantissas and exponents drawn independently, zeros included), and every
+// mismatching bit pattern is counted into *mismatches (which the caller zeroes).
+__device__ __forceinline__ uint32_t selftest_hash(uint32_t x) {
+  x ^= x >> 16;
+  x *= 0x7feb352dU;
+  x ^= x >> 15;
+  x *= 0x846ca68bU;
+  x ^= x >> 16;
+  return x;
+}
+__global__ void __launch_bounds__(256)
+    division_selftest_kernel(long long n, uint32_t seed, unsigned long long* mismatches) {
+  unsigned long long bad = 0;
+  for (long long i = (long long)blockIdx.x * 256 + threadIdx.x; i < n; i += (long long)gridDim.x * 256) {
+    const uint32_t h0 = selftest_hash((uint32_t)i * 2u + 1u + seed * 0x9e3779b9U);
+    const uint32_t h1 = selftest_hash(h0 ^ 0x5bd1e995U);
+    const uint32_t h2 = selftest_hash(h1 + (uint32_t)(i >> 32));
+    // amax = mantissa (23 random bits) x 2^(e - 40), e in [0, 80]
+    const float amax = __uint_as_float(((h0 % 81u + 87u) << 23) | (h1 & 0x7FFFFFu));
+    const float s = __fdiv_rn(fmaxf(amax, 1e-10f), 448.0f);
+    // x = +-(random mantissa) x 2^-k x amax-scale, k in [0, 40); 1 in 64 exactly 0 or amax
+    float x = __uint_as_float(((h2 % 40u + 87u) << 23) | (h2 >> 9 & 0x7FFFFFu));
+    x = fminf(__fmul_rn(x, __uint_as_float(__float_as_uint(amax) & 0x7F800000u)), amax);  // x amax's power of 2
+    if ((h1 >> 23 & 63u) == 0u) x = (h1 & (1u << 30)) ? amax : 0.0f;
+    if (h2 & 1u) x = -x;
+    const float q_ref = __fdiv_rn(x, s);
+    const float q = div_rn_by(x, s, __frcp_rn(s));
+    if (__float_as_uint(q) != __float_as_uint(q_ref)) ++bad;
+  }
+  if (bad) atomicAdd(mismatches, bad);
+}
+
 __global__ void __launch_bounds__(32) selftest_wait_kernel(uint64_t limit_ns) {
   __shared__ uint64_t bar;
   if (threadIdx.x == 0) {
@@ -2649,6 +2703,15 @@ extern "C" moe_status_t moe_layer_fused(const float* logits, const void* a1, int
                          fp) != cudaSuccess)
     return MOE_ERR_CUDA;
   return MOE_OK;
+}
+
+extern "C" moe_status_t moe_selftest_row_division(long long n, uint32_t seed, unsigned long long* mismatches,
+                                                  moe_stream_t stream) {
+  MOE_CHECK_ARG(n >= 0 && mismatches);
+  if (n == 0) return MOE_OK;
+  division_selftest_kernel<<<(unsigned)std::min<long long>((n + 255) / 256, 4096), 256, 0,
+                             reinterpret_cast<cudaStream_t>(stream)>>>(n, seed, mismatches);
+  return launch_status();
 }
 
 extern "C" moe_status_t moe_selftest_wait_timeout(uint64_t limit_ns, moe_stream_t stream) {

@@ -96,6 +96,7 @@ SIGNATURES = {
     "moe_finalize_batched": ([_P, _P, _I, _P, _P, _P, _P, _P, _P, _P, _F, _I, _I, _I, _I, _I, _P, _F, _P, _P], _I),
     "moe_device_status": ([_I], _I),
     "moe_selftest_wait_timeout": ([ctypes.c_uint64, _P], _I),
+    "moe_selftest_row_division": ([ctypes.c_longlong, ctypes.c_uint32, _P, _P], _I),
     "moe_status_string": ([_I], ctypes.c_char_p),
 }
 
@@ -484,6 +485,15 @@ def moe_finalize(fused_expert_output: torch.Tensor, topk_weights: Optional[torch
 
 def moe_device_status(clear: bool = True) -> int:
     return int(lib().moe_device_status(int(clear)))
+
+
+def moe_selftest_row_division(n: int, seed: int, stream=None) -> int:
+    """Run the library's self-test of the requantisation division (see moe.h) on n
+    pairs; returns how many results differ from the IEEE division."""
+    cnt = torch.zeros(1, dtype=torch.int64, device="cuda")
+    _check("moe_selftest_row_division",
+           lib().moe_selftest_row_division(int(n), int(seed) & 0xFFFFFFFF, _ptr(cnt), _stream(stream)))
+    return int(cnt.item())
 
 
 def moe_selftest_wait_timeout(limit_ns: int, stream=None) -> None:
