@@ -147,7 +147,12 @@ struct Cfg {
   static constexpr int SCALE_SLOTS = 8;
   static constexpr int SCALE_SLOT_FLOATS = 132;
   static constexpr int SCALE_RING_BYTES = kFP8 ? SCALE_SLOTS * SCALE_SLOT_FLOATS * 4 : 0;
+  // fp8: per epilogue warp a 32-row x 32-column bf16 staging tile for the gemm2 output
+  // (80-byte rows: conflict-free for the row-per-lane writes and the 8-rows-per-store reads)
+  static constexpr int OUT_STAGE_STRIDE = 80;
+  static constexpr int OUT_STAGE_BYTES = kFP8 ? Warps<kFP8>::EPI * 32 * OUT_STAGE_STRIDE : 0;
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 4096 /*barriers, exchange*/ + SCALE_RING_BYTES +
+                                    OUT_STAGE_BYTES +
                                     1024 /*align*/;
   static_assert(!kFP4 || (!kFP8 && kMG == 1), "NVFP4 units hold one M tile");
   static_assert(!kFP4 || SF_TMEM_BASE + STAGES * SF_TMEM_STAGE <= TMEM_COLS, "NVFP4 scales must fit the TMEM");
@@ -395,6 +400,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(uempty + UNIT_SLOTS);
   volatile int* unit_ring = reinterpret_cast<volatile int*>(tmem_slot + 1);  // [UNIT_SLOTS]
   float* scale_ring = reinterpret_cast<float*>(ctrl + 4096);  // fp8: [SCALE_SLOTS][SCALE_SLOT_FLOATS]
+  uint8_t* out_stage = ctrl + 4096 + C::SCALE_RING_BYTES;  // fp8 gemm2: [EPI warps][32][OUT_STAGE_STRIDE]
   float* amax_x = reinterpret_cast<float*>(ctrl + 512);  // [2 items][2 halves][BM]
   // control block: barriers, TMEM address and unit ring below byte 512, the amax exchange up
   // to 2560, the NVFP4 scale barriers from 3072, the fp8 scale ring from 4096
@@ -943,6 +949,9 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
         //        [64 half, +64) and up columns [128 + 64 half, +64).
         // gemm2: this thread owns output columns [128 half, +128).
         const int half = sub;
+        // gemm2: the slot this row's output goes to, loaded now so that its latency
+        // passes under the K loop instead of stalling the unit's end
+        const int f_out = kKind == kGemm2 && valid ? (p.sorted_slot ? ld_tab<kCoh>(p.sorted_slot + prow) : prow) : -1;
         // sums as pairs of columns: one packed two-wide fp32 FMA (each lane an IEEE fma)
         // per pair and K block
         float2 acc2[64];
@@ -1081,18 +1090,36 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
             if (half == 0) p.out_scale_t[(size_t)it.n * p.s_pad + prow] = s;
           }
         } else {
+          // y rows (scattered to their slots): a lane holds one row's 128 columns, so the
+          // warp passes them through its staging tile 32 columns at a time and each store
+          // then writes 64 contiguous bytes of each of 8 rows, not 16 bytes of 32 rows
           const int c0 = it.n * 256 + 128 * half;
-          if (valid && c0 < p.H) {
-            const int f = p.sorted_slot ? ld_tab<kCoh>(p.sorted_slot + prow) : prow;
-            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + (size_t)f * p.H + c0);
+          if (c0 < p.H) {  // (warp-uniform)
+            const int f = f_out;
+            uint8_t* stg = out_stage + (warp - Warps<kFP8>::FIRST_EPI) * 32 * C::OUT_STAGE_STRIDE;
+            __nv_bfloat16* ybase = static_cast<__nv_bfloat16*>(p.out) + c0;
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              uint4 o;
-              o.x = pack_bf16x2(accv[8 * j + 0], accv[8 * j + 1]);
-              o.y = pack_bf16x2(accv[8 * j + 2], accv[8 * j + 3]);
-              o.z = pack_bf16x2(accv[8 * j + 4], accv[8 * j + 5]);
-              o.w = pack_bf16x2(accv[8 * j + 6], accv[8 * j + 7]);
-              dst[j] = o;
+            for (int ch = 0; ch < 4; ++ch) {
+              uint4* srow = reinterpret_cast<uint4*>(stg + lane * C::OUT_STAGE_STRIDE);
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                const int j = 32 * ch + 8 * q;
+                uint4 o;
+                o.x = pack_bf16x2(accv[j + 0], accv[j + 1]);
+                o.y = pack_bf16x2(accv[j + 2], accv[j + 3]);
+                o.z = pack_bf16x2(accv[j + 4], accv[j + 5]);
+                o.w = pack_bf16x2(accv[j + 6], accv[j + 7]);
+                srow[q] = o;
+              }
+              __syncwarp();
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const int rr = 8 * i + (lane & 7), pc = lane >> 3;  // row of the tile, 16-byte piece
+                const int fr = __shfl_sync(0xffffffffu, f, rr);
+                const uint4 v = *reinterpret_cast<const uint4*>(stg + rr * C::OUT_STAGE_STRIDE + pc * 16);
+                if (fr >= 0) *reinterpret_cast<uint4*>(ybase + (size_t)fr * p.H + 32 * ch + 8 * pc) = v;
+              }
+              __syncwarp();
             }
           }
         }
