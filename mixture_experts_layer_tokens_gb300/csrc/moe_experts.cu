@@ -2070,7 +2070,7 @@ FusedLayout fused_layout(int T, int H, int I, int E, int top_k, bool shared, int
   L.nflags1 = (cap + (shared ? sh_tiles : 0)) * (I / 128);
   L.nflags2 = (cap + (shared ? sh_tiles : 0)) * ((H + 255) / 256);
   size_t off = 0;
-  L.ctr = off;
+  L.ctr = off;  // the grid barrier's arrival count, then the two GEMM phases' unit counters
   off += 16;
   L.flags1 = off;
   off += (size_t)L.nflags1 * 4;
@@ -2702,6 +2702,10 @@ extern "C" moe_status_t moe_layer_fused(const float* logits, const void* a1, int
     q2.out = i ? (void*)fp.ys : (void*)fp.y;
     q2.flags = reinterpret_cast<int*>(wsb + L.flags2) + (i ? cap * ((H + 255) / 256) : 0);
     q2.allow_split = split2;
+    // the GEMM phases' unit counters (dynamic schedule when units go round-robin): the two
+    // words after the barrier counter, cleared with it before the launch
+    q1.unit_ctr = i == 0 ? reinterpret_cast<int*>(wsb + L.ctr) + 1 : nullptr;
+    q2.unit_ctr = i == 0 ? reinterpret_cast<int*>(wsb + L.ctr) + 2 : nullptr;
   }
   static int configured[64] = {0};
   void (*kern)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap,
