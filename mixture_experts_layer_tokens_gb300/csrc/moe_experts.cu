@@ -351,19 +351,6 @@ __device__ __forceinline__ float act_mul(float g, float u) {
   return act_gate<kAct>(g) * u;
 }
 
-// x / s rounded to nearest (the IEEE quotient) for a divisor shared by many
-// dividends, given rs = __frcp_rn(s), its correctly rounded reciprocal: q = RN(x rs) is
-// within one ulp of x / s, the residual x - s q is exact in one fma, and RN(q + r rs) is
-// then the correctly rounded quotient (P. Markstein, "IA-64 and Elementary Functions",
-// 2000, the final correction step of division).  A zero quotient keeps the sign of x.
-// Three operations per element against a full division each; the self-test
-// moe_selftest_row_division compares it with __fdiv_rn bit for bit.
-__device__ __forceinline__ float div_rn_by(float x, float s, float rs) {
-  const float q = __fmul_rn(x, rs);
-  const float r = __fmaf_rn(-q, s, x);
-  return copysignf(__fmaf_rn(r, rs, q), x);
-}
-
 // The persistent GEMM (see the top of the file), run by every CTA of the grid over the
 // dynamic shared memory `smem_raw`.  `standalone`: the CTA's only work (it gives up its
 // TMEM allocation permit after allocating); otherwise one phase of a longer kernel,

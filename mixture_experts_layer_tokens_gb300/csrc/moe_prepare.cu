@@ -72,10 +72,11 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
   for (int off = 8; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(half_mask, amax, off));
   const float s = __fdiv_rn(fmaxf(amax, 1e-10f), 448.0f);
+  const float rs = __frcp_rn(s);
   uint32_t packed[2];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const float2 r = make_float2(__fdiv_rn(x[2 * i], s), __fdiv_rn(x[2 * i + 1], s));
+    const float2 r = make_float2(div_rn_by(x[2 * i], s, rs), div_rn_by(x[2 * i + 1], s, rs));
     const uint32_t two = (uint32_t)__nv_cvt_float2_to_fp8x2(r, __NV_SATFINITE, __NV_E4M3);
     if (i & 1)
       packed[i >> 1] |= two << 16;
