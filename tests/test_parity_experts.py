@@ -130,6 +130,35 @@ def test_experts_identity_permutation(cuda_dev):
     check_bf16(y, yref, "identity", slack=_stored_pair_slack(yref))
 
 
+@pytest.mark.parametrize("quant,identity", [("fp8", False), ("bf16", False), ("bf16", True)])
+def test_experts_reused_dirty_workspace(cuda_dev, quant, identity):
+    """Units dealt round-robin are taken from counters in the workspace; every call clears
+    them (in its gather or plan launch, or a memset for the identity case with neither), so
+    a workspace that starts as garbage and serves call after call gives the same bits, and
+    those agree with the oracle."""
+    E, k = (1, 1) if identity else (8, 2)
+    base = CONFIGS["deepseek"] if quant == "fp8" else CONFIGS["tiny"]
+    inp = make_inputs(scaled(base, T=600, H=512, I=384, E=E, top_k=k, shared_I=0))
+    ids = torch.zeros((600, 1), dtype=torch.int32) if identity else _ids(600, k, E, 5)
+    T, H, I = 600, 512, 384
+    al = moe.moe_align(ids.to(cuda_dev), E)
+    a1q, sc = moe.moe_prepare(inp.a1.to(cuda_dev), None, k, False, quant)
+    d = lambda t: None if t is None else t.to(cuda_dev)
+    ws = torch.full((max(moe.workspace_size(T, H, I, E, k, quant), 16),), 0xFF, dtype=torch.uint8, device=cuda_dev)
+    ys = [moe.moe_experts(a1q, sc, d(inp.w13), d(inp.w13_scale), d(inp.w2), d(inp.w2_scale), al, quant,
+                          identity=identity, ws=ws).clone() for _ in range(3)]
+    torch.cuda.synchronize()
+    assert moe.moe_device_status() == moe.MOE_OK
+    assert torch.equal(ys[0], ys[1]) and torch.equal(ys[1], ys[2])
+    rq, rs = moe_ref.prepare(inp.a1, None, False, quant)
+    yref = moe_ref.experts(rq, rs, inp.w13, inp.w13_scale, inp.w2, inp.w2_scale, moe_ref.align(ids, E, 128), k, quant,
+                           "silu")
+    if quant == "bf16":
+        check_bf16(ys[0], yref, "reused workspace", slack=_stored_pair_slack(yref))
+    else:
+        check_fp8(ys[0], yref, "reused workspace")
+
+
 def test_experts_twice_same_bits(cuda_dev):
     inp = make_inputs(scaled(CONFIGS["tiny"], T=300, H=512, I=384, E=4))
     ids = _ids(300, 2, 4, 3)
