@@ -1604,12 +1604,19 @@ moe_status_t experts_run(const moe_experts_problem* probs, int nprob, int H, con
     const long long S = (long long)pr[0].T * pr[0].top_k;
     const int cap_tiles = std::max(1, moe_tile_map_capacity((int)S, pr[0].E, BM));
     const bool full_tiles = S >= (long long)BM * pr[0].E;  // experts average a full 128-row tile or more
-    auto mg_for = [&](int nt) {
+    // also prefill-sized problems (four or more waves of two-tile units) with deep K loops
+    // (64+ blocks): the weight tile goes through shared memory once for two M tiles, and
+    // the unit's epilogue, not overlapped with MMAs (the two tiles' accumulators take the
+    // whole TMEM), is short against its K loop -- Mixtral-like T=4096 / 8192 experts -5 %
+    // / -8 %; with short K loops (Qwen3-like, 12-32 blocks) the unhidden epilogues lose 8 %
+    auto mg_for = [&](int nt, int K) {
       const long long units2 = (long long)((cap_tiles + 1) / 2) * nt;  // estimate with two tiles per unit
-      return (full_tiles && 2 * units2 >= grid && units2 <= grid) ? 2 : 1;
+      const bool one_wave = 2 * units2 >= grid && units2 <= grid;
+      const bool prefill = units2 >= 4LL * grid && K / 64 >= 64;
+      return (full_tiles && (one_wave || prefill)) ? 2 : 1;
     };
-    mg1 = mg_for(nt1);
-    mg2 = mg_for((H + 255) / 256);
+    mg1 = mg_for(nt1, H);
+    mg2 = mg_for((H + 255) / 256, pr[0].I);
   }
   const bool split1 = allow_split && H / 64 >= 32, split2 = allow_split && pr[0].I / 64 >= 32;
 
