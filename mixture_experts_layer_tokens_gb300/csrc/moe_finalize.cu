@@ -45,6 +45,14 @@ __device__ __forceinline__ void add_bf16x8(float (&o)[8], uint4 v, float w) {
   }
 }
 
+// 16-byte asynchronous copy global -> shared (L2 only), and the wait for this thread's own
+__device__ __forceinline__ void cp_async_16(void* smem_dst, const void* gmem_src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)), "l"(gmem_src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_own() {
+  asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+
 __device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
@@ -94,6 +102,9 @@ __global__ void __launch_bounds__(kThreads)
   const bool res_in_place = residual_out != nullptr && residual_out == residual;
   __shared__ float red[kThreads / 32];
   __shared__ float cta_ss;
+  // the slice of the RMSNorm weight, copied in at the start (no registers held while
+  // the rows stream in); each thread reads back only the vectors it copied
+  __shared__ __align__(16) uint4 gamma_s[NV * kThreads];
   const int t = blockIdx.x / kC;
   const uint32_t rank = kC > 1 ? cluster_rank() : 0;
   const int vslice = H / 8 / kC;                // vectors of this CTA's slice
@@ -115,6 +126,13 @@ __global__ void __launch_bounds__(kThreads)
     // then the shared and residual slices
     if (shared) prefetch_l2(shared + row + (size_t)v0 * 8, (uint32_t)vslice * 16);
     if (residual) prefetch_l2(residual + row + (size_t)v0 * 8, (uint32_t)vslice * 16);
+  }
+  if (gamma) {
+#pragma unroll
+    for (int u = 0; u < NV; ++u) {
+      const int vi = threadIdx.x + u * kThreads;
+      if (vi < vslice) cp_async_16(&gamma_s[vi], gamma + (size_t)(v0 + vi) * 8);
+    }
   }
 
   // Short slices (a few vectors per thread, the cluster launches of small T): every row's
@@ -231,11 +249,12 @@ __global__ void __launch_bounds__(kThreads)
       total = cta_ss;
     }
     const float inv = rsqrtf(total / (float)H + eps);
+    cp_async_wait_own();
 #pragma unroll
     for (int u = 0; u < NV; ++u) {
       const int vi = threadIdx.x + u * kThreads;
       if (vi < vslice) {
-        const uint4 g = __ldg(reinterpret_cast<const uint4*>(gamma + (size_t)(v0 + vi) * 8));
+        const uint4 g = gamma_s[vi];
         const uint32_t gu[4] = {g.x, g.y, g.z, g.w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
