@@ -65,12 +65,18 @@ __device__ __forceinline__ uint32_t cluster_rank() {
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
-__device__ __forceinline__ float ld_dsmem_f32(const float* local, uint32_t rank) {
+// The two halves of a cluster barrier phase that orders nothing: arrived at on entry, waited
+// on before the first write to another CTA's shared memory (every CTA of the cluster has
+// started by then)
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.aligned;" ::: "memory"); }
+// Store v at the same shared-memory variable of the cluster's CTA `rank` (distributed shared memory).
+__device__ __forceinline__ void st_dsmem_f32(float* local, uint32_t rank, float v) {
   uint32_t remote;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
-  return v;
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote), "f"(v) : "memory");
 }
 
 // Where the expert rows of the slots are: token-major rows y[t * top_k + j] (the standard
@@ -101,12 +107,13 @@ __global__ void __launch_bounds__(kThreads)
   // by the thread that later writes it, through coherent loads in that case
   const bool res_in_place = residual_out != nullptr && residual_out == residual;
   __shared__ float red[kThreads / 32];
-  __shared__ float cta_ss;
+  __shared__ float cta_ss[kC];  // the sum of squares of each CTA of the cluster, by rank
   // the slice of the RMSNorm weight, copied in at the start (no registers held while
   // the rows stream in); each thread reads back only the vectors it copied
   __shared__ __align__(16) uint4 gamma_s[NV * kThreads];
   const int t = blockIdx.x / kC;
   const uint32_t rank = kC > 1 ? cluster_rank() : 0;
+  if (kC > 1 && gamma) cluster_arrive_relaxed();
   const int vslice = H / 8 / kC;                // vectors of this CTA's slice
   const int v0 = (int)rank * vslice;            // first vector of the slice within the row
   const size_t row = (size_t)t * H;
@@ -230,24 +237,29 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
     if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+    if (kC > 1) cluster_wait();  // (the phase arrived at on entry: every peer has started)
     __syncthreads();
     if (threadIdx.x == 0) {
       float s = 0.f;
 #pragma unroll
       for (int w = 0; w < kThreads / 32; ++w) s += red[w];
-      cta_ss = s;
-    }
-    float total;
-    if (kC > 1) {
-      cluster_sync();  // every CTA's cta_ss is written
-      total = 0.f;
+      // this CTA's sum goes to slot `rank` of every CTA of the cluster (its own included)
+      if (kC > 1) {
 #pragma unroll
-      for (int r = 0; r < kC; ++r) total += ld_dsmem_f32(&cta_ss, (uint32_t)r);
-      cluster_sync();  // no CTA leaves while another still reads its cta_ss
-    } else {
-      __syncthreads();
-      total = cta_ss;
+        for (int r = 0; r < kC; ++r) st_dsmem_f32(&cta_ss[rank], (uint32_t)r, s);
+      } else {
+        cta_ss[0] = s;
+      }
     }
+    // one cluster barrier: every slot of every CTA is written (the stores precede the
+    // release), and no CTA is read from after it, so each may leave as soon as it is done
+    if (kC > 1)
+      cluster_sync();
+    else
+      __syncthreads();
+    float total = 0.f;
+#pragma unroll
+    for (int r = 0; r < kC; ++r) total += cta_ss[r];  // rank order: the same bits in every CTA
     const float inv = rsqrtf(total / (float)H + eps);
     cp_async_wait_own();
 #pragma unroll
