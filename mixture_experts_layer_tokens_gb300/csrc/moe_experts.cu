@@ -1608,12 +1608,16 @@ moe_status_t experts_run(const moe_experts_problem* probs, int nprob, int H, con
     // (64+ blocks): the weight tile goes through shared memory once for two M tiles, and
     // the unit's epilogue, not overlapped with MMAs (the two tiles' accumulators take the
     // whole TMEM), is short against its K loop -- Mixtral-like T=4096 / 8192 experts -5 %
-    // / -8 %; with short K loops (Qwen3-like, 12-32 blocks) the unhidden epilogues lose 8 %
+    // / -8 %; with short K loops (Qwen3-like, 12-32 blocks) the unhidden epilogues lose 8 %.
+    // And one dense expert (a shared expert) with a wave or more of two-tile units: the
+    // DeepSeek-like shared expert at T=4096 / 16384 (-1 % on the layer step, whose routed
+    // units fill the shared expert's last wave)
     auto mg_for = [&](int nt, int K) {
       const long long units2 = (long long)((cap_tiles + 1) / 2) * nt;  // estimate with two tiles per unit
       const bool one_wave = 2 * units2 >= grid && units2 <= grid;
       const bool prefill = units2 >= 4LL * grid && K / 64 >= 64;
-      return (full_tiles && (one_wave || prefill)) ? 2 : 1;
+      const bool dense = pr[0].E == 1 && units2 >= grid;
+      return (full_tiles && (one_wave || prefill || dense)) ? 2 : 1;
     };
     mg1 = mg_for(nt1, H);
     mg2 = mg_for((H + 255) / 256, pr[0].I);
