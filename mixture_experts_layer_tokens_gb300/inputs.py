@@ -81,6 +81,11 @@ def _cfgs():
                              description="Qwen3-MoE-like layer T4096 H2048 I768 E128 top8 bf16")
     c["qwen3_fp8"] = LayerConfig("qwen3_fp8", 4096, 2048, 768, 128, 8, quant="fp8",
                                  description="Qwen3-MoE-like layer T4096 H2048 I768 E128 top8 fp8 G(128)")
+    # the Llama-4-Scout-like shared expert alone at T=512: one dense expert of 512 rows, where the
+    # expert GEMMs are tensor-bound (top-1 over one expert: every weight is 1)
+    c["llama_shared512"] = LayerConfig("llama_shared512", 512, 5120, 8192, 1, 1,
+                                       description="Llama-4-Scout-like shared expert alone T512 H5120 I8192 "
+                                                   "(one dense expert, bf16)")
     c["deepseek_T16384"] = LayerConfig("deepseek_T16384", 16384, 7168, 2048, 256, 8, quant="fp8", shared_I=2048,
                                        description="DeepSeek-V3-like layer T16384 H7168 I2048 E256 top8 fp8 + bf16 shared (prefill)")
     # same per-expert shape as the DeepSeek-V3-like layer (~128 rows per expert), a quarter of the
