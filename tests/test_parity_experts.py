@@ -101,6 +101,12 @@ def _ids(T, k, E, seed, skew=False):
     (1, 4096, 1024, 8, 1, False),     # stream-K GEMM1: 8 units cut into ~19 segments each
     (16, 2048, 4096, 1, 1, False),    # stream-K, 16 valid rows in one tile (the shared-expert shape)
     (12, 2048, 2048, 8, 2, True),     # stream-K with skewed routing: one expert holds most rows
+    # two-tile units (on 152 SMs): 96 GEMM1 / 128 GEMM2 units of two 128-row tiles fill one
+    # wave, experts of ~128 rows give groups of one and of two tiles
+    (512, 4096, 1536, 8, 2, False),
+    # one dense expert of 16 tiles: 160 two-tile GEMM1 units (more than a wave: the dense
+    # expert's rule), 80 two-tile GEMM2 units (one wave)
+    (2048, 2560, 2560, 1, 1, False),
 ])
 def test_experts_bf16(cuda_dev, T, H, I, E, k, skew):
     inp = make_inputs(scaled(CONFIGS["tiny"], T=T, H=H, I=I, E=E, top_k=k))

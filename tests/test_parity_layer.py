@@ -128,7 +128,8 @@ def test_layer_small_all_tokens(cuda_dev, name):
     _check(cfg, out, ref, name)
 
 
-@pytest.mark.parametrize("name,sample", [("mixtral", 12), ("deepseek", 3), ("qwen3", 8), ("qwen3_fp8", 8),
+@pytest.mark.parametrize("name,sample", [("mixtral", 12), ("mixtral_T4096", 4), ("deepseek", 3), ("deepseek_T16384", 3),
+                                         ("qwen3", 8), ("qwen3_fp8", 8),
                                          ("llama1", 1), ("llama8", 8),
                                          ("llama64", 6), ("llama512", 6), ("llama_shared512", 6), ("mixtral_nvfp4", 12),
                                          ("llama1_nvfp4", 1), ("llama1_fused", 1), ("llama64_fused", 6),
