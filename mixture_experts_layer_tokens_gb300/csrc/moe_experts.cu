@@ -133,11 +133,17 @@ constexpr int SFB_BYTES = 2 * 128 * 16;
 constexpr int SF_TMEM_BASE = 256;
 constexpr int SF_TMEM_STAGE = 4 * 4 + 4 * 8;
 
-template <bool kFP8, int kMG, bool kFP4 = false>
+// kDec: decode-sized bf16 problems (at most 32 rows per tile, i.e. T <= 32): a stage holds
+// the first 32 rows of the A tile (a 32-row box; the MMA still reads 128 rows, the last 96
+// from the weight tile beside them, and their accumulator lanes are never read) and the
+// 12 KB saved per stage buy two more stages, so each SM has half as many weight bytes again
+// in flight and spends a quarter less of its copy bandwidth on padding rows.
+template <bool kFP8, int kMG, bool kFP4 = false, bool kDec = false>
 struct Cfg {
   static constexpr int MG = kMG;  // M tiles per unit
-  static constexpr int STAGES = kMG == 2 ? 3 : 4;
-  static constexpr int STAGE_BYTES = MG * A_BYTES + 2 * B_HALF_BYTES + (kFP4 ? SFA_BYTES + SFB_BYTES : 0);
+  static constexpr int A_STAGE = kDec ? A_BYTES / 4 : A_BYTES;  // A bytes per M tile in a stage
+  static constexpr int STAGES = kDec ? 6 : (kMG == 2 ? 3 : 4);
+  static constexpr int STAGE_BYTES = MG * A_STAGE + 2 * B_HALF_BYTES + (kFP4 ? SFA_BYTES + SFB_BYTES : 0);
   static constexpr int kBK = kFP4 ? 2 * BKB : (kFP8 ? BKB : BKB / 2);  // K elements per stage
   static constexpr int kMapK = kFP4 ? BKB : kBK;  // the same in units of the tensor maps' elements
   static constexpr int kMmaBytes = 32;            // bytes of K per tcgen05.mma (K = 16 bf16, 32 fp8, 64 fp4)
@@ -155,6 +161,7 @@ struct Cfg {
                                     OUT_STAGE_BYTES +
                                     1024 /*align*/;
   static_assert(!kFP4 || (!kFP8 && kMG == 1), "NVFP4 units hold one M tile");
+  static_assert(!kDec || (!kFP8 && !kFP4 && kMG == 1), "decode stages: bf16 units of one tile");
   static_assert(!kFP4 || SF_TMEM_BASE + STAGES * SF_TMEM_STAGE <= TMEM_COLS, "NVFP4 scales must fit the TMEM");
 };
 
@@ -356,13 +363,13 @@ __device__ __forceinline__ float act_mul(float g, float u) {
 // TMEM allocation permit after allocating); otherwise one phase of a longer kernel,
 // which may allocate again and re-initialise the barriers, so they are invalidated at
 // the end.
-template <bool kFP8, int kKind, int kMG, int kAct, bool kHB16, bool kFP4, bool kCoh = false>
+template <bool kFP8, int kKind, int kMG, int kAct, bool kHB16, bool kFP4, bool kCoh = false, bool kDec = false>
 __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensorMap& tmA2, const CUtensorMap& tmB,
                                           const CUtensorMap& tmA_1, const CUtensorMap& tmA2_1,
                                           const CUtensorMap& tmB_1, const CUtensorMap& tmSA,
                                           const CUtensorMap& tmSB, const GemmProblems& pp, uint8_t* smem_raw,
                                           bool standalone) {
-  using C = Cfg<kFP8, kMG, kFP4>;
+  using C = Cfg<kFP8, kMG, kFP4, kDec>;
   // gemm1 forms: a gated activation reads 128 gate + 128 up rows per unit (one 3-D
   // box); a *_NO_MUL one reads 256 consecutive gate rows, like gemm2
   constexpr bool kNoMul = kKind == kGemm1 && (kAct == MOE_ACT_SILU_NO_MUL || kAct == MOE_ACT_GELU_NO_MUL);
@@ -541,9 +548,9 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
         }
         if (lane == 0) {
           uint8_t* sA = smem + stage * C::STAGE_BYTES;
-          uint8_t* sB = sA + MG * A_BYTES;
+          uint8_t* sB = sA + MG * C::A_STAGE;
           mbar_arrive_expect_tx(&full[stage],
-                                mcnt * A_BYTES + 2 * B_HALF_BYTES + (kFP4 ? SFA_BYTES + SFB_BYTES : 0));
+                                mcnt * C::A_STAGE + 2 * B_HALF_BYTES + (kFP4 ? SFA_BYTES + SFB_BYTES : 0));
           const int kx = kb * C::kMapK;
           if (kFP4) {
             // the block scales of the stage: 16 bytes of each A row and of each weight row
@@ -604,7 +611,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
         tc_fence_after();
         if (lane == 0) {
           const uint32_t a0 = smem_u32(smem + stage * C::STAGE_BYTES);
-          const uint32_t b0 = a0 + MG * A_BYTES;
+          const uint32_t b0 = a0 + MG * C::A_STAGE;
           for (int m = 0; m < mcnt; ++m) {
             const uint32_t d = tmem + ((kFP8 || MG == 1) ? acc * BN : m * BN);
 #pragma unroll
@@ -616,9 +623,9 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
                 mma_nvf4(d, sw128_desc(a0 + koff), sw128_desc(b0 + koff), C::kIdesc, sf + 4 * kk, sf + 16 + 8 * kk,
                          accum);
               } else if (kFP8)
-                mma_fp8(d, sw128_desc(a0 + m * A_BYTES + koff), sw128_desc(b0 + koff), C::kIdesc, accum);
+                mma_fp8(d, sw128_desc(a0 + m * C::A_STAGE + koff), sw128_desc(b0 + koff), C::kIdesc, accum);
               else
-                mma_bf16(d, sw128_desc(a0 + m * A_BYTES + koff), sw128_desc(b0 + koff), C::kIdesc, accum);
+                mma_bf16(d, sw128_desc(a0 + m * C::A_STAGE + koff), sw128_desc(b0 + koff), C::kIdesc, accum);
             }
           }
           tc_commit(&empty[stage]);
@@ -688,7 +695,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
         bool fed = true;
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!(fed = warp_wait(&full[fstage], fphase))) break;
-          const uint8_t* sSF = smem + fstage * C::STAGE_BYTES + MG * A_BYTES + 2 * B_HALF_BYTES;
+          const uint8_t* sSF = smem + fstage * C::STAGE_BYTES + MG * C::A_STAGE + 2 * B_HALF_BYTES;
           uint4 ra[4], rb[8];
 #pragma unroll
           for (int c = 0; c < 4; ++c) ra[c] = *reinterpret_cast<const uint4*>(sSF + (lane + 32 * c) * 16);
@@ -1158,7 +1165,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
   }
 }
 
-template <bool kFP8, int kKind, int kMG, int kAct, bool kHB16, bool kFP4>
+template <bool kFP8, int kKind, int kMG, int kAct, bool kHB16, bool kFP4, bool kDec>
 __global__ void __launch_bounds__(Warps<kFP8>::THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
                 const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmA_1,
@@ -1166,8 +1173,8 @@ __global__ void __launch_bounds__(Warps<kFP8>::THREADS, 1)
                 const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
                 const __grid_constant__ GemmProblems pp) {
   extern __shared__ uint8_t smem_raw[];
-  gemm_body<kFP8, kKind, kMG, kAct, kHB16, kFP4>(tmA, tmA2, tmB, tmA_1, tmA2_1, tmB_1, tmSA, tmSB, pp, smem_raw,
-                                                 true);
+  gemm_body<kFP8, kKind, kMG, kAct, kHB16, kFP4, false, kDec>(tmA, tmA2, tmB, tmA_1, tmA2_1, tmB_1, tmSA, tmSB, pp,
+                                                              smem_raw, true);
 }
 
 // Groups of MG tiles of one expert (expert, first row) and their count, from
@@ -1429,14 +1436,14 @@ struct GemmMaps {
   CUtensorMap a, a2, b, sa, sb;
 };
 
-template <bool kFP8, int kKind, int kMG, int kAct, bool kHB16 = false, bool kFP4 = false>
+template <bool kFP8, int kKind, int kMG, int kAct, bool kHB16 = false, bool kFP4 = false, bool kDec = false>
 cudaError_t launch_gemm(const GemmMaps* m, const GemmProblems& pp, int grid, cudaStream_t s) {
-  using C = Cfg<kFP8, kMG, kFP4>;
+  using C = Cfg<kFP8, kMG, kFP4, kDec>;
   static int configured[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_kernel<kFP8, kKind, kMG, kAct, kHB16, kFP4>,
+    cudaError_t e = cudaFuncSetAttribute(gemm_kernel<kFP8, kKind, kMG, kAct, kHB16, kFP4, kDec>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     if (kFP8) {
@@ -1444,30 +1451,32 @@ cudaError_t launch_gemm(const GemmMaps* m, const GemmProblems& pp, int grid, cud
       // balances only when the block launches with kLaunchRegs per thread; with fewer
       // the epilogue's increase could never be granted, so such a build never launches
       cudaFuncAttributes fa;
-      e = cudaFuncGetAttributes(&fa, gemm_kernel<kFP8, kKind, kMG, kAct, kHB16, kFP4>);
+      e = cudaFuncGetAttributes(&fa, gemm_kernel<kFP8, kKind, kMG, kAct, kHB16, kFP4, kDec>);
       if (e != cudaSuccess) return e;
       if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidConfiguration;
     }
     configured[dev] = 1;
   }
   const GemmMaps& m1 = pp.nprob > 1 ? m[1] : m[0];
-  gemm_kernel<kFP8, kKind, kMG, kAct, kHB16, kFP4><<<grid, Warps<kFP8>::THREADS, C::SMEM_BYTES, s>>>(
+  gemm_kernel<kFP8, kKind, kMG, kAct, kHB16, kFP4, kDec><<<grid, Warps<kFP8>::THREADS, C::SMEM_BYTES, s>>>(
       m[0].a, m[0].a2, m[0].b, m1.a, m1.a2, m1.b, m[0].sa, m[0].sb, pp);
   return cudaGetLastError();
 }
 
 // gemm1 with the activation chosen at run time (kHB16: fp8 mainloop, bf16 h out)
-template <bool kFP8, int kMG, bool kHB16 = false, bool kFP4 = false>
+template <bool kFP8, int kMG, bool kHB16 = false, bool kFP4 = false, bool kDec = false>
 cudaError_t launch_gemm1(int act, const GemmMaps* m, const GemmProblems& pp, int grid, cudaStream_t s) {
   switch (act) {
-    case MOE_ACT_SILU: return launch_gemm<kFP8, kGemm1, kMG, MOE_ACT_SILU, kHB16, kFP4>(m, pp, grid, s);
-    case MOE_ACT_GELU: return launch_gemm<kFP8, kGemm1, kMG, MOE_ACT_GELU, kHB16, kFP4>(m, pp, grid, s);
-    case MOE_ACT_GELU_TANH: return launch_gemm<kFP8, kGemm1, kMG, MOE_ACT_GELU_TANH, kHB16, kFP4>(m, pp, grid, s);
-    case MOE_ACT_SWIGLUOAI: return launch_gemm<kFP8, kGemm1, kMG, MOE_ACT_SWIGLUOAI, kHB16, kFP4>(m, pp, grid, s);
+    case MOE_ACT_SILU: return launch_gemm<kFP8, kGemm1, kMG, MOE_ACT_SILU, kHB16, kFP4, kDec>(m, pp, grid, s);
+    case MOE_ACT_GELU: return launch_gemm<kFP8, kGemm1, kMG, MOE_ACT_GELU, kHB16, kFP4, kDec>(m, pp, grid, s);
+    case MOE_ACT_GELU_TANH:
+      return launch_gemm<kFP8, kGemm1, kMG, MOE_ACT_GELU_TANH, kHB16, kFP4, kDec>(m, pp, grid, s);
+    case MOE_ACT_SWIGLUOAI:
+      return launch_gemm<kFP8, kGemm1, kMG, MOE_ACT_SWIGLUOAI, kHB16, kFP4, kDec>(m, pp, grid, s);
     case MOE_ACT_SILU_NO_MUL:
-      return launch_gemm<kFP8, kGemm1, kMG, MOE_ACT_SILU_NO_MUL, kHB16, kFP4>(m, pp, grid, s);
+      return launch_gemm<kFP8, kGemm1, kMG, MOE_ACT_SILU_NO_MUL, kHB16, kFP4, kDec>(m, pp, grid, s);
     case MOE_ACT_GELU_NO_MUL:
-      return launch_gemm<kFP8, kGemm1, kMG, MOE_ACT_GELU_NO_MUL, kHB16, kFP4>(m, pp, grid, s);
+      return launch_gemm<kFP8, kGemm1, kMG, MOE_ACT_GELU_NO_MUL, kHB16, kFP4, kDec>(m, pp, grid, s);
   }
   return cudaErrorInvalidValue;
 }
@@ -1623,6 +1632,10 @@ moe_status_t experts_run(const moe_experts_problem* probs, int nprob, int H, con
     mg2 = mg_for((H + 255) / 256, pr[0].I);
   }
   const bool split1 = allow_split && H / 64 >= 32, split2 = allow_split && pr[0].I / 64 >= 32;
+  // decode-sized bf16 problems (at most 32 slots each, so no tile holds more than 32 rows):
+  // the GEMMs' decode stages (32-row A boxes, six stages)
+  bool dec = !fp8;
+  for (int i = 0; i < n; ++i) dec = dec && (long long)pr[i].T * pr[i].top_k <= 32;
 
   GemmMaps maps1[kMaxProblems] = {}, maps2[kMaxProblems] = {};
   GemmProblems g1 = {}, g2 = {};
@@ -1673,8 +1686,9 @@ moe_status_t experts_run(const moe_experts_problem* probs, int nprob, int H, con
     // land in discarded output columns, zero-filled past the last expert)
     const bool b1_ok = no_mul ? make_map(&maps1[i].b, q.w13, fp8, H, (long long)E * I, 256)
                               : make_map_gate_up(&maps1[i].b, q.w13, fp8, H, I, E);
-    if (!b1_ok || !make_map(&maps1[i].a, A, fp8, H, S, 128) || !make_map(&maps1[i].a2, A, fp8, H, S, 256) ||
-        !make_map(&maps2[i].a, h, fp8, I, S, 128) || !make_map(&maps2[i].a2, h, fp8, I, S, 256) ||
+    const int a_box = dec ? 32 : 128;
+    if (!b1_ok || !make_map(&maps1[i].a, A, fp8, H, S, a_box) || !make_map(&maps1[i].a2, A, fp8, H, S, 256) ||
+        !make_map(&maps2[i].a, h, fp8, I, S, a_box) || !make_map(&maps2[i].a2, h, fp8, I, S, 256) ||
         !make_map(&maps2[i].b, q.w2, fp8, I, (long long)E * H, 256))
       return MOE_ERR_CUDA;
 
@@ -1747,11 +1761,13 @@ moe_status_t experts_run(const moe_experts_problem* probs, int nprob, int H, con
     }
     if (e == cudaSuccess) e = launch_gemm<true, kGemm2, 1, 0>(maps2, g2, grid, s);
   } else {
-    e = mg1 == 1 ? launch_gemm1<false, 1>(activation, maps1, g1, grid, s)
-                 : launch_gemm1<false, 2>(activation, maps1, g1, grid, s);
+    e = dec         ? launch_gemm1<false, 1, false, false, true>(activation, maps1, g1, grid, s)
+        : mg1 == 1 ? launch_gemm1<false, 1>(activation, maps1, g1, grid, s)
+                   : launch_gemm1<false, 2>(activation, maps1, g1, grid, s);
     if (e == cudaSuccess)
-      e = mg2 == 1 ? launch_gemm<false, kGemm2, 1, 0>(maps2, g2, grid, s)
-                   : launch_gemm<false, kGemm2, 2, 0>(maps2, g2, grid, s);
+      e = dec         ? launch_gemm<false, kGemm2, 1, 0, false, false, true>(maps2, g2, grid, s)
+          : mg2 == 1 ? launch_gemm<false, kGemm2, 1, 0>(maps2, g2, grid, s)
+                     : launch_gemm<false, kGemm2, 2, 0>(maps2, g2, grid, s);
   }
   return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
