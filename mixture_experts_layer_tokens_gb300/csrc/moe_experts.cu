@@ -1924,6 +1924,8 @@ __device__ void fused_align(const int32_t* __restrict__ ids, int S, int E, int32
   }
 }
 
+// kDec: the GEMM phases with decode stages (at most 32 slots)
+template <bool kDec>
 __global__ void __launch_bounds__(kFusedThreads, 1)
     fused_layer_kernel(const __grid_constant__ CUtensorMap g1a, const __grid_constant__ CUtensorMap g1b,
                        const __grid_constant__ CUtensorMap g1a_s, const __grid_constant__ CUtensorMap g1b_s,
@@ -1996,12 +1998,12 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
   // the expert GEMMs (the routed experts and the shared expert in the same units)
   // (after a failed phase the tile maps may be unset: the GEMMs are skipped)
   if (!status_failed())
-    gemm_body<false, kGemm1, 1, MOE_ACT_SILU, false, false, true>(g1a, g1a, g1b, g1a_s, g1a_s, g1b_s, g1a, g1a, pp1,
-                                                                  smem_raw, false);
+    gemm_body<false, kGemm1, 1, MOE_ACT_SILU, false, false, true, kDec>(g1a, g1a, g1b, g1a_s, g1a_s, g1b_s, g1a, g1a,
+                                                                        pp1, smem_raw, false);
   grid_barrier(fp.grid_ctr, ++bar);
   if (!status_failed())
-    gemm_body<false, kGemm2, 1, MOE_ACT_SILU, false, false, true>(g2a, g2a, g2b, g2a_s, g2a_s, g2b_s, g2a, g2a, pp2,
-                                                                  smem_raw, false);
+    gemm_body<false, kGemm2, 1, MOE_ACT_SILU, false, false, true, kDec>(g2a, g2a, g2b, g2a_s, g2a_s, g2b_s, g2a, g2a,
+                                                                        pp2, smem_raw, false);
   grid_barrier(fp.grid_ctr, ++bar);
 
   // finalize: one CTA per token; sums in fp32 (the weighted expert rows, the shared row,
@@ -2676,12 +2678,16 @@ extern "C" moe_status_t moe_layer_fused(const float* logits, const void* a1, int
 
   // tensor maps: gemm1 reads the gathered rows and w13 (the shared expert: a1 and its
   // w13), gemm2 the intermediates and w2
+  // (at most 32 slots: the decode stages, 32-row A boxes)
+  const bool dec = S <= 32;
+  const int a_box = dec ? 32 : 128;
   GemmMaps m1[2] = {}, m2[2] = {};
-  if (!make_map(&m1[0].a, fp.A, false, H, S, 128) || !make_map_gate_up(&m1[0].b, w13, false, H, I, E) ||
-      !make_map(&m2[0].a, h, false, I, S, 128) || !make_map(&m2[0].b, w2, false, I, (long long)E * H, 256))
+  if (!make_map(&m1[0].a, fp.A, false, H, S, a_box) || !make_map_gate_up(&m1[0].b, w13, false, H, I, E) ||
+      !make_map(&m2[0].a, h, false, I, S, a_box) || !make_map(&m2[0].b, w2, false, I, (long long)E * H, 256))
     return MOE_ERR_CUDA;
-  if (shared && (!make_map(&m1[1].a, a1, false, H, T, 128) || !make_map_gate_up(&m1[1].b, shared_w13, false, H, I, 1) ||
-                 !make_map(&m2[1].a, hs, false, I, T, 128) || !make_map(&m2[1].b, shared_w2, false, I, H, 256)))
+  if (shared &&
+      (!make_map(&m1[1].a, a1, false, H, T, a_box) || !make_map_gate_up(&m1[1].b, shared_w13, false, H, I, 1) ||
+       !make_map(&m2[1].a, hs, false, I, T, a_box) || !make_map(&m2[1].b, shared_w2, false, I, H, 256)))
     return MOE_ERR_CUDA;
   if (!shared) {
     m1[1] = m1[0];
@@ -2721,15 +2727,16 @@ extern "C" moe_status_t moe_layer_fused(const float* logits, const void* a1, int
     q1.unit_ctr = i == 0 ? reinterpret_cast<int*>(wsb + L.ctr) + 1 : nullptr;
     q2.unit_ctr = i == 0 ? reinterpret_cast<int*>(wsb + L.ctr) + 2 : nullptr;
   }
-  static int configured[64] = {0};
+  static int configured[2][64] = {{0}};
   void (*kern)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap,
-               CUtensorMap, GemmProblems, GemmProblems, FusedParams) = fused_layer_kernel;
-  const int smem = Cfg<false, 1>::SMEM_BYTES;
-  if (dev < 64 && !configured[dev]) {
+               CUtensorMap, GemmProblems, GemmProblems, FusedParams) =
+      dec ? fused_layer_kernel<true> : fused_layer_kernel<false>;
+  const int smem = dec ? Cfg<false, 1, false, true>::SMEM_BYTES : Cfg<false, 1>::SMEM_BYTES;
+  if (dev < 64 && !configured[dec][dev]) {
     if (cudaFuncSetAttribute(reinterpret_cast<const void*>(kern), cudaFuncAttributeMaxDynamicSharedMemorySize,
                              smem) != cudaSuccess)
       return MOE_ERR_CUDA;
-    configured[dev] = 1;
+    configured[dec][dev] = 1;
   }
   // the barrier counter and the split flags start at zero
   if (cudaMemsetAsync(wsb + L.ctr, 0, L.ctl_end - L.ctr, s) != cudaSuccess) return MOE_ERR_CUDA;

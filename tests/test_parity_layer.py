@@ -101,6 +101,10 @@ SMALL = {
     # with and without the shared expert, residual and RMSNorm
     "llama_small_single": scaled(CONFIGS["llama8_fused"], T=100, H=384, I=512, shared_I=512),
     "llama_small_single_T1": scaled(CONFIGS["llama1_fused"], H=2048, I=2048, shared_I=2048),
+    # at most 32 slots (decode stages: 32-row A boxes) with residual and RMSNorm
+    "llama_small_single_T24": scaled(CONFIGS["llama8_fused"], T=24, H=1024, I=1024, shared_I=1024, residual=True,
+                                     rms=True),
+    "llama_small_fused_T24": scaled(CONFIGS["llama8"], T=24, H=1024, I=1024, shared_I=1024),
     "mixtral_small_single": scaled(CONFIGS["mixtral_fused"], T=200, H=512, I=768),
     "residual_rms_single": scaled(CONFIGS["mixtral_fused"], T=64, H=256, I=256, residual=True, rms=True),
     # the single launch's limits: E = 256 with top-8 (eight logits per lane, many small experts),
@@ -154,11 +158,12 @@ def test_layer_full_size_sampled_tokens(cuda_dev, name, sample):
         assert int(layer.al.expert_offsets[-1]) == cfg.T * cfg.top_k
 
 
-def test_single_launch_matches_the_separate_calls(cuda_dev):
+@pytest.mark.parametrize("T", [40, 20])  # 20 slots: both sides with the decode stages
+def test_single_launch_matches_the_separate_calls(cuda_dev, T):
     """The one-launch step routes exactly like moe_route and, its GEMMs being the same
     units in the same order, gives the separate calls' output up to the finalize's fp32
     summation order."""
-    cfg = scaled(CONFIGS["llama8_fused"], T=40, H=1024, I=1024, shared_I=1024, residual=True, rms=True)
+    cfg = scaled(CONFIGS["llama8_fused"], T=T, H=1024, I=1024, shared_I=1024, residual=True, rms=True)
     inp = make_inputs(cfg, device=cuda_dev)
     single = MoELayer(inp)
     sep = MoELayer(make_inputs(scaled(cfg, single_launch=False), device=cuda_dev))
