@@ -133,16 +133,18 @@ constexpr int SFB_BYTES = 2 * 128 * 16;
 constexpr int SF_TMEM_BASE = 256;
 constexpr int SF_TMEM_STAGE = 4 * 4 + 4 * 8;
 
-// kDec: decode-sized bf16 problems (at most 32 rows per tile, i.e. T <= 32): a stage holds
-// the first 32 rows of the A tile (a 32-row box; the MMA still reads 128 rows, the last 96
-// from the weight tile beside them, and their accumulator lanes are never read) and the
-// 12 KB saved per stage buy two more stages, so each SM has half as many weight bytes again
-// in flight and spends a quarter less of its copy bandwidth on padding rows.
+// kDec: decode-sized problems (at most 32 rows per tile): a stage holds the first 32 rows of
+// the A tile (a 32-row box; the MMA still reads 128 rows, the last 96 from the weight tile
+// beside them, and their accumulator lanes are never read) and the 12 KB saved per stage buy
+// more stages (bf16: six instead of four; NVFP4: five, whose 32-row A scale boxes leave the
+// other 96 rows' scale words stale, for rows never read either), so each SM has more weight
+// bytes in flight and spends less of its copy bandwidth on padding rows.
 template <bool kFP8, int kMG, bool kFP4 = false, bool kDec = false>
 struct Cfg {
   static constexpr int MG = kMG;  // M tiles per unit
   static constexpr int A_STAGE = kDec ? A_BYTES / 4 : A_BYTES;  // A bytes per M tile in a stage
-  static constexpr int STAGES = kDec ? 6 : (kMG == 2 ? 3 : 4);
+  static constexpr int STAGES = kDec ? (kFP4 ? 5 : 6) : (kMG == 2 ? 3 : 4);
+  static constexpr int SFA_LOAD = kDec ? SFA_BYTES / 4 : SFA_BYTES;  // NVFP4: A scale bytes copied per stage
   static constexpr int STAGE_BYTES = MG * A_STAGE + 2 * B_HALF_BYTES + (kFP4 ? SFA_BYTES + SFB_BYTES : 0);
   static constexpr int kBK = kFP4 ? 2 * BKB : (kFP8 ? BKB : BKB / 2);  // K elements per stage
   static constexpr int kMapK = kFP4 ? BKB : kBK;  // the same in units of the tensor maps' elements
@@ -161,7 +163,7 @@ struct Cfg {
                                     OUT_STAGE_BYTES +
                                     1024 /*align*/;
   static_assert(!kFP4 || (!kFP8 && kMG == 1), "NVFP4 units hold one M tile");
-  static_assert(!kDec || (!kFP8 && !kFP4 && kMG == 1), "decode stages: bf16 units of one tile");
+  static_assert(!kDec || (!kFP8 && kMG == 1), "decode stages: bf16 or NVFP4 units of one tile");
   static_assert(!kFP4 || SF_TMEM_BASE + STAGES * SF_TMEM_STAGE <= TMEM_COLS, "NVFP4 scales must fit the TMEM");
 };
 
@@ -550,7 +552,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
           uint8_t* sA = smem + stage * C::STAGE_BYTES;
           uint8_t* sB = sA + MG * C::A_STAGE;
           mbar_arrive_expect_tx(&full[stage],
-                                mcnt * C::A_STAGE + 2 * B_HALF_BYTES + (kFP4 ? SFA_BYTES + SFB_BYTES : 0));
+                                mcnt * C::A_STAGE + 2 * B_HALF_BYTES + (kFP4 ? C::SFA_LOAD + SFB_BYTES : 0));
           const int kx = kb * C::kMapK;
           if (kFP4) {
             // the block scales of the stage: 16 bytes of each A row and of each weight row
@@ -2397,14 +2399,17 @@ moe_status_t experts_nvfp4_run(const void* a1q, const void* a1q_sf, const float*
   uint8_t* hq = wsb + L.hq;
   uint8_t* hsf = wsb + L.hsf;
   // packed operands are uint8 maps over rows of K/2 bytes; scale rows are K/16 bytes
+  // (at most 32 slots: the decode stages, 32-row A and A-scale boxes)
+  const bool dec = S <= 32;
+  const int a_box = dec ? 32 : 128;
   GemmMaps m1 = {}, m2 = {};
   const bool b1 = no_mul ? make_map(&m1.b, w13, true, H / 2, (long long)E * I, 256)
                          : make_map_gate_up(&m1.b, w13, true, H / 2, I, E);
   const bool sb1 = no_mul ? make_map_sf(&m1.sb, w13_sf, H / 16, (long long)E * I, 256)
                           : make_map_sf_gate_up(&m1.sb, w13_sf, H / 16, I, E);
-  if (!b1 || !sb1 || !make_map(&m1.a, A, true, H / 2, S, 128) || !make_map(&m1.a2, A, true, H / 2, S, 128) ||
-      !make_map_sf(&m1.sa, ASF, H / 16, S, 128) || !make_map(&m2.a, hq, true, I / 2, S, 128) ||
-      !make_map(&m2.a2, hq, true, I / 2, S, 128) || !make_map_sf(&m2.sa, hsf, I / 16, S, 128) ||
+  if (!b1 || !sb1 || !make_map(&m1.a, A, true, H / 2, S, a_box) || !make_map(&m1.a2, A, true, H / 2, S, 128) ||
+      !make_map_sf(&m1.sa, ASF, H / 16, S, a_box) || !make_map(&m2.a, hq, true, I / 2, S, a_box) ||
+      !make_map(&m2.a2, hq, true, I / 2, S, 128) || !make_map_sf(&m2.sa, hsf, I / 16, S, a_box) ||
       !make_map(&m2.b, w2, true, I / 2, (long long)E * H, 256) ||
       !make_map_sf(&m2.sb, w2_sf, I / 16, (long long)E * H, 256))
     return MOE_ERR_CUDA;
@@ -2438,7 +2443,8 @@ moe_status_t experts_nvfp4_run(const void* a1q, const void* a1q_sf, const float*
   p2.flags = flags + L.nflags1;
   p2.allow_split = split2;
 
-  cudaError_t e = launch_gemm1<false, 1, false, true>(activation, &m1, g1, grid, s);
+  cudaError_t e = dec ? launch_gemm1<false, 1, false, true, true>(activation, &m1, g1, grid, s)
+                      : launch_gemm1<false, 1, false, true>(activation, &m1, g1, grid, s);
   if (e == cudaSuccess) {
     const long long groups = S * (I / 16);
     nvfp4_quant_kernel<<<(unsigned)((groups + 255) / 256), 256, 0, s>>>(static_cast<const __nv_bfloat16*>(hb), I, S,
@@ -2446,7 +2452,9 @@ moe_status_t experts_nvfp4_run(const void* a1q, const void* a1q_sf, const float*
                                                                         hsf);
     e = cudaGetLastError();
   }
-  if (e == cudaSuccess) e = launch_gemm<false, kGemm2, 1, 0, false, true>(&m2, g2, grid, s);
+  if (e == cudaSuccess)
+    e = dec ? launch_gemm<false, kGemm2, 1, 0, false, true, true>(&m2, g2, grid, s)
+            : launch_gemm<false, kGemm2, 1, 0, false, true>(&m2, g2, grid, s);
   return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
